@@ -1,0 +1,202 @@
+/*
+ * mxfp8.h - C ABI of the GB300 (sm_103a) MXFP8 quantizer and block-scaled GEMMs.
+ *
+ * The method: "End-to-End MXFP8 RL on Blackwell: What Matching Buys, When It Pays Off,
+ * and How It Fails" (verl blog post). Section "The pipeline", paragraph "The format":
+ * MXFP8 is the OCP microscaling FP8 format - E4M3 elements in blocks of 32 along the
+ * reduction dimension, each block sharing one power-of-two E8M0 scale. The learner
+ * paragraph of the same section: each linear layer runs three GEMMs (forward, data
+ * gradient, weight gradient) on quantized operands, some quantized along the token
+ * dimension, with token counts padded to multiples of 32. The weight-synchronization
+ * paragraph: the synced weights are the forward GEMM's weight quantization, byte for
+ * byte. Section "Where the time goes": scales are rearranged into the layout the GEMM
+ * reads; here the quantizer writes that layout directly.
+ *
+ * Conventions shared by every call:
+ *  - Pointers named *_dev are device pointers; the caller allocates and owns every
+ *    buffer. The library allocates no device memory in any call. Its only state is a
+ *    per-device status word (see mxfp8_get_device_status) and per-device capability
+ *    flags, set up on the first call on each device.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Every compute call only enqueues work on `stream` and returns; none synchronizes
+ *    except mxfp8_get_device_status.
+ *  - Return value: an mxfp8_status. Arguments are checked on the host before anything
+ *    is enqueued; a failed check returns its code and enqueues nothing. Errors found
+ *    by a kernel (bad expert offsets, a pipeline wait that ran out) are latched in the
+ *    device status word and read with mxfp8_get_device_status. No call throws.
+ *  - Matrices are row-major with packed rows (leading dimension = number of columns).
+ *    BF16 and E4M3 tensors must start on a 16-byte boundary, scale tensors too.
+ *  - Quantization rule (OCP, floor form): per block of 32, e = max(-127,
+ *    floor(log2 amax) - 8); scale byte = e + 127; element = E4M3(v * 2^-e), round to
+ *    nearest even, saturating at +-448, sign of zero kept. A block holding a NaN or an
+ *    infinity gets scale 0xFF and every element 0x7F | (its sign bit).
+ *  - Scale layouts. LINEAR: scales [S_rows][S_cols] row-major, one byte per block.
+ *    SWIZZLED: the tensor cores' 128 x 4 tiles - byte offset of scale (r, c) is
+ *    ((r / 128) * ceil(S_cols / 4) + c / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4
+ *    + (c % 4); the padding bytes of partial tiles are written as 0x00. The GEMMs read
+ *    SWIZZLED scales only.
+ */
+#ifndef MXFP8_H_
+#define MXFP8_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MXFP8_ABI_VERSION 1
+
+typedef enum mxfp8_status {
+  MXFP8_OK = 0,
+  MXFP8_ERR_INVALID_ARG = 1,      /* null pointer, negative or unsupported size/enum */
+  MXFP8_ERR_ALIGNMENT = 2,        /* a blocked dim not a multiple of 32, or a pointer
+                                     not 16-byte aligned */
+  MXFP8_ERR_UNSUPPORTED_ARCH = 3, /* current device is not compute capability 10.3 */
+  MXFP8_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed */
+  MXFP8_ERR_BAD_OFFSETS = 5,      /* (device) expert offsets not 0-based, non-decreasing,
+                                     32-aligned and ending at total_rows */
+  MXFP8_ERR_TIMEOUT = 6           /* (device) a pipeline wait in a kernel ran out; the
+                                     kernel abandoned its work */
+} mxfp8_status;
+
+typedef enum mxfp8_axis {
+  MXFP8_AXIS_ROW = 0, /* blocks along the contiguous (last) dim: out [rows][cols] */
+  MXFP8_AXIS_COL = 1  /* blocks along the first dim, emitted transposed: out [cols][rows] */
+} mxfp8_axis;
+
+typedef enum mxfp8_scale_layout {
+  MXFP8_SCALES_LINEAR = 0,
+  MXFP8_SCALES_SWIZZLED = 1
+} mxfp8_scale_layout;
+
+typedef enum mxfp8_op {
+  MXFP8_OP_FPROP = 0, /* Y  = X  . W^T   A = X  rows,  B = W  rows          */
+  MXFP8_OP_DGRAD = 1, /* dX = dY . W     A = dY rows,  B = W  cols (= W^T)  */
+  MXFP8_OP_WGRAD = 2  /* dW = dY^T . X   A = dY cols,  B = X  cols (tokens) */
+} mxfp8_op;
+
+typedef enum mxfp8_out_dtype {
+  MXFP8_OUT_BF16 = 0,
+  MXFP8_OUT_FP32 = 1
+} mxfp8_out_dtype;
+
+/* ABI version of the loaded library (MXFP8_ABI_VERSION). */
+int mxfp8_version(void);
+
+/* Static text for a status code; never NULL. */
+const char* mxfp8_status_string(int status);
+
+/*
+ * Bytes of the scale tensor that mxfp8_quantize writes for a [rows][cols] BF16 input.
+ * S_rows x S_cols = rows x cols/32 (ROW) or cols x rows/32 (COL); LINEAR is
+ * S_rows * S_cols bytes, SWIZZLED is ceil(S_rows/128) * ceil(S_cols/4) * 512 bytes.
+ * Returns 0 for invalid arguments (negative sizes, a blocked dim not a multiple of 32,
+ * unknown enums).
+ */
+size_t mxfp8_scale_bytes(int64_t rows, int64_t cols, int axis, int scale_layout);
+
+/*
+ * MXFP8-quantize a BF16 matrix ("The pipeline" - "The format"; column-wise copies for
+ * the weight-gradient GEMM: the learner paragraph).
+ *   src_dev      BF16 [rows][cols], read only.
+ *   axis ROW     requires cols % 32 == 0; out_dev E4M3 [rows][cols]; scales for
+ *                [rows][cols/32].
+ *   axis COL     requires rows % 32 == 0 and cols % 8 == 0; out_dev E4M3 [cols][rows]
+ *                (the transpose, blocked along its contiguous dim); scales for
+ *                [cols][rows/32].
+ *   scales_dev   mxfp8_scale_bytes(rows, cols, axis, scale_layout) bytes, written in
+ *                full (padding included).
+ * rows == 0 or cols == 0 is a no-op. Deterministic: the same input gives the same bytes
+ * from every call, which is what makes the synchronized weights equal the forward
+ * weights byte for byte (section "The grid, byte for byte").
+ */
+int mxfp8_quantize(const void* src_dev, int64_t rows, int64_t cols, int axis,
+                   void* out_dev, void* scales_dev, int scale_layout, void* stream);
+
+/*
+ * `batch` independent matrices [batch][rows][cols] quantized as by mxfp8_quantize, each
+ * with its own scale block of mxfp8_scale_bytes(rows, cols, axis, layout) bytes; the
+ * scale blocks are concatenated in batch order. Used for per-expert MoE weights.
+ */
+int mxfp8_quantize_batched(const void* src_dev, int64_t batch, int64_t rows, int64_t cols,
+                           int axis, void* out_dev, void* scales_dev, int scale_layout,
+                           void* stream);
+
+/*
+ * Capacity (bytes) to allocate for the scales of mxfp8_quantize_grouped on a
+ * [total_rows][cols] input split into at most num_experts token segments. It is an
+ * upper bound that needs no expert counts on the host:
+ *   ROW: (ceil(total_rows/128) + num_experts) * ceil(cols/128) * 512
+ *   COL: ceil(cols/128) * (ceil(total_rows/128) + num_experts) * 512
+ * Returns 0 for invalid arguments.
+ */
+size_t mxfp8_grouped_scale_bytes(int64_t total_rows, int64_t cols, int num_experts, int axis);
+
+/*
+ * MXFP8-quantize a token-segmented (MoE) BF16 matrix [total_rows][cols]; expert e owns
+ * rows [off[e], off[e+1]) (section "A held-out workload, and end to end", Table 4).
+ *   expert_offsets_dev  int32 [num_experts + 1] on the device: off[0] = 0,
+ *                       non-decreasing, multiples of 32, off[E] = total_rows. Checked
+ *                       on the device; a violation latches MXFP8_ERR_BAD_OFFSETS and
+ *                       the scales are left unspecified.
+ *   axis ROW  out_dev [total_rows][cols] (cols % 32 == 0); scales: expert e's SWIZZLED
+ *             block for its [cnt_e][cols/32] scales, rows padded to 128.
+ *   axis COL  out_dev [cols][total_rows] (cols % 8 == 0); scales: expert e's SWIZZLED
+ *             block for its [cols][cnt_e/32] scales, token blocks padded to 4.
+ *   Blocks are concatenated in expert order (empty experts take no bytes) inside
+ *   scales_dev, whose capacity is mxfp8_grouped_scale_bytes(...); bytes past the last
+ *   block are not written. The element bytes equal those of mxfp8_quantize.
+ */
+int mxfp8_quantize_grouped(const void* src_dev, int64_t total_rows, int64_t cols, int axis,
+                           const int32_t* expert_offsets_dev, int num_experts,
+                           void* out_dev, void* scales_dev, void* stream);
+
+/*
+ * Block-scaled GEMM on tcgen05 (kind::mxf8f6f4, E4M3 x E4M3, UE8M0 scales, FP32
+ * accumulation): C[M][N] = sum_k deq(A)[m][k] * deq(B)[n][k] ("The pipeline", learner
+ * paragraph: the three GEMMs of a linear layer).
+ *   A_dev, sA_dev  E4M3 [M][K] and its SWIZZLED scales (rows M, K/32 blocks);
+ *   B_dev, sB_dev  E4M3 [N][K] and its SWIZZLED scales (rows N, K/32 blocks);
+ *   C_dev          [M][N], BF16 or FP32 (out_dtype), fully overwritten.
+ * Both operands are K-major ("TN"); `op` names which quantized copies are passed
+ * (see mxfp8_op) and does not change the arithmetic. Requires K % 32 == 0,
+ * M % 16 == 0 and N % 16 == 0 (M, N, K > 0). Accuracy: |C - C_exact| <=
+ * 2^-9 * sum_k |a_k b_k| per element before the output rounding.
+ */
+int mxfp8_gemm(const void* A_dev, const void* sA_dev, const void* B_dev, const void* sB_dev,
+               void* C_dev, int64_t M, int64_t N, int64_t K, int op, int out_dtype,
+               void* stream);
+
+/*
+ * Grouped (MoE expert) block-scaled GEMMs over token segments off[e] .. off[e+1]
+ * (expert_offsets_dev as for mxfp8_quantize_grouped).
+ *   op FPROP / DGRAD:  A [total_rows][K] with grouped ROW scales (one block per expert,
+ *                      as written by mxfp8_quantize_grouped ROW); B [E][N][K] with
+ *                      batched SWIZZLED scales (mxfp8_quantize_batched); C
+ *                      [total_rows][N]: rows of expert e get A_e . B[e]^T. C rows of
+ *                      no expert (none when off[E] = total_rows) are not written.
+ *   op WGRAD:          A [N][total_rows] and B [K][total_rows] (column-wise copies,
+ *                      grouped COL scales); C [E][N][K], C[e] = A[:, seg e] .
+ *                      B[:, seg e]^T; an expert with no tokens gets C[e] = 0.
+ * Requires K % 32 == 0, N % 16 == 0, total_rows % 32 == 0, and for WGRAD K % 16 == 0.
+ */
+int mxfp8_grouped_gemm(const void* A_dev, const void* sA_dev, const void* B_dev,
+                       const void* sB_dev, void* C_dev, const int32_t* expert_offsets_dev,
+                       int num_experts, int64_t total_rows, int64_t N, int64_t K, int op,
+                       int out_dtype, void* stream);
+
+/*
+ * Synchronizes `stream`, then returns and clears the current device's status word:
+ * MXFP8_OK, or the first device-side error latched since the last call
+ * (MXFP8_ERR_BAD_OFFSETS, MXFP8_ERR_TIMEOUT), or MXFP8_ERR_CUDA if the synchronization
+ * itself failed.
+ */
+int mxfp8_get_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP8_H_ */

@@ -1,0 +1,212 @@
+"""GB300-native MXFP8 quantizer and block-scaled GEMMs - Python binding.
+
+Argument marshalling only: every call goes through the C ABI of ``libmxfp8.so``
+(``include/mxfp8.h``), whose kernels do all of the work on the GPU. PyTorch provides
+device memory and the current CUDA stream. There is no CPU fallback: if the library is
+not built, or the device is not sm_103a, calls raise.
+
+Method: "End-to-End MXFP8 RL on Blackwell" (verl blog post), section "The pipeline"
+(paragraph "The format" and the learner and weight-synchronization paragraphs).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+ROW, COL = 0, 1
+LINEAR, SWIZZLED = 0, 1
+FPROP, DGRAD, WGRAD = 0, 1, 2
+OUT_BF16, OUT_FP32 = 0, 1
+
+OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED_ARCH, ERR_CUDA, ERR_BAD_OFFSETS, \
+    ERR_TIMEOUT = range(7)
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp8.so")
+
+# every symbol include/mxfp8.h declares: (name, restype, argtypes)
+_P, _I64, _I, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "mxfp8_version": (_I, []),
+    "mxfp8_status_string": (ctypes.c_char_p, [_I]),
+    "mxfp8_scale_bytes": (_SZ, [_I64, _I64, _I, _I]),
+    "mxfp8_grouped_scale_bytes": (_SZ, [_I64, _I64, _I, _I]),
+    "mxfp8_quantize": (_I, [_P, _I64, _I64, _I, _P, _P, _I, _P]),
+    "mxfp8_quantize_batched": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _I, _P]),
+    "mxfp8_quantize_grouped": (_I, [_P, _I64, _I64, _I, _P, _I, _P, _P, _P]),
+    "mxfp8_gemm": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _P]),
+    "mxfp8_grouped_gemm": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _P]),
+    "mxfp8_get_device_status": (_I, [_P]),
+}
+
+_lib = None
+
+
+class MXFP8Error(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = lib().mxfp8_status_string(status).decode()
+        super().__init__(f"{what}: {msg} (status {status})" if what else msg)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C-ABI library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                "g.build()\"` (nvcc, sm_103a). There is no CPU fallback.")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise MXFP8Error(status, what)
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: torch.Tensor):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _require(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ------------------------------------------------------------------------- quantizer
+
+def scale_bytes(rows: int, cols: int, axis: int = ROW, layout: int = SWIZZLED) -> int:
+    n = lib().mxfp8_scale_bytes(rows, cols, axis, layout)
+    if n == 0 and rows * cols != 0:
+        raise ValueError(f"no scale layout for rows={rows} cols={cols} axis={axis}")
+    return n
+
+
+def grouped_scale_bytes(total_rows: int, cols: int, num_experts: int, axis: int = ROW) -> int:
+    return lib().mxfp8_grouped_scale_bytes(total_rows, cols, num_experts, axis)
+
+
+def quantize(src: torch.Tensor, axis: int = ROW, layout: int = SWIZZLED, out=None, scales=None,
+             stream=None):
+    """MXFP8-quantize a BF16 [rows, cols] CUDA tensor. Returns (E4M3 codes as uint8, E8M0
+    scale bytes as uint8): codes [rows, cols] (ROW) or [cols, rows] (COL); scales flat
+    (SWIZZLED) or [S_rows, S_cols] (LINEAR)."""
+    _require(src, torch.bfloat16, "src")
+    rows, cols = src.shape
+    oshape = (rows, cols) if axis == ROW else (cols, rows)
+    if out is None:
+        out = torch.empty(oshape, dtype=torch.uint8, device=src.device)
+    if scales is None:
+        nb = scale_bytes(rows, cols, axis, layout)
+        if layout == LINEAR:
+            s_rows, s_cols = (rows, cols // 32) if axis == ROW else (cols, rows // 32)
+            scales = torch.empty((s_rows, s_cols), dtype=torch.uint8, device=src.device)
+        else:
+            scales = torch.empty(nb, dtype=torch.uint8, device=src.device)
+    _check(lib().mxfp8_quantize(_ptr(src), rows, cols, axis, _ptr(out), _ptr(scales), layout,
+                                _stream(stream)), "mxfp8_quantize")
+    return out, scales
+
+
+def quantize_batched(src: torch.Tensor, axis: int = ROW, layout: int = SWIZZLED, out=None,
+                     scales=None, stream=None):
+    """Quantize each of `batch` BF16 matrices [batch, rows, cols] independently; scale
+    blocks concatenated in batch order."""
+    _require(src, torch.bfloat16, "src")
+    batch, rows, cols = src.shape
+    oshape = (batch, rows, cols) if axis == ROW else (batch, cols, rows)
+    if out is None:
+        out = torch.empty(oshape, dtype=torch.uint8, device=src.device)
+    if scales is None:
+        scales = torch.empty(batch * scale_bytes(rows, cols, axis, layout), dtype=torch.uint8,
+                             device=src.device)
+    _check(lib().mxfp8_quantize_batched(_ptr(src), batch, rows, cols, axis, _ptr(out),
+                                        _ptr(scales), layout, _stream(stream)),
+           "mxfp8_quantize_batched")
+    return out, scales
+
+
+def quantize_grouped(src: torch.Tensor, offsets: torch.Tensor, axis: int = ROW, out=None,
+                     scales=None, stream=None):
+    """Quantize a token-segmented BF16 [total_rows, cols] tensor (expert e owns rows
+    offsets[e]..offsets[e+1], int32 CUDA tensor); per-expert swizzled scale blocks."""
+    _require(src, torch.bfloat16, "src")
+    _require(offsets, torch.int32, "offsets")
+    total, cols = src.shape
+    e = offsets.numel() - 1
+    oshape = (total, cols) if axis == ROW else (cols, total)
+    if out is None:
+        out = torch.empty(oshape, dtype=torch.uint8, device=src.device)
+    if scales is None:
+        scales = torch.empty(grouped_scale_bytes(total, cols, e, axis), dtype=torch.uint8,
+                             device=src.device)
+    _check(lib().mxfp8_quantize_grouped(_ptr(src), total, cols, axis, _ptr(offsets), e,
+                                        _ptr(out), _ptr(scales), _stream(stream)),
+           "mxfp8_quantize_grouped")
+    return out, scales
+
+
+# ----------------------------------------------------------------------------- GEMMs
+
+def gemm(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.Tensor, op: int = FPROP,
+         out_dtype: int = OUT_BF16, out=None, stream=None) -> torch.Tensor:
+    """C[M, N] = deq(A)[M, K] . deq(B)[N, K]^T with swizzled scales (both K-major)."""
+    _require(a, torch.uint8, "A")
+    _require(b, torch.uint8, "B")
+    m, k = a.shape
+    n, k2 = b.shape
+    if k != k2:
+        raise ValueError(f"K mismatch: {k} vs {k2}")
+    if out is None:
+        dt = torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32
+        out = torch.empty((m, n), dtype=dt, device=a.device)
+    _check(lib().mxfp8_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out), m, n, k, op,
+                            out_dtype, _stream(stream)), "mxfp8_gemm")
+    return out
+
+
+def grouped_gemm(a, sa, b, sb, offsets: torch.Tensor, op: int = FPROP,
+                 out_dtype: int = OUT_BF16, out=None, stream=None) -> torch.Tensor:
+    """Grouped expert GEMMs (see mxfp8_grouped_gemm). FPROP/DGRAD: a [T, K], b [E, N, K]
+    -> [T, N]. WGRAD: a [N, T], b [K, T] -> [E, N, K]."""
+    _require(a, torch.uint8, "A")
+    _require(b, torch.uint8, "B")
+    _require(offsets, torch.int32, "offsets")
+    e = offsets.numel() - 1
+    dt = torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32
+    if op == WGRAD:
+        n_, total = a.shape
+        k_ = b.shape[0]
+        shape = (e, n_, k_)
+    else:
+        total, k_ = a.shape
+        n_ = b.shape[1]
+        shape = (total, n_)
+    if out is None:
+        out = torch.empty(shape, dtype=dt, device=a.device)
+    _check(lib().mxfp8_grouped_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out),
+                                    _ptr(offsets), e, total, n_, k_, op, out_dtype,
+                                    _stream(stream)), "mxfp8_grouped_gemm")
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronizes the stream and returns-and-clears the device status word."""
+    return lib().mxfp8_get_device_status(_stream(stream))

@@ -1,0 +1,246 @@
+// api.cu - the extern "C" boundary (include/mxfp8.h): argument checks, per-device
+// set-up (architecture check, SM count, status word) and dispatch to the launchers.
+
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "mxfp8.h"
+
+namespace mxfp8 {
+
+namespace {
+
+// First error a kernel detected on this device since the host last read it.
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  int sms = 0;
+  int* status = nullptr;
+};
+
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+// Per-device set-up on first use: capability 10.3 (GB300) required, SM count cached,
+// address of the status word looked up. Returns MXFP8_OK or an error code.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MXFP8_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MXFP8_ERR_CUDA;
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!d.ready) {
+      int major = 0, minor = 0, sms = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return MXFP8_ERR_CUDA;
+      d.supported = (major == 10 && minor == 3);
+      d.sms = sms;
+      if (d.supported) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return MXFP8_ERR_CUDA;
+        d.status = static_cast<int*>(p);
+      }
+      d.ready = true;
+    }
+  }
+  if (!d.supported) return MXFP8_ERR_UNSUPPORTED_ARCH;
+  *out = &d;
+  return MXFP8_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+constexpr int64_t kMaxTokenTiles = 65535;  // grid.y limit of the quantizer launch
+
+}  // namespace
+
+int num_sms() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return (dev >= 0 && dev < kMaxDevices && g_dev[dev].sms > 0) ? g_dev[dev].sms : 148;
+}
+
+int64_t scale_bytes_host(int64_t rows, int64_t cols, int axis, int layout) {
+  if (rows < 0 || cols < 0) return -1;
+  int64_t s_rows, s_cols;
+  if (axis == MXFP8_AXIS_ROW) {
+    if (cols % 32) return -1;
+    s_rows = rows;
+    s_cols = cols / 32;
+  } else if (axis == MXFP8_AXIS_COL) {
+    if (rows % 32) return -1;
+    s_rows = cols;
+    s_cols = rows / 32;
+  } else {
+    return -1;
+  }
+  if (layout == MXFP8_SCALES_LINEAR) return s_rows * s_cols;
+  if (layout == MXFP8_SCALES_SWIZZLED) {
+    if (s_rows == 0 || s_cols == 0) return 0;
+    return cdiv(s_rows, 128) * cdiv(s_cols, 4) * 512;
+  }
+  return -1;
+}
+
+}  // namespace mxfp8
+
+using namespace mxfp8;
+
+extern "C" {
+
+int mxfp8_version(void) { return MXFP8_ABI_VERSION; }
+
+const char* mxfp8_status_string(int status) {
+  switch (status) {
+    case MXFP8_OK: return "ok";
+    case MXFP8_ERR_INVALID_ARG: return "invalid argument";
+    case MXFP8_ERR_ALIGNMENT: return "alignment: blocked dim not a multiple of 32 or pointer not 16-byte aligned";
+    case MXFP8_ERR_UNSUPPORTED_ARCH: return "unsupported device (needs compute capability 10.3, sm_103a)";
+    case MXFP8_ERR_CUDA: return "CUDA call failed";
+    case MXFP8_ERR_BAD_OFFSETS: return "expert offsets invalid (must be 0-based, non-decreasing, 32-aligned, end at total_rows)";
+    case MXFP8_ERR_TIMEOUT: return "a kernel pipeline wait timed out; its work was abandoned";
+    default: return "unknown status";
+  }
+}
+
+size_t mxfp8_scale_bytes(int64_t rows, int64_t cols, int axis, int scale_layout) {
+  const int64_t b = scale_bytes_host(rows, cols, axis, scale_layout);
+  return b < 0 ? 0 : static_cast<size_t>(b);
+}
+
+size_t mxfp8_grouped_scale_bytes(int64_t total_rows, int64_t cols, int num_experts, int axis) {
+  if (total_rows < 0 || cols <= 0 || num_experts <= 0 || total_rows % 32) return 0;
+  if (axis == MXFP8_AXIS_ROW) {
+    if (cols % 32) return 0;
+    return static_cast<size_t>((cdiv(total_rows, 128) + num_experts) * cdiv(cols / 32, 4) * 512);
+  }
+  if (axis == MXFP8_AXIS_COL)
+    return static_cast<size_t>(cdiv(cols, 128) * (cdiv(total_rows, 128) + num_experts) * 512);
+  return 0;
+}
+
+static int quantize_common(const void* src, int64_t batch, int64_t rows, int64_t cols, int axis,
+                           void* out, void* scales, int layout, const int32_t* offsets, int E,
+                           void* stream) {
+  if (batch < 0 || rows < 0 || cols < 0) return MXFP8_ERR_INVALID_ARG;
+  if (axis != MXFP8_AXIS_ROW && axis != MXFP8_AXIS_COL) return MXFP8_ERR_INVALID_ARG;
+  if (layout != MXFP8_SCALES_LINEAR && layout != MXFP8_SCALES_SWIZZLED)
+    return MXFP8_ERR_INVALID_ARG;
+  if (axis == MXFP8_AXIS_ROW && cols % 32) return MXFP8_ERR_ALIGNMENT;
+  if (axis == MXFP8_AXIS_COL && (rows % 32 || cols % 8)) return MXFP8_ERR_ALIGNMENT;
+  if (batch == 0 || rows == 0 || cols == 0) return MXFP8_OK;
+  if (!src || !out || !scales) return MXFP8_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(out)) return MXFP8_ERR_ALIGNMENT;
+  if (layout == MXFP8_SCALES_SWIZZLED && !aligned16(scales)) return MXFP8_ERR_ALIGNMENT;
+  if (batch > 65535) return MXFP8_ERR_INVALID_ARG;
+  const int64_t token_tiles = cdiv(rows, 128) + (offsets ? E : 0);
+  if (token_tiles > kMaxTokenTiles || cdiv(cols, 128) > 0x7FFFFFFF) return MXFP8_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  const int st = device_state(&d);
+  if (st != MXFP8_OK) return st;
+  QuantizeArgs a{src, batch, rows, cols, axis, out, scales, layout, offsets, E, d->status};
+  return launch_quantize(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MXFP8_OK
+                                                                               : MXFP8_ERR_CUDA;
+}
+
+int mxfp8_quantize(const void* src_dev, int64_t rows, int64_t cols, int axis, void* out_dev,
+                   void* scales_dev, int scale_layout, void* stream) {
+  return quantize_common(src_dev, 1, rows, cols, axis, out_dev, scales_dev, scale_layout,
+                         nullptr, 0, stream);
+}
+
+int mxfp8_quantize_batched(const void* src_dev, int64_t batch, int64_t rows, int64_t cols,
+                           int axis, void* out_dev, void* scales_dev, int scale_layout,
+                           void* stream) {
+  return quantize_common(src_dev, batch, rows, cols, axis, out_dev, scales_dev, scale_layout,
+                         nullptr, 0, stream);
+}
+
+int mxfp8_quantize_grouped(const void* src_dev, int64_t total_rows, int64_t cols, int axis,
+                           const int32_t* expert_offsets_dev, int num_experts, void* out_dev,
+                           void* scales_dev, void* stream) {
+  if (num_experts <= 0 || num_experts > 1024 || !expert_offsets_dev) return MXFP8_ERR_INVALID_ARG;
+  if (total_rows % 32) return MXFP8_ERR_ALIGNMENT;
+  return quantize_common(src_dev, 1, total_rows, cols, axis, out_dev, scales_dev,
+                         MXFP8_SCALES_SWIZZLED, expert_offsets_dev, num_experts, stream);
+}
+
+static int gemm_checks(const void* A, const void* sA, const void* B, const void* sB, void* C,
+                       int op, int out_dtype) {
+  if (!A || !sA || !B || !sB || !C) return MXFP8_ERR_INVALID_ARG;
+  if (op < MXFP8_OP_FPROP || op > MXFP8_OP_WGRAD) return MXFP8_ERR_INVALID_ARG;
+  if (out_dtype != MXFP8_OUT_BF16 && out_dtype != MXFP8_OUT_FP32) return MXFP8_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(C))
+    return MXFP8_ERR_ALIGNMENT;
+  return MXFP8_OK;
+}
+
+int mxfp8_gemm(const void* A_dev, const void* sA_dev, const void* B_dev, const void* sB_dev,
+               void* C_dev, int64_t M, int64_t N, int64_t K, int op, int out_dtype,
+               void* stream) {
+  if (M <= 0 || N <= 0 || K <= 0) return MXFP8_ERR_INVALID_ARG;
+  if (M > 0x7FFFFF00 || N > 0x7FFFFF00 || K > 0x7FFFFF00) return MXFP8_ERR_INVALID_ARG;
+  if (K % 32 || M % 16 || N % 16) return MXFP8_ERR_ALIGNMENT;
+  int st = gemm_checks(A_dev, sA_dev, B_dev, sB_dev, C_dev, op, out_dtype);
+  if (st != MXFP8_OK) return st;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != MXFP8_OK) return st;
+  GemmArgs a{A_dev, sA_dev, B_dev, sB_dev, C_dev, M, N, K, op, out_dtype, nullptr, 0, 0,
+             d->status};
+  return launch_gemm(a, static_cast<cudaStream_t>(stream));
+}
+
+int mxfp8_grouped_gemm(const void* A_dev, const void* sA_dev, const void* B_dev,
+                       const void* sB_dev, void* C_dev, const int32_t* expert_offsets_dev,
+                       int num_experts, int64_t total_rows, int64_t N, int64_t K, int op,
+                       int out_dtype, void* stream) {
+  if (num_experts <= 0 || num_experts > 1024 || !expert_offsets_dev) return MXFP8_ERR_INVALID_ARG;
+  if (total_rows < 0 || N <= 0 || K <= 0) return MXFP8_ERR_INVALID_ARG;
+  if (total_rows > 0x7FFFFF00 || N > 0x7FFFFF00 || K > 0x7FFFFF00) return MXFP8_ERR_INVALID_ARG;
+  if (total_rows % 32 || K % 32 || N % 16) return MXFP8_ERR_ALIGNMENT;
+  int st = gemm_checks(A_dev, sA_dev, B_dev, sB_dev, C_dev, op, out_dtype);
+  if (st != MXFP8_OK) return st;
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != MXFP8_OK) return st;
+  if (total_rows == 0) {
+    // no tokens: fprop/dgrad have no rows to write; every expert's dW is zero
+    if (op != MXFP8_OP_WGRAD) return MXFP8_OK;
+    const size_t elem = out_dtype == MXFP8_OUT_FP32 ? 4 : 2;
+    return cudaMemsetAsync(C_dev, 0, static_cast<size_t>(num_experts) * N * K * elem,
+                           static_cast<cudaStream_t>(stream)) == cudaSuccess ? MXFP8_OK
+                                                                             : MXFP8_ERR_CUDA;
+  }
+  GemmArgs a{A_dev, sA_dev, B_dev, sB_dev, C_dev, 0, N, K, op, out_dtype,
+             expert_offsets_dev, num_experts, total_rows, d->status};
+  return launch_grouped_gemm(a, static_cast<cudaStream_t>(stream));
+}
+
+int mxfp8_get_device_status(void* stream) {
+  DeviceState* d = nullptr;
+  const int st = device_state(&d);
+  if (st != MXFP8_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MXFP8_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return MXFP8_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return MXFP8_ERR_CUDA;
+  return v;
+}
+
+}  // extern "C"

@@ -1,0 +1,586 @@
+// gemm.cu - MXFP8 block-scaled GEMMs on the 5th-generation tensor cores (tcgen05,
+// kind::mxf8f6f4 with UE8M0 scales), dense and grouped over MoE token segments.
+//
+// Method: "End-to-End MXFP8 RL on Blackwell" (verl blog post), section "The pipeline":
+// the format paragraph (Blackwell tensor cores take the 32-element block scales as
+// operands of the MMA instruction) and the learner paragraph (forward, data-gradient
+// and weight-gradient GEMMs per linear layer); expert GEMMs of Qwen3-30B-A3B: section
+// "A held-out workload, and end to end", Table 4.
+//
+// Kernel design (one persistent CTA per SM, warp-specialised):
+//   warp 0      TMA producer: per 128-wide K stage, one tiled load of the A tile
+//               (128 x 128 B) and of the B tile (BN x 128 B), both with the 128-byte
+//               swizzle, plus one 512-byte bulk copy per 128-row scale tile.
+//   warp 1      allocates TMEM; one thread copies the stage's scale tiles into TMEM
+//               (tcgen05.cp 32x128b.warpx4: a 512-byte swizzled tile lands as 4 TMEM
+//               columns, byte k of each column = K block k) and issues four
+//               128 x BN x 32 block-scaled MMAs into the FP32 accumulator in TMEM.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator, FP32 -> BF16/FP32, stores.
+// Shared-memory stages are recycled through full/empty mbarriers; the accumulator
+// through acc_full/acc_empty, so the producer already streams the next tile's operands
+// while the epilogue drains the current one. Each stage has its own TMEM scale slot,
+// so a slot is only rewritten after the MMAs that read it have completed (the stage's
+// empty barrier, armed by tcgen05.commit, precedes its refill).
+// Every wait is bounded: past the limit the CTA latches MXFP8_ERR_TIMEOUT, all roles
+// leave their loops, outstanding copies and MMAs are waited for, TMEM is freed.
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "device.cuh"
+#include "internal.h"
+#include "mxfp8.h"
+
+namespace mxfp8 {
+namespace {
+
+constexpr int BM = 128;           // accumulator rows = TMEM lanes
+constexpr int BK = 128;           // K elements (bytes) per pipeline stage
+constexpr int kThreads = 192;     // 6 warps
+constexpr int kMaxExperts = 1024;
+
+enum Mode : int { kDense = 0, kGroupRows = 1, kGroupWgrad = 2 };
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kABytes = BM * BK;
+  static constexpr int kBBytes = BN * BK;
+  static constexpr int kSfbTiles = BN / 128;
+  static constexpr int kSfbBytes = kSfbTiles * 512;
+  // shared memory carve-up (offsets from a 1024-byte aligned base)
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffSfa = kOffB + kStages * kBBytes;
+  static constexpr int kOffSfb = kOffSfa + kStages * 512;
+  static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
+  static constexpr int kNumBars = 2 * kStages + 3;  // full, empty, acc_full, acc_empty, done
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+  // TMEM columns: accumulator, then per-stage scale slots
+  static constexpr int kSfaCol = BN;
+  static constexpr int kSfbCol = BN + 4 * kStages;
+  static constexpr int kColsUsed = kSfbCol + (BN / 32) * kStages;
+  static constexpr int kTmemCols = kColsUsed <= 256 ? 256 : 512;
+  static_assert(kColsUsed <= 512, "TMEM overflow");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory overflow");
+};
+
+struct Params {
+  const uint8_t* sA;
+  const uint8_t* sB;
+  void* C;
+  int64_t M, N;          // output rows / cols of one problem
+  int64_t K;             // reduction length (dense / grouped rows)
+  int out_fp32;
+  const int32_t* offsets;
+  int E;
+  int64_t total_rows;
+  int64_t sb_item_bytes; // grouped rows: bytes of one expert's B scale block
+  int64_t num_tiles;     // dense: all tiles; grouped: upper bound
+  int num_m_tiles, num_n_tiles;
+  int* status;
+  uint64_t wait_ns;
+};
+
+// Everything a role needs to know about one output tile.
+struct Tile {
+  int64_t m0, n0;        // output tile origin within its problem
+  int rows_valid, cols_valid;
+  int64_t a_row;         // TMA row coordinate of A
+  int64_t k_origin;      // TMA K coordinate of the first stage
+  int nk;                // K stages
+  int last_blocks;       // valid 32-blocks in the last stage (1..4)
+  int b_z;               // expert index for the 3-D B map (grouped rows)
+  int64_t sfa_tile0;     // scale tile index of (row tile, stage 0) in sA
+  int64_t sfa_kstride;   // tiles between consecutive stages (1)
+  const uint8_t* sfb_base;
+  int64_t sfb_row_tiles_stride;  // tiles between consecutive 128-row B tiles
+  int64_t c_off;         // element offset of the problem's C
+  int64_t ldc;
+  bool live;
+};
+
+struct SegShared {
+  int32_t off[kMaxExperts + 1];
+  int32_t tile_base[kMaxExperts + 1];
+  int ok;
+};
+
+__device__ int find_seg(const SegShared& s, int E, int64_t t) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s.tile_base[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int BN, int kMode>
+__device__ Tile make_tile(const Params& p, const SegShared* seg, int64_t id) {
+  Tile t;
+  t.live = false;
+  const int64_t n_kt_dense = (p.K + BK - 1) / BK;
+  if (kMode == kDense) {
+    if (id >= p.num_tiles) return t;
+    // grouped raster: bands of 8 M tiles sweep across N, so concurrent CTAs share
+    // operand tiles in L2
+    constexpr int64_t GM = 8;
+    const int64_t band = GM * p.num_n_tiles;
+    const int64_t g = id / band;
+    const int64_t first_m = g * GM;
+    const int64_t gm = (p.num_m_tiles - first_m) < GM ? (p.num_m_tiles - first_m) : GM;
+    const int64_t mt = first_m + (id % band) % gm;
+    const int64_t nt = (id % band) / gm;
+    t.m0 = mt * BM;
+    t.n0 = nt * BN;
+    t.rows_valid = static_cast<int>((p.M - t.m0) < BM ? (p.M - t.m0) : BM);
+    t.cols_valid = static_cast<int>((p.N - t.n0) < BN ? (p.N - t.n0) : BN);
+    t.a_row = t.m0;
+    t.k_origin = 0;
+    t.nk = static_cast<int>(n_kt_dense);
+    t.last_blocks = static_cast<int>(((p.K - (n_kt_dense - 1) * BK) + 31) / 32);
+    t.b_z = 0;
+    t.sfa_tile0 = mt * n_kt_dense;
+    t.sfa_kstride = 1;
+    t.sfb_base = p.sB + nt * (BN / 128) * n_kt_dense * 512;
+    t.sfb_row_tiles_stride = n_kt_dense;
+    t.c_off = 0;
+    t.ldc = p.N;
+    t.live = true;
+    return t;
+  }
+  if (kMode == kGroupRows) {
+    const int64_t n_tiles = static_cast<int64_t>(seg->tile_base[p.E]) * p.num_n_tiles;
+    if (!seg->ok || id >= n_tiles) return t;
+    const int64_t row_tile = id / p.num_n_tiles;
+    const int64_t nt = id % p.num_n_tiles;
+    const int e = find_seg(*seg, p.E, row_tile);
+    const int64_t i = row_tile - seg->tile_base[e];
+    t.m0 = seg->off[e] + i * BM;
+    t.n0 = nt * BN;
+    const int64_t left = seg->off[e + 1] - t.m0;
+    t.rows_valid = static_cast<int>(left < BM ? left : BM);
+    t.cols_valid = static_cast<int>((p.N - t.n0) < BN ? (p.N - t.n0) : BN);
+    t.a_row = t.m0;
+    t.k_origin = 0;
+    t.nk = static_cast<int>(n_kt_dense);
+    t.last_blocks = static_cast<int>(((p.K - (n_kt_dense - 1) * BK) + 31) / 32);
+    t.b_z = e;
+    t.sfa_tile0 = row_tile * n_kt_dense;
+    t.sfa_kstride = 1;
+    t.sfb_base = p.sB + e * p.sb_item_bytes + nt * (BN / 128) * n_kt_dense * 512;
+    t.sfb_row_tiles_stride = n_kt_dense;
+    t.c_off = 0;
+    t.ldc = p.N;
+    t.live = true;
+    return t;
+  }
+  // grouped weight gradient: problem e is [M = N_out] x [N = K_out], reduced over the
+  // tokens of segment e
+  const int64_t per = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+  if (!seg->ok || id >= per * p.E) return t;
+  const int e = static_cast<int>(id / per);
+  const int64_t r = id % per;
+  const int64_t mt = r / p.num_n_tiles, nt = r % p.num_n_tiles;
+  const int64_t cnt = seg->off[e + 1] - seg->off[e];
+  const int64_t nk = (cnt + BK - 1) / BK;
+  t.m0 = mt * BM;
+  t.n0 = nt * BN;
+  t.rows_valid = static_cast<int>((p.M - t.m0) < BM ? (p.M - t.m0) : BM);
+  t.cols_valid = static_cast<int>((p.N - t.n0) < BN ? (p.N - t.n0) : BN);
+  t.a_row = t.m0;
+  t.k_origin = seg->off[e];
+  t.nk = static_cast<int>(nk);
+  t.last_blocks = nk ? static_cast<int>((cnt - (nk - 1) * BK) / 32) : 0;
+  t.b_z = 0;
+  const int64_t n_rt_a = (p.M + 127) / 128, n_rt_b = (p.N + 127) / 128;
+  const int64_t tb = seg->tile_base[e];
+  t.sfa_tile0 = n_rt_a * tb + mt * nk;
+  t.sfa_kstride = 1;
+  t.sfb_base = p.sB + (n_rt_b * tb + nt * (BN / 128) * nk) * 512;
+  t.sfb_row_tiles_stride = nk;
+  t.c_off = static_cast<int64_t>(e) * p.M * p.N;
+  t.ldc = p.N;
+  t.live = true;
+  return t;
+}
+
+template <int BN, int kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                  const __grid_constant__ CUtensorMap map_b, const Params p) {
+  using C = Cfg<BN>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::kStages;
+  uint64_t* acc_full = bars + 2 * C::kStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* mma_done = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  __shared__ SegShared seg_storage;
+  SegShared* seg = (kMode == kDense) ? nullptr : &seg_storage;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b);
+  }
+  if (kMode != kDense) {
+    // segment table: offsets checked (0-based, non-decreasing, 32-aligned, ending at
+    // total_rows) and prefix sums of ceil(count / 128)
+    const int E = p.E;
+    if (threadIdx.x == 0) seg->ok = 1;
+    __syncthreads();
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) seg->off[i] = p.offsets[i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < E; i += blockDim.x) {
+      const int32_t lo = seg->off[i], hi = seg->off[i + 1];
+      if (hi < lo || (lo & 31) || (hi & 31)) seg->ok = 0;
+    }
+    if (threadIdx.x == 0 &&
+        (seg->off[0] != 0 || static_cast<int64_t>(seg->off[E]) != p.total_rows))
+      seg->ok = 0;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int32_t acc = 0;
+      for (int e = 0; e < E; ++e) {
+        seg->tile_base[e] = acc;
+        const int32_t cnt = seg->off[e + 1] - seg->off[e];
+        acc += cnt > 0 ? (cnt + 127) / 128 : 0;
+      }
+      seg->tile_base[E] = acc;
+      if (!seg->ok && blockIdx.x == 0) latch_error(p.status, MXFP8_ERR_BAD_OFFSETS);
+    }
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------- TMA producer
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t id = blockIdx.x; ok; id += gridDim.x) {
+      const Tile t = make_tile<BN, kMode>(p, seg, id);
+      if (!t.live) break;
+      for (int kb = 0; kb < t.nk; ++kb, ++it) {
+        const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1;
+        if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
+        int n_sfb = 0;
+        for (int h = 0; h < C::kSfbTiles; ++h) n_sfb += (t.n0 + 128 * h < p.N);
+        const uint32_t bytes = C::kABytes + C::kBBytes + 512 + 512 * n_sfb;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        const int32_t kx = static_cast<int32_t>(t.k_origin + static_cast<int64_t>(kb) * BK);
+        tma_load_2d(smem + C::kOffA + s * C::kABytes, &map_a, kx,
+                    static_cast<int32_t>(t.a_row), &full[s]);
+        if (kMode == kGroupRows)
+          tma_load_3d(smem + C::kOffB + s * C::kBBytes, &map_b, kx, static_cast<int32_t>(t.n0),
+                      t.b_z, &full[s]);
+        else
+          tma_load_2d(smem + C::kOffB + s * C::kBBytes, &map_b, kx, static_cast<int32_t>(t.n0),
+                      &full[s]);
+        bulk_load(smem + C::kOffSfa + s * 512, p.sA + (t.sfa_tile0 + kb) * 512, 512, &full[s]);
+        for (int h = 0; h < n_sfb; ++h)
+          bulk_load(smem + C::kOffSfb + s * C::kSfbBytes + h * 512,
+                    t.sfb_base + (h * t.sfb_row_tiles_stride + kb) * 512, 512, &full[s]);
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      latch_error(p.status, MXFP8_ERR_TIMEOUT);
+    }
+    // whatever happened, no copy may still be landing when the CTA exits
+    const uint32_t n = it < static_cast<uint32_t>(C::kStages) ? it : C::kStages;
+    for (uint32_t j = 0; j < n; ++j) {
+      const uint32_t i2 = it - 1 - j;
+      mbar_wait_timed(&full[i2 % C::kStages], (i2 / C::kStages) & 1, p.wait_ns);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------- MMA issuer
+    uint32_t it = 0, acc_it = 0;
+    bool ok = true;
+    const uint32_t sa_base = smem_u32(smem + C::kOffA);
+    const uint32_t sb_base = smem_u32(smem + C::kOffB);
+    for (int64_t id = blockIdx.x; ok; id += gridDim.x) {
+      const Tile t = make_tile<BN, kMode>(p, seg, id);
+      if (!t.live) break;
+      if (t.nk == 0) continue;
+      if (!mbar_wait_bounded(acc_empty, (acc_it & 1) ^ 1, abort_flag, p.wait_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int kb = 0; kb < t.nk; ++kb, ++it) {
+        const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1;
+        if (!mbar_wait_bounded(&full[s], ph, abort_flag, p.wait_ns)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sfa_t = tmem + C::kSfaCol + 4 * s;
+        const uint32_t sfb_t = tmem + C::kSfbCol + (BN / 32) * s;
+        tmem_cp_32x128b_x4(sfa_t, smem_desc(smem_u32(smem + C::kOffSfa + s * 512), 0, 128, 0));
+#pragma unroll
+        for (int h = 0; h < C::kSfbTiles; ++h)
+          tmem_cp_32x128b_x4(sfb_t + 4 * h,
+                             smem_desc(smem_u32(smem + C::kOffSfb + s * C::kSfbBytes + h * 512),
+                                       0, 128, 0));
+        const int nblk = (kb == t.nk - 1) ? t.last_blocks : 4;
+        for (int k = 0; k < nblk; ++k) {
+          const uint64_t ad = smem_desc(sa_base + s * C::kABytes + 32 * k, 16, 1024, 2);
+          const uint64_t bd = smem_desc(sb_base + s * C::kBBytes + 32 * k, 16, 1024, 2);
+          mma_mxf8(tmem, ad, bd, mxf8_idesc(BM, BN, k, k), sfa_t, sfb_t,
+                   (kb > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(&empty[s]);
+      }
+      if (!ok) break;
+      mma_commit(acc_full);
+      ++acc_it;
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      latch_error(p.status, MXFP8_ERR_TIMEOUT);
+    }
+    // all issued tensor-core work must be finished before TMEM is released
+    mma_commit(mma_done);
+    mbar_wait_timed(mma_done, 0, p.wait_ns);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    uint32_t acc_it = 0;
+    bool ok = true;
+    for (int64_t id = blockIdx.x; ok; id += gridDim.x) {
+      const Tile t = make_tile<BN, kMode>(p, seg, id);
+      if (!t.live) break;
+      const int r = 32 * q + lane;
+      const bool row_ok = r < t.rows_valid;
+      const int64_t row = t.m0 + r;
+      if (t.nk > 0) {
+        // one lane waits, the warp follows its verdict (keeps the warp converged)
+        int got = 0;
+        if (lane == 0) got = mbar_wait_bounded(acc_full, acc_it & 1, abort_flag, p.wait_ns);
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        if (!got) { ok = false; break; }
+        tc_fence_after();
+      }
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        __syncwarp();
+        if (t.nk > 0) {
+          tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * c, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0;
+        }
+        const int cols_left = t.cols_valid - 32 * c;
+        if (row_ok && cols_left > 0) {
+          if (p.out_fp32) {
+            float* dst = static_cast<float*>(p.C) + t.c_off + row * t.ldc + t.n0 + 32 * c;
+            const int nvec = cols_left >= 32 ? 8 : cols_left / 4;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (i < nvec)
+                reinterpret_cast<uint4*>(dst)[i] =
+                    make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          } else {
+            uint16_t* dst = static_cast<uint16_t*>(p.C) + t.c_off + row * t.ldc + t.n0 + 32 * c;
+            uint32_t b[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              b[i] = cvt_bf16x2(__uint_as_float(v[2 * i + 1]), __uint_as_float(v[2 * i]));
+            const int nvec = cols_left >= 32 ? 4 : cols_left / 8;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (i < nvec)
+                reinterpret_cast<uint4*>(dst)[i] =
+                    make_uint4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
+          }
+        }
+      }
+      if (t.nk > 0) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);
+        ++acc_it;
+      }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      latch_error(p.status, MXFP8_ERR_TIMEOUT);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// Row-major u8 matrix [outer][inner] (optionally [depth][outer][inner]) viewed through a
+// box of box_inner bytes x box_outer rows with the 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, int rank, uint64_t inner, uint64_t outer,
+              uint64_t depth, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {inner, outer, depth};
+  cuuint64_t strides[2] = {inner, inner * outer};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+uint64_t wait_limit_ns() {
+  static uint64_t ns = [] {
+    const char* e = getenv("MXFP8_WAIT_LIMIT_MS");
+    long ms = e ? atol(e) : 0;
+    if (ms <= 0) ms = 4000;
+    return static_cast<uint64_t>(ms) * 1000000ull;
+  }();
+  return ns;
+}
+
+template <int BN, int kMode>
+int launch(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int64_t grid,
+           cudaStream_t stream) {
+  using C = Cfg<BN>;
+  auto k = mxfp8_gemm_kernel<BN, kMode>;
+  static bool attr_set[64] = {};  // per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+      return MXFP8_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  if (grid <= 0) return MXFP8_OK;
+  k<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(ma, mb, p);
+  return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
+  Params p{};
+  p.sA = static_cast<const uint8_t*>(a.sA);
+  p.sB = static_cast<const uint8_t*>(a.sB);
+  p.C = a.C;
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.out_fp32 = a.out_dtype == MXFP8_OUT_FP32;
+  p.status = a.status;
+  p.wait_ns = wait_limit_ns();
+  const bool wide = a.N > 128;
+  const int bn = wide ? 256 : 128;
+  p.num_m_tiles = static_cast<int>((a.M + BM - 1) / BM);
+  p.num_n_tiles = static_cast<int>((a.N + bn - 1) / bn);
+  p.num_tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, a.A, 2, a.K, a.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
+  if (!make_map(&mb, a.B, 2, a.K, a.N, 1, BK, bn)) return MXFP8_ERR_CUDA;
+  const int64_t grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+  return wide ? launch<256, kDense>(ma, mb, p, grid, stream)
+              : launch<128, kDense>(ma, mb, p, grid, stream);
+}
+
+int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
+  if (a.num_experts > kMaxExperts) return MXFP8_ERR_INVALID_ARG;
+  Params p{};
+  p.sA = static_cast<const uint8_t*>(a.sA);
+  p.sB = static_cast<const uint8_t*>(a.sB);
+  p.C = a.C;
+  p.out_fp32 = a.out_dtype == MXFP8_OUT_FP32;
+  p.offsets = a.offsets;
+  p.E = a.num_experts;
+  p.total_rows = a.total_rows;
+  p.status = a.status;
+  p.wait_ns = wait_limit_ns();
+  CUtensorMap ma, mb;
+  if (a.op == MXFP8_OP_WGRAD) {
+    // A = dY^T [N][T], B = X^T [K][T], C[e] = [N][K]
+    p.M = a.N;
+    p.N = a.K;
+    p.K = a.total_rows;
+    const bool wide = p.N > 128;
+    const int bn = wide ? 256 : 128;
+    p.num_m_tiles = static_cast<int>((p.M + BM - 1) / BM);
+    p.num_n_tiles = static_cast<int>((p.N + bn - 1) / bn);
+    const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles * p.E;
+    p.num_tiles = tiles;
+    if (!make_map(&ma, a.A, 2, a.total_rows, p.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
+    if (!make_map(&mb, a.B, 2, a.total_rows, p.N, 1, BK, bn)) return MXFP8_ERR_CUDA;
+    const int64_t grid = tiles < num_sms() ? tiles : num_sms();
+    return wide ? launch<256, kGroupWgrad>(ma, mb, p, grid, stream)
+                : launch<128, kGroupWgrad>(ma, mb, p, grid, stream);
+  }
+  // fprop / dgrad: A [T][K] segmented by rows, B [E][N][K], C [T][N]
+  p.M = a.total_rows;
+  p.N = a.N;
+  p.K = a.K;
+  const bool wide = p.N > 128;
+  const int bn = wide ? 256 : 128;
+  const int64_t n_kt = (a.K + BK - 1) / BK;
+  p.sb_item_bytes = ((a.N + 127) / 128) * n_kt * 512;
+  p.num_m_tiles = static_cast<int>((a.total_rows + BM - 1) / BM + a.num_experts);
+  p.num_n_tiles = static_cast<int>((p.N + bn - 1) / bn);
+  const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+  p.num_tiles = tiles;
+  if (!make_map(&ma, a.A, 2, a.K, a.total_rows, 1, BK, BM)) return MXFP8_ERR_CUDA;
+  if (!make_map(&mb, a.B, 3, a.K, a.N, a.num_experts, BK, bn)) return MXFP8_ERR_CUDA;
+  const int64_t grid = tiles < num_sms() ? tiles : num_sms();
+  return wide ? launch<256, kGroupRows>(ma, mb, p, grid, stream)
+              : launch<128, kGroupRows>(ma, mb, p, grid, stream);
+}
+
+}  // namespace mxfp8

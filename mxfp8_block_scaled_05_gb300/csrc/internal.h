@@ -1,0 +1,46 @@
+// internal.h - host-side interface between the C ABI (api.cu) and the kernel launchers.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mxfp8 {
+
+struct QuantizeArgs {
+  const void* src;
+  int64_t batch;          // independent matrices (1 for a plain call)
+  int64_t rows, cols;     // one matrix
+  int axis;               // MXFP8_AXIS_ROW / COL
+  void* out;
+  void* scales;
+  int layout;             // MXFP8_SCALES_LINEAR / SWIZZLED
+  const int32_t* offsets; // grouped call: device [num_experts + 1], else nullptr
+  int num_experts;
+  int* status;            // device status word
+};
+
+cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream);
+
+struct GemmArgs {
+  const void* A;
+  const void* sA;
+  const void* B;
+  const void* sB;
+  void* C;
+  int64_t M, N, K;
+  int op;
+  int out_dtype;
+  // grouped call
+  const int32_t* offsets;  // nullptr for the dense GEMM
+  int num_experts;
+  int64_t total_rows;
+  int* status;
+};
+
+// Returns MXFP8_OK or an mxfp8_status code.
+int launch_gemm(const GemmArgs& a, cudaStream_t stream);
+int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream);
+
+int num_sms();  // of the current device (cached)
+
+}  // namespace mxfp8

@@ -1,0 +1,105 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it loads, exports every symbol
+include/mxfp8.h declares, sizes scale tensors as documented, and rejects bad arguments
+with status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import __graft_entry__
+import mxfp8_block_scaled_05_gb300 as m
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return m.lib()
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w \*]*?\b(mxfp8_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    so = ctypes.CDLL(m.LIB_PATH)
+    for n in names:
+        assert hasattr(so, n), f"{n} declared in include/ but not exported"
+        assert n in m.SIGNATURES, f"{n} has no binding"
+    assert set(m.SIGNATURES) <= set(names)
+    assert lib.mxfp8_version() == 1
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lib.mxfp8_status_string(s)
+    assert lib.mxfp8_status_string(99) == b"unknown status"
+
+
+def test_scale_bytes(lib):
+    sb = lib.mxfp8_scale_bytes
+    assert sb(256, 256, m.ROW, m.LINEAR) == 256 * 8
+    assert sb(256, 256, m.ROW, m.SWIZZLED) == 2 * 2 * 512
+    assert sb(129, 32, m.ROW, m.SWIZZLED) == 2 * 1 * 512
+    assert sb(64, 40, m.COL, m.LINEAR) == 40 * 2
+    assert sb(64, 40, m.COL, m.SWIZZLED) == 1 * 1 * 512
+    assert sb(4096, 24576, m.ROW, m.SWIZZLED) == 32 * 192 * 512
+    assert sb(100, 48, m.ROW, m.LINEAR) == 0          # cols % 32
+    assert sb(48, 100, m.COL, m.LINEAR) == 0          # rows % 32
+    assert sb(-1, 32, m.ROW, m.LINEAR) == 0
+    assert sb(32, 32, 7, m.LINEAR) == 0
+    assert sb(0, 64, m.ROW, m.SWIZZLED) == 0
+    gb = lib.mxfp8_grouped_scale_bytes
+    assert gb(65536, 2048, 128, m.ROW) == (512 + 128) * 16 * 512
+    assert gb(65536, 1536, 128, m.COL) == 12 * (512 + 128) * 512
+    assert gb(65536 + 16, 2048, 128, m.ROW) == 0
+
+
+def test_argument_errors_need_no_device(lib):
+    p = ctypes.c_void_p(0x10000)          # never dereferenced: every call below fails a check
+    bad = ctypes.c_void_p(0x10001)
+    q = lib.mxfp8_quantize
+    assert q(p, 64, 48, m.ROW, p, p, m.SWIZZLED, None) == m.ERR_ALIGNMENT
+    assert q(p, 48, 64, m.COL, p, p, m.SWIZZLED, None) == m.ERR_ALIGNMENT
+    assert q(p, 64, 36, m.COL, p, p, m.SWIZZLED, None) == m.ERR_ALIGNMENT   # cols % 8
+    assert q(None, 64, 64, m.ROW, p, p, m.SWIZZLED, None) == m.ERR_INVALID_ARG
+    assert q(p, 64, 64, 2, p, p, m.SWIZZLED, None) == m.ERR_INVALID_ARG
+    assert q(p, 64, 64, m.ROW, p, p, 5, None) == m.ERR_INVALID_ARG
+    assert q(bad, 64, 64, m.ROW, p, p, m.SWIZZLED, None) == m.ERR_ALIGNMENT
+    assert q(p, -1, 64, m.ROW, p, p, m.SWIZZLED, None) == m.ERR_INVALID_ARG
+    assert q(None, 0, 64, m.ROW, None, None, m.SWIZZLED, None) == m.OK      # empty: no-op
+    g = lib.mxfp8_gemm
+    assert g(p, p, p, p, p, 128, 128, 48, 0, 0, None) == m.ERR_ALIGNMENT
+    assert g(p, p, p, p, p, 120, 128, 64, 0, 0, None) == m.ERR_ALIGNMENT
+    assert g(p, p, p, p, p, 0, 128, 64, 0, 0, None) == m.ERR_INVALID_ARG
+    assert g(p, p, p, p, p, 128, 128, 64, 3, 0, None) == m.ERR_INVALID_ARG
+    assert g(p, p, p, p, p, 128, 128, 64, 0, 2, None) == m.ERR_INVALID_ARG
+    assert g(p, p, bad, p, p, 128, 128, 64, 0, 0, None) == m.ERR_ALIGNMENT
+    assert g(p, None, p, p, p, 128, 128, 64, 0, 0, None) == m.ERR_INVALID_ARG
+    gg = lib.mxfp8_grouped_gemm
+    assert gg(p, p, p, p, p, p, 0, 64, 128, 64, 0, 0, None) == m.ERR_INVALID_ARG
+    assert gg(p, p, p, p, p, p, 2000, 64, 128, 64, 0, 0, None) == m.ERR_INVALID_ARG
+    assert gg(p, p, p, p, p, None, 4, 64, 128, 64, 0, 0, None) == m.ERR_INVALID_ARG
+    assert gg(p, p, p, p, p, p, 4, 48, 128, 64, 0, 0, None) == m.ERR_ALIGNMENT
+    qg = lib.mxfp8_quantize_grouped
+    assert qg(p, 64, 64, m.ROW, None, 4, p, p, None) == m.ERR_INVALID_ARG
+    assert qg(p, 48, 64, m.ROW, p, 4, p, p, None) == m.ERR_ALIGNMENT
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU failure path")
+def test_valid_call_without_a_gpu_fails_cleanly(lib):
+    p = ctypes.c_void_p(0x10000)
+    assert lib.mxfp8_quantize(p, 64, 64, m.ROW, p, p, m.SWIZZLED, None) in (
+        m.ERR_CUDA, m.ERR_UNSUPPORTED_ARCH)
+    assert lib.mxfp8_get_device_status(None) in (m.ERR_CUDA, m.ERR_UNSUPPORTED_ARCH)
