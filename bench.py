@@ -1,0 +1,575 @@
+"""Benchmark: one step = the whole MXFP8 hot path of a Qwen3-8B linear layer set at one
+micro-batch of 4096 tokens ("End-to-End MXFP8 RL on Blackwell", sections "The pipeline"
+and "Where the time goes": per linear layer, the operands X, W and dY are quantized
+row-wise and column-wise, then the fprop, dgrad and wgrad block-scaled GEMMs run).
+
+Per step and layer (qkv 4096->6144, o 4096->4096, gate_up 4096->24576, down 12288->4096):
+6 quantize launches + 3 GEMM launches; 36 launches per step. Inputs are synthetic
+(seeded, BF16) and live in HBM before the timed region; the step's working set (453 MB
+of BF16 inputs) is larger than L2, so no flush is needed between steps.
+
+Output: one JSON line (rank 0). `value` is the step's MXFP8 GEMM FLOPs divided by the
+step time (quantization included), in TFLOP/s; the `quantize` and `gemm` objects split
+the time; `roofline` is for the dominant kernel (the GEMM).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --workload moe|sync|sweep     # the other configurations
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantize GB/s + MXFP8 GEMM TFLOP/s on Qwen3-8B linears, % of GB300 roofline"
+FP8_OVER_BF16 = 2.0   # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
+QBYTES_PER_ELEM = 2.0 + 1.0 + 1.0 / 32.0   # BF16 read + E4M3 + E8M0/32 written
+REF_ROW_FRAC = 1.0 / 8192   # reference arm: 32 rows of every operand per step
+REF_BLOCK = (8, 16)         # reference arm: output block sampled per GEMM
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ----------------------------------------------------------------------- distributed
+
+def dist_setup(n_gpus):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, ws
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    """The slowest rank's value (timing only; no data-path collective)."""
+    if ws == 1:
+        return x
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self, busy_mhz_floor: float = 0.0):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]),
+                                 hw=f[5], hwt=f[6], swt=f[7], pcap=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        load = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# --------------------------------------------------------------------------- workload
+
+def layer_flops(t, n, k):
+    return 3 * 2.0 * t * n * k
+
+
+def layer_quant_elems(t, n, k):
+    # X [t,k], W [n,k], dY [t,n], each row-wise and column-wise
+    return 2 * (t * k + n * k + t * n)
+
+
+class DenseStep:
+    """Buffers and launches of one step; every launch goes through the C ABI."""
+
+    def __init__(self, m, tokens: int, seed: int, dev):
+        from mxfp8_block_scaled_05_gb300 import workloads as W
+        self.m = m
+        self.layers = []
+        for name, n, k, x, w, dy in W.qwen3_8b_layer_set(tokens, dev, seed):
+            t = x.shape[0]
+            L = dict(name=name, t=t, n=n, k=k, x=x, w=w, dy=dy)
+            for key, src, axis in (("xr", x, m.ROW), ("xc", x, m.COL), ("wr", w, m.ROW),
+                                   ("wc", w, m.COL), ("dyr", dy, m.ROW), ("dyc", dy, m.COL)):
+                r, c = src.shape
+                shape = (r, c) if axis == m.ROW else (c, r)
+                L[key] = (torch.empty(shape, dtype=torch.uint8, device=dev),
+                          torch.empty(m.scale_bytes(r, c, axis, m.SWIZZLED), dtype=torch.uint8,
+                                      device=dev), src, axis)
+            L["y"] = torch.empty((t, n), dtype=torch.bfloat16, device=dev)
+            L["dx"] = torch.empty((t, k), dtype=torch.bfloat16, device=dev)
+            L["dw"] = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
+            self.layers.append(L)
+        self.flops = sum(layer_flops(L["t"], L["n"], L["k"]) for L in self.layers)
+        self.qelems = sum(layer_quant_elems(L["t"], L["n"], L["k"]) for L in self.layers)
+        self.launches = 9 * len(self.layers)
+
+    def run(self, stream, events=None):
+        """Enqueues one step. With `events` (a list), appends (kind, units, start, end)."""
+        m = self.m
+        for L in self.layers:
+            for key in ("xr", "xc", "wr", "wc", "dyr", "dyc"):
+                q, s, src, axis = L[key]
+                ev = self._ev(events, stream, "quantize", src.numel())
+                m.quantize(src, axis, m.SWIZZLED, out=q, scales=s, stream=stream)
+                self._end(events, stream, ev)
+            t, n, k = L["t"], L["n"], L["k"]
+            for op, a, b, out, mnk in ((m.FPROP, "xr", "wr", L["y"], (t, n, k)),
+                                       (m.DGRAD, "dyr", "wc", L["dx"], (t, k, n)),
+                                       (m.WGRAD, "dyc", "xc", L["dw"], (n, k, t))):
+                ev = self._ev(events, stream, "gemm", 2.0 * mnk[0] * mnk[1] * mnk[2])
+                m.gemm(L[a][0], L[a][1], L[b][0], L[b][1], op, m.OUT_BF16, out=out, stream=stream)
+                self._end(events, stream, ev)
+
+    @staticmethod
+    def _ev(events, stream, kind, units):
+        if events is None:
+            return None
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        return (kind, units, s, e)
+
+    @staticmethod
+    def _end(events, stream, ev):
+        if ev is not None:
+            ev[3].record(stream)
+            events.append(ev)
+
+
+def gemm_source_sha():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "device.cuh"):
+        with open(os.path.join(ROOT, "mxfp8_block_scaled_05_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    sha = gemm_source_sha()
+    for line in open(p):
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if f.get("kernel") == kernel_key and f.get("source_sha") == sha:
+            return float(f["dram_bytes_per_launch"])
+    return None
+
+
+# ------------------------------------------------------------------------- CPU oracle
+
+def oracle_step_sample(seed: int = 0, row_frac: float = 1.0 / 512, block=(32, 64)):
+    """Times the CPU oracle on a bounded sample of one step: a fraction of the rows of
+    every quantized operand and one 32 x 64 output block per GEMM. Returns (seconds for
+    the sampled work, seconds extrapolated to a full step, description)."""
+    import oracle.mxfp8_oracle as O
+    from mxfp8_block_scaled_05_gb300 import workloads as W
+    rng = np.random.default_rng(seed)
+    q_sec, q_elems, g_sec, g_flops = 0.0, 0, 0.0, 0.0
+    total_q, total_f = 0, 0.0
+    for name, n, k in W.QWEN3_8B_LINEARS:
+        t = 4096
+        total_q += layer_quant_elems(t, n, k)
+        total_f += layer_flops(t, n, k)
+        for rows, cols in ((t, k), (n, k), (t, n)):
+            r = max(32, int(rows * row_frac) // 32 * 32)
+            x = (rng.standard_normal((r, cols)).astype(np.float32).view(np.uint32) >> 16
+                 ).astype(np.uint16)
+            t0 = time.perf_counter()
+            O.quantize(x, O.ROW)
+            O.quantize(x, O.COL)
+            q_sec += time.perf_counter() - t0
+            q_elems += 2 * r * cols
+        for mm, nn, kk in ((t, n, k), (t, k, n), (n, k, t)):
+            a = (rng.standard_normal((block[0], kk)).astype(np.float32).view(np.uint32) >> 16
+                 ).astype(np.uint16)
+            b = (rng.standard_normal((block[1], kk)).astype(np.float32).view(np.uint32) >> 16
+                 ).astype(np.uint16)
+            qa, sa = O.quantize(a, O.ROW)
+            qb, sb = O.quantize(b, O.ROW)
+            t0 = time.perf_counter()
+            O.gemm(qa, sa, qb, sb)
+            O.gemm_abs(qa, sa, qb, sb)
+            g_sec += time.perf_counter() - t0
+            g_flops += 2.0 * block[0] * block[1] * kk
+    est = q_sec * total_q / q_elems + g_sec * total_f / g_flops
+    desc = (f"{row_frac:.4g} of every operand's rows quantized row+col ({q_elems} elems) and a "
+            f"{block[0]}x{block[1]} output block of each of the 12 GEMMs ({g_flops / 1e9:.3f} GFLOP), "
+            "extrapolated to the full step")
+    return q_sec + g_sec, est, desc, total_f
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------- arms
+
+def run_reference(args, rank, ws):
+    """The oracle as it stands, on the host cores (a deliberately slow program)."""
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_step_sample(0, REF_ROW_FRAC, REF_BLOCK)
+    secs, ests, desc, flops = [], [], "", 0.0
+    for i in range(args.steps):
+        s, est, desc, flops = oracle_step_sample(i + 1, REF_ROW_FRAC, REF_BLOCK)
+        secs.append(s)
+        ests.append(est)
+    step_s = float(np.mean(ests))
+    value = flops / step_s / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_obj(),
+        "cpu_baseline": {"kind": "oracle", "value": value, "unit": "TFLOP/s",
+                         "cores": cpu_cores(), "sample": desc,
+                         "sample_seconds_per_step": float(np.mean(secs))},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_obj(tokens=4096):
+    return {"workload": f"Qwen3-8B dense linear layer set at {tokens} tokens: qkv 4096->6144, "
+                        "o 4096->4096, gate_up 4096->24576, down 12288->4096; X, W, dY "
+                        "quantized row- and column-wise (swizzled scales), then fprop, dgrad "
+                        "and wgrad MXFP8 GEMMs (BF16 out) per layer",
+            "tokens": tokens, "layers": 4,
+            "l2": "inputs larger than L2 (453 MB BF16 per step), no flush"}
+
+
+def run_ours(args, rank, ws):
+    import mxfp8_block_scaled_05_gb300 as m
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pk = peaks()
+    step = DenseStep(m, args.tokens, seed=1 + rank, dev=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step.run(stream)
+    torch.cuda.synchronize()
+    if m.device_status() != m.OK:
+        raise RuntimeError("device status set during warm-up")
+
+    events = []
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier(ws)
+        start.record(stream)
+        for _ in range(args.steps):
+            step.run(stream, events)
+        end.record(stream)
+        barrier(ws)
+    ms = start.elapsed_time(end)
+    ms_max = max_over_ranks(ms, ws)
+    status = m.device_status()
+    if status != m.OK:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    q_ms = sum(s.elapsed_time(e) for k, _, s, e in events if k == "quantize")
+    g_ms = sum(s.elapsed_time(e) for k, _, s, e in events if k == "gemm")
+    g_units = sum(u for k, u, _, _ in events if k == "gemm")
+    g_launches = sum(1 for k, *_ in events if k == "gemm")
+    q_units = sum(u for k, u, _, _ in events if k == "quantize")
+    step_ms = ms_max / args.steps
+    value = ws * step.flops / (step_ms * 1e-3) / 1e12
+    gemm_tflops = g_units / (g_ms * 1e-3) / 1e12
+    quant_gbs = q_units * QBYTES_PER_ELEM / (q_ms * 1e-3) / 1e9
+    fp8_peak = pk["bf16_sus"] * FP8_OVER_BF16
+    traffic = recorded_traffic("mxfp8_gemm_kernel")
+    e2e = run_e2e(args, m, step, dev, stream, ws)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic (seeded N(0,1) activations with 0.5% x30 outlier channels, "
+                "N(0,0.02) weights, N(0,1) gradients; BF16)",
+        "config": config_obj(args.tokens),
+        "gpu_launches": step.launches * args.steps,
+        "quantize": {"GB/s": quant_gbs, "frac_of_hbm": quant_gbs / pk["hbm"],
+                     "ms_per_step": q_ms / args.steps,
+                     "bytes_per_elem": QBYTES_PER_ELEM, "peak_GB/s": pk["hbm"],
+                     "peak_src": pk["src"]},
+        "gemm": {"TFLOP/s": gemm_tflops, "frac_of_mxfp8": gemm_tflops / fp8_peak,
+                 "ms_per_step": g_ms / args.steps, "flops_per_step": step.flops},
+        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
+                     "traffic": traffic,
+                     "kernel": "mxfp8_gemm_kernel (12 launches per step)",
+                     "peak_note": f"{pk['src']} bf16 sustained {pk['bf16_sus']} x "
+                                  f"{FP8_OVER_BF16} (nominal FP8:BF16 ratio)",
+                     "flops_per_launch": g_units / g_launches},
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline_obj()
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, m, step, dev, stream, ws):
+    """Same step through the public API, with the BF16 inputs copied in from pinned host
+    memory and the BF16 results copied back inside the timed region."""
+    host_in, host_out = [], []
+    for L in step.layers:
+        for key in ("x", "w", "dy"):
+            host_in.append((torch.empty_like(L[key], device="cpu").pin_memory(), L[key]))
+        for key in ("y", "dx", "dw"):
+            host_out.append((L[key], torch.empty_like(L[key], device="cpu").pin_memory()))
+    for h, d in host_in:
+        h.copy_(d)
+    h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
+    d2h = sum(h.numel() * h.element_size() for _, h in host_out)
+    steps = max(3, args.steps // 4)
+
+    def one():
+        for h, d in host_in:
+            d.copy_(h, non_blocking=True)
+        step.run(stream)
+        for d, h in host_out:
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    barrier(ws)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        one()
+    e.record(stream)
+    barrier(ws)
+    ms = max_over_ranks(s.elapsed_time(e), ws) / steps
+    return {"value": ws * step.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "steps": steps}
+
+
+def cpu_baseline_obj():
+    budget, t0 = 15.0, time.perf_counter()
+    ests, secs, desc, flops = [], [], "", 0.0
+    i = 0
+    while time.perf_counter() - t0 < budget and i < 50:
+        s, est, desc, flops = oracle_step_sample(100 + i)
+        ests.append(est)
+        secs.append(s)
+        i += 1
+    step_s = float(np.mean(ests))
+    return {"value": flops / step_s / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
+            "kind": "oracle", "sample": f"{i} samples of: {desc}",
+            "seconds": time.perf_counter() - t0, "ms_per_step_extrapolated": step_s * 1e3}
+
+
+# ------------------------------------------------------------ other configurations
+
+def run_workload(args):
+    """Secondary configurations, one JSON line each (not the headline)."""
+    import mxfp8_block_scaled_05_gb300 as m
+    from mxfp8_block_scaled_05_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(reps):
+            fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / reps
+
+    if args.workload == "sync":
+        shapes = W.sync_weight_shapes()
+        # one buffer per distinct shape, reused across layers (inputs > L2 each)
+        bufs = {}
+        for _, name, n, k in shapes[:4]:
+            w = W.sync_weight(0, name, n, k, dev)
+            bufs[name] = (w, torch.empty_like(w, dtype=torch.uint8),
+                          torch.empty(m.scale_bytes(n, k), dtype=torch.uint8, device=dev))
+
+        def sync_pass():
+            for _, name, n, k in shapes:
+                w, q, s = bufs[name]
+                m.quantize(w, m.ROW, m.SWIZZLED, out=q, scales=s, stream=stream)
+
+        ms = timed(sync_pass, 5)
+        elems = sum(n * k for _, _, n, k in shapes)
+        gbs = elems * QBYTES_PER_ELEM / (ms * 1e-3) / 1e9
+        print(json.dumps({"workload": "weight-sync quantize pass, Qwen3-8B shapes (144 weights, "
+                          f"{elems / 1e9:.3f} G elems)", "ms": ms, "GB/s": gbs,
+                          "frac_of_hbm": gbs / pk["hbm"], "launches": len(shapes)}), flush=True)
+    elif args.workload == "moe":
+        d = W.moe_expert_layer(dev)
+        offs = d["offsets"].to(dev)
+        x, w, dy = d["x"], d["w_gate_up"], d["dy_gate_up"]
+        E, n, k = w.shape
+        qx, sx = m.quantize_grouped(x, offs, m.ROW)
+        qw, sw = m.quantize_batched(w, m.ROW)
+        qdy, sdy = m.quantize_grouped(dy, offs, m.ROW)
+        qwt, swt = m.quantize_batched(w, m.COL)
+        qdyt, sdyt = m.quantize_grouped(dy, offs, m.COL)
+        qxt, sxt = m.quantize_grouped(x, offs, m.COL)
+        real = int(d["counts"].sum())
+        flops = 2.0 * real * n * k
+        res = {}
+        for name, fn in (
+                ("fprop", lambda: m.grouped_gemm(qx, sx, qw, sw, offs, m.FPROP, stream=stream)),
+                ("dgrad", lambda: m.grouped_gemm(qdy, sdy, qwt, swt, offs, m.DGRAD, stream=stream)),
+                ("wgrad", lambda: m.grouped_gemm(qdyt, sdyt, qxt, sxt, offs, m.WGRAD, stream=stream)),
+                ("quantize_x_row", lambda: m.quantize_grouped(x, offs, m.ROW, out=qx, scales=sx, stream=stream)),
+                ("quantize_x_col", lambda: m.quantize_grouped(x, offs, m.COL, out=qxt, scales=sxt, stream=stream))):
+            ms = timed(fn, 20)
+            if name.startswith("quantize"):
+                res[name] = {"ms": ms, "GB/s": x.numel() * QBYTES_PER_ELEM / (ms * 1e-3) / 1e9}
+            else:
+                res[name] = {"ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12}
+        print(json.dumps({"workload": "Qwen3-30B-A3B gate_up experts (128 x 1536 x 2048), "
+                          f"{real} routed rows, {int(d['offsets'][-1])} padded", **res}), flush=True)
+    elif args.workload == "sweep":
+        for t in W.SWEEP_TOKENS:
+            layers = W.sweep_layers(t, dev)
+            out = {"tokens": t}
+            qms, gms, flops = 0.0, 0.0, 0.0
+            for name, n, k, x, w, dy in layers:
+                tt = x.shape[0]
+                qs = {}
+                for key, src, axis in (("xr", x, m.ROW), ("xc", x, m.COL), ("wr", w, m.ROW),
+                                       ("wc", w, m.COL), ("dyr", dy, m.ROW), ("dyc", dy, m.COL)):
+                    qs[key] = m.quantize(src, axis)
+                qms += timed(lambda: [m.quantize(src, axis, out=qs[key][0], scales=qs[key][1],
+                                                 stream=stream)
+                                      for key, src, axis in (("xr", x, m.ROW), ("xc", x, m.COL),
+                                                             ("wr", w, m.ROW), ("wc", w, m.COL),
+                                                             ("dyr", dy, m.ROW), ("dyc", dy, m.COL))], 10)
+                y = torch.empty((tt, n), dtype=torch.bfloat16, device=dev)
+                dx = torch.empty((tt, k), dtype=torch.bfloat16, device=dev)
+                dw = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
+                gms += timed(lambda: (m.gemm(*qs["xr"], *qs["wr"], m.FPROP, out=y, stream=stream),
+                                      m.gemm(*qs["dyr"], *qs["wc"], m.DGRAD, out=dx, stream=stream),
+                                      m.gemm(*qs["dyc"], *qs["xc"], m.WGRAD, out=dw, stream=stream)), 10)
+                flops += layer_flops(tt, n, k)
+            out.update(quantize_ms=qms, gemm_ms=gms, gemm_TFLOPs=flops / (gms * 1e-3) / 1e12,
+                       quantize_share=qms / (qms + gms))
+            print(json.dumps(out), flush=True)
+            del layers
+            torch.cuda.empty_cache()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--workload", choices=("dense", "moe", "sync", "sweep"), default="dense")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, rank, int(os.environ.get("WORLD_SIZE", "1")))
+        return
+    import __graft_entry__
+    __graft_entry__.build()
+    rank, ws = dist_setup(args.gpus)
+    try:
+        if args.workload != "dense":
+            if rank == 0:
+                run_workload(args)
+        else:
+            run_ours(args, rank, ws)
+    finally:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

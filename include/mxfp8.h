@@ -116,6 +116,18 @@ int mxfp8_quantize(const void* src_dev, int64_t rows, int64_t cols, int axis,
                    void* out_dev, void* scales_dev, int scale_layout, void* stream);
 
 /*
+ * Both copies of one BF16 matrix from a single read of it: the row-wise copy (as
+ * mxfp8_quantize ROW) into row_out_dev / row_scales_dev and the column-wise copy (as
+ * mxfp8_quantize COL) into col_out_dev / col_scales_dev. The learner needs both for X and
+ * dY (forward/dgrad operands blocked along K, wgrad operands blocked along tokens:
+ * "The pipeline", learner paragraph). Requires rows % 32 == 0 and cols % 32 == 0. Bytes
+ * are identical to the two separate calls.
+ */
+int mxfp8_quantize_dual(const void* src_dev, int64_t rows, int64_t cols, void* row_out_dev,
+                        void* row_scales_dev, void* col_out_dev, void* col_scales_dev,
+                        int scale_layout, void* stream);
+
+/*
  * `batch` independent matrices [batch][rows][cols] quantized as by mxfp8_quantize, each
  * with its own scale block of mxfp8_scale_bytes(rows, cols, axis, layout) bytes; the
  * scale blocks are concatenated in batch order. Used for per-expert MoE weights.
@@ -152,6 +164,16 @@ size_t mxfp8_grouped_scale_bytes(int64_t total_rows, int64_t cols, int num_exper
 int mxfp8_quantize_grouped(const void* src_dev, int64_t total_rows, int64_t cols, int axis,
                            const int32_t* expert_offsets_dev, int num_experts,
                            void* out_dev, void* scales_dev, void* stream);
+
+/*
+ * mxfp8_quantize_grouped ROW and COL from one read of the input (cols % 32 == 0);
+ * each copy's scales go to its own buffer, sized by mxfp8_grouped_scale_bytes for its
+ * axis.
+ */
+int mxfp8_quantize_grouped_dual(const void* src_dev, int64_t total_rows, int64_t cols,
+                                const int32_t* expert_offsets_dev, int num_experts,
+                                void* row_out_dev, void* row_scales_dev, void* col_out_dev,
+                                void* col_scales_dev, void* stream);
 
 /*
  * Block-scaled GEMM on tcgen05 (kind::mxf8f6f4, E4M3 x E4M3, UE8M0 scales, FP32

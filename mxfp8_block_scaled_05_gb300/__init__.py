@@ -33,7 +33,9 @@ SIGNATURES = {
     "mxfp8_scale_bytes": (_SZ, [_I64, _I64, _I, _I]),
     "mxfp8_grouped_scale_bytes": (_SZ, [_I64, _I64, _I, _I]),
     "mxfp8_quantize": (_I, [_P, _I64, _I64, _I, _P, _P, _I, _P]),
+    "mxfp8_quantize_dual": (_I, [_P, _I64, _I64, _P, _P, _P, _P, _I, _P]),
     "mxfp8_quantize_batched": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _I, _P]),
+    "mxfp8_quantize_grouped_dual": (_I, [_P, _I64, _I64, _P, _I, _P, _P, _P, _P, _P]),
     "mxfp8_quantize_grouped": (_I, [_P, _I64, _I64, _I, _P, _I, _P, _P, _P]),
     "mxfp8_gemm": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _P]),
     "mxfp8_grouped_gemm": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _P]),
@@ -123,6 +125,56 @@ def quantize(src: torch.Tensor, axis: int = ROW, layout: int = SWIZZLED, out=Non
     _check(lib().mxfp8_quantize(_ptr(src), rows, cols, axis, _ptr(out), _ptr(scales), layout,
                                 _stream(stream)), "mxfp8_quantize")
     return out, scales
+
+
+def _alloc_scales(rows, cols, axis, layout, dev):
+    if layout == LINEAR:
+        s_rows, s_cols = (rows, cols // 32) if axis == ROW else (cols, rows // 32)
+        return torch.empty((s_rows, s_cols), dtype=torch.uint8, device=dev)
+    return torch.empty(scale_bytes(rows, cols, axis, layout), dtype=torch.uint8, device=dev)
+
+
+def quantize_dual(src: torch.Tensor, layout: int = SWIZZLED, row_out=None, row_scales=None,
+                  col_out=None, col_scales=None, stream=None):
+    """Row-wise and column-wise copies of a BF16 [rows, cols] tensor from one read.
+    Returns (row_codes, row_scales, col_codes, col_scales)."""
+    _require(src, torch.bfloat16, "src")
+    rows, cols = src.shape
+    dev = src.device
+    row_out = torch.empty((rows, cols), dtype=torch.uint8, device=dev) if row_out is None else row_out
+    col_out = torch.empty((cols, rows), dtype=torch.uint8, device=dev) if col_out is None else col_out
+    if row_scales is None:
+        row_scales = _alloc_scales(rows, cols, ROW, layout, dev)
+    if col_scales is None:
+        col_scales = _alloc_scales(rows, cols, COL, layout, dev)
+    _check(lib().mxfp8_quantize_dual(_ptr(src), rows, cols, _ptr(row_out), _ptr(row_scales),
+                                     _ptr(col_out), _ptr(col_scales), layout, _stream(stream)),
+           "mxfp8_quantize_dual")
+    return row_out, row_scales, col_out, col_scales
+
+
+def quantize_grouped_dual(src: torch.Tensor, offsets: torch.Tensor, row_out=None,
+                          row_scales=None, col_out=None, col_scales=None, stream=None):
+    """mxfp8_quantize_grouped ROW and COL from one read. Returns
+    (row_codes, row_scales, col_codes, col_scales)."""
+    _require(src, torch.bfloat16, "src")
+    _require(offsets, torch.int32, "offsets")
+    total, cols = src.shape
+    e = offsets.numel() - 1
+    dev = src.device
+    row_out = torch.empty((total, cols), dtype=torch.uint8, device=dev) if row_out is None else row_out
+    col_out = torch.empty((cols, total), dtype=torch.uint8, device=dev) if col_out is None else col_out
+    if row_scales is None:
+        row_scales = torch.empty(grouped_scale_bytes(total, cols, e, ROW), dtype=torch.uint8,
+                                 device=dev)
+    if col_scales is None:
+        col_scales = torch.empty(grouped_scale_bytes(total, cols, e, COL), dtype=torch.uint8,
+                                 device=dev)
+    _check(lib().mxfp8_quantize_grouped_dual(_ptr(src), total, cols, _ptr(offsets), e,
+                                             _ptr(row_out), _ptr(row_scales), _ptr(col_out),
+                                             _ptr(col_scales), _stream(stream)),
+           "mxfp8_quantize_grouped_dual")
+    return row_out, row_scales, col_out, col_scales
 
 
 def quantize_batched(src: torch.Tensor, axis: int = ROW, layout: int = SWIZZLED, out=None,

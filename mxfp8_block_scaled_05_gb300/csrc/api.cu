@@ -132,50 +132,97 @@ size_t mxfp8_grouped_scale_bytes(int64_t total_rows, int64_t cols, int num_exper
   return 0;
 }
 
+// axis: MXFP8_AXIS_ROW, MXFP8_AXIS_COL or kAxisBoth (out/scales = row-wise copy,
+// out2/scales2 = column-wise copy).
 static int quantize_common(const void* src, int64_t batch, int64_t rows, int64_t cols, int axis,
-                           void* out, void* scales, int layout, const int32_t* offsets, int E,
-                           void* stream) {
+                           void* out, void* scales, void* out2, void* scales2, int layout,
+                           const int32_t* offsets, int E, void* stream) {
   if (batch < 0 || rows < 0 || cols < 0) return MXFP8_ERR_INVALID_ARG;
-  if (axis != MXFP8_AXIS_ROW && axis != MXFP8_AXIS_COL) return MXFP8_ERR_INVALID_ARG;
+  if (axis != MXFP8_AXIS_ROW && axis != MXFP8_AXIS_COL && axis != kAxisBoth)
+    return MXFP8_ERR_INVALID_ARG;
   if (layout != MXFP8_SCALES_LINEAR && layout != MXFP8_SCALES_SWIZZLED)
     return MXFP8_ERR_INVALID_ARG;
-  if (axis == MXFP8_AXIS_ROW && cols % 32) return MXFP8_ERR_ALIGNMENT;
-  if (axis == MXFP8_AXIS_COL && (rows % 32 || cols % 8)) return MXFP8_ERR_ALIGNMENT;
+  const bool row = axis != MXFP8_AXIS_COL, col = axis != MXFP8_AXIS_ROW;
+  if (row && cols % 32) return MXFP8_ERR_ALIGNMENT;
+  if (col && (rows % 32 || cols % 8)) return MXFP8_ERR_ALIGNMENT;
   if (batch == 0 || rows == 0 || cols == 0) return MXFP8_OK;
   if (!src || !out || !scales) return MXFP8_ERR_INVALID_ARG;
-  if (!aligned16(src) || !aligned16(out)) return MXFP8_ERR_ALIGNMENT;
-  if (layout == MXFP8_SCALES_SWIZZLED && !aligned16(scales)) return MXFP8_ERR_ALIGNMENT;
+  if (axis == kAxisBoth && (!out2 || !scales2)) return MXFP8_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(out) || (out2 && !aligned16(out2)))
+    return MXFP8_ERR_ALIGNMENT;
+  if (layout == MXFP8_SCALES_SWIZZLED && (!aligned16(scales) || (scales2 && !aligned16(scales2))))
+    return MXFP8_ERR_ALIGNMENT;
   if (batch > 65535) return MXFP8_ERR_INVALID_ARG;
   const int64_t token_tiles = cdiv(rows, 128) + (offsets ? E : 0);
   if (token_tiles > kMaxTokenTiles || cdiv(cols, 128) > 0x7FFFFFFF) return MXFP8_ERR_INVALID_ARG;
   DeviceState* d = nullptr;
   const int st = device_state(&d);
   if (st != MXFP8_OK) return st;
-  QuantizeArgs a{src, batch, rows, cols, axis, out, scales, layout, offsets, E, d->status};
+  QuantizeArgs a{};
+  a.src = src;
+  a.batch = batch;
+  a.rows = rows;
+  a.cols = cols;
+  a.axis = axis;
+  a.layout = layout;
+  a.offsets = offsets;
+  a.num_experts = E;
+  a.status = d->status;
+  if (row) {
+    a.out = out;
+    a.scales = scales;
+    a.scale_item_bytes = scale_bytes_host(rows, cols, MXFP8_AXIS_ROW, layout);
+  }
+  if (col) {
+    a.out_col = axis == kAxisBoth ? out2 : out;
+    a.scales_col = axis == kAxisBoth ? scales2 : scales;
+    a.scale_item_bytes_col = scale_bytes_host(rows, cols, MXFP8_AXIS_COL, layout);
+  }
   return launch_quantize(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MXFP8_OK
                                                                                : MXFP8_ERR_CUDA;
 }
 
 int mxfp8_quantize(const void* src_dev, int64_t rows, int64_t cols, int axis, void* out_dev,
                    void* scales_dev, int scale_layout, void* stream) {
-  return quantize_common(src_dev, 1, rows, cols, axis, out_dev, scales_dev, scale_layout,
-                         nullptr, 0, stream);
+  if (axis != MXFP8_AXIS_ROW && axis != MXFP8_AXIS_COL) return MXFP8_ERR_INVALID_ARG;
+  return quantize_common(src_dev, 1, rows, cols, axis, out_dev, scales_dev, nullptr, nullptr,
+                         scale_layout, nullptr, 0, stream);
+}
+
+int mxfp8_quantize_dual(const void* src_dev, int64_t rows, int64_t cols, void* row_out_dev,
+                        void* row_scales_dev, void* col_out_dev, void* col_scales_dev,
+                        int scale_layout, void* stream) {
+  return quantize_common(src_dev, 1, rows, cols, kAxisBoth, row_out_dev, row_scales_dev,
+                         col_out_dev, col_scales_dev, scale_layout, nullptr, 0, stream);
 }
 
 int mxfp8_quantize_batched(const void* src_dev, int64_t batch, int64_t rows, int64_t cols,
                            int axis, void* out_dev, void* scales_dev, int scale_layout,
                            void* stream) {
-  return quantize_common(src_dev, batch, rows, cols, axis, out_dev, scales_dev, scale_layout,
-                         nullptr, 0, stream);
+  if (axis != MXFP8_AXIS_ROW && axis != MXFP8_AXIS_COL) return MXFP8_ERR_INVALID_ARG;
+  return quantize_common(src_dev, batch, rows, cols, axis, out_dev, scales_dev, nullptr, nullptr,
+                         scale_layout, nullptr, 0, stream);
 }
 
 int mxfp8_quantize_grouped(const void* src_dev, int64_t total_rows, int64_t cols, int axis,
                            const int32_t* expert_offsets_dev, int num_experts, void* out_dev,
                            void* scales_dev, void* stream) {
   if (num_experts <= 0 || num_experts > 1024 || !expert_offsets_dev) return MXFP8_ERR_INVALID_ARG;
+  if (axis != MXFP8_AXIS_ROW && axis != MXFP8_AXIS_COL) return MXFP8_ERR_INVALID_ARG;
   if (total_rows % 32) return MXFP8_ERR_ALIGNMENT;
-  return quantize_common(src_dev, 1, total_rows, cols, axis, out_dev, scales_dev,
-                         MXFP8_SCALES_SWIZZLED, expert_offsets_dev, num_experts, stream);
+  return quantize_common(src_dev, 1, total_rows, cols, axis, out_dev, scales_dev, nullptr,
+                         nullptr, MXFP8_SCALES_SWIZZLED, expert_offsets_dev, num_experts, stream);
+}
+
+int mxfp8_quantize_grouped_dual(const void* src_dev, int64_t total_rows, int64_t cols,
+                                const int32_t* expert_offsets_dev, int num_experts,
+                                void* row_out_dev, void* row_scales_dev, void* col_out_dev,
+                                void* col_scales_dev, void* stream) {
+  if (num_experts <= 0 || num_experts > 1024 || !expert_offsets_dev) return MXFP8_ERR_INVALID_ARG;
+  if (total_rows % 32) return MXFP8_ERR_ALIGNMENT;
+  return quantize_common(src_dev, 1, total_rows, cols, kAxisBoth, row_out_dev, row_scales_dev,
+                         col_out_dev, col_scales_dev, MXFP8_SCALES_SWIZZLED, expert_offsets_dev,
+                         num_experts, stream);
 }
 
 static int gemm_checks(const void* A, const void* sA, const void* B, const void* sB, void* C,

@@ -6,13 +6,19 @@
 
 namespace mxfp8 {
 
+constexpr int kAxisBoth = 2;  // both copies from one read (row-wise + column-wise)
+
 struct QuantizeArgs {
   const void* src;
   int64_t batch;          // independent matrices (1 for a plain call)
   int64_t rows, cols;     // one matrix
-  int axis;               // MXFP8_AXIS_ROW / COL
-  void* out;
+  int axis;               // MXFP8_AXIS_ROW / COL, or kAxisBoth
+  void* out;              // ROW or COL output (ROW output when axis == kAxisBoth)
   void* scales;
+  int64_t scale_item_bytes;
+  void* out_col;          // kAxisBoth: the column-wise output
+  void* scales_col;
+  int64_t scale_item_bytes_col;
   int layout;             // MXFP8_SCALES_LINEAR / SWIZZLED
   const int32_t* offsets; // grouped call: device [num_experts + 1], else nullptr
   int num_experts;

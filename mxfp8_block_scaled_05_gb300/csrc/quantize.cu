@@ -31,13 +31,6 @@ constexpr int kTile = 128;        // rows and columns of a CTA tile
 constexpr int kThreads = 256;
 constexpr int kMaxExperts = 1024; // grouped calls: experts scanned in shared memory
 
-struct TileInfo {
-  int64_t row0;        // first input row of the tile
-  int rows_valid;      // input rows of the tile that exist (multiple of 32 for COL)
-  int64_t scale_tile;  // index of this tile's 512-byte swizzled scale tile
-  bool live;
-};
-
 // Expert segmentation of the token rows for grouped calls. Every CTA re-derives the
 // prefix sums of ceil(count / 128) from the offsets, so that no table has to be kept in
 // global memory; invalid offsets make every CTA return without writing anything.
@@ -121,257 +114,206 @@ __device__ __forceinline__ uint32_t e4m3x4(uint32_t w0, uint32_t w1, float mul, 
   return p0 | (p1 << 16);
 }
 
-template <bool kGrouped>
-__device__ TileInfo row_tile_info(const Segments* seg, int E, int64_t rows, int64_t n_ct) {
-  TileInfo ti;
-  const int64_t t = blockIdx.y;
-  if (!kGrouped) {
-    ti.row0 = t * kTile;
-    const int64_t left = rows - ti.row0;
-    ti.rows_valid = static_cast<int>(left < kTile ? left : kTile);
-    ti.scale_tile = t * n_ct + blockIdx.x;
-    ti.live = true;
-    return ti;
-  }
-  ti.live = seg->ok && t < seg->tile_base[E];
-  if (!ti.live) return ti;
-  const int e = find_expert(*seg, E, static_cast<int>(t));
-  const int64_t i = t - seg->tile_base[e];
-  ti.row0 = seg->off[e] + i * kTile;
-  const int64_t left = seg->off[e + 1] - ti.row0;
-  ti.rows_valid = static_cast<int>(left < kTile ? left : kTile);
-  ti.scale_tile = t * n_ct + blockIdx.x;
-  return ti;
-}
+// One CTA = one 128 x 128 BF16 tile (128 token rows x 128 columns). kRow: write the
+// row-wise copy (blocks along the columns); kCol: write the column-wise copy (blocks
+// along the rows, emitted transposed). With both, the input is read once.
+struct QOut {
+  uint8_t* codes;
+  uint8_t* scales;
+  int64_t scale_item_bytes;  // bytes of one batch item's scale block
+};
 
-// ------------------------------------------------------------------ row-wise kernel
-
-template <bool kSwizzled, bool kGrouped>
+template <bool kRow, bool kCol, bool kSwizzled, bool kGrouped>
 __global__ void __launch_bounds__(kThreads)
-quantize_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t cols,
-                     uint8_t* __restrict__ out, uint8_t* __restrict__ scales,
-                     int64_t scale_bytes_per_item, const int32_t* __restrict__ offsets,
-                     int E, int* status) {
-  __shared__ __align__(16) uint8_t stile[512];
+quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t cols, QOut ro,
+                     QOut co, const int32_t* __restrict__ offsets, int E, int* status) {
+  __shared__ __align__(16) uint16_t tile[kCol ? kTile : 1][kCol ? kTile : 8];
+  __shared__ __align__(16) uint8_t stile_r[512];
+  __shared__ __align__(16) uint8_t stile_c[512];
   extern __shared__ __align__(16) uint8_t dyn[];  // Segments for grouped calls
   Segments* seg = reinterpret_cast<Segments*>(dyn);
   if (kGrouped) load_segments(*seg, offsets, E, rows, status);
 
-  const int64_t s_cols = cols / 32;
-  const int64_t n_ct = (s_cols + 3) / 4;
-  const TileInfo ti = row_tile_info<kGrouped>(seg, E, rows, n_ct);
-  if (!ti.live) return;
+  // ---- which tile, and where its two 512-byte scale tiles go
+  const int64_t n_col_tiles = (cols + kTile - 1) / kTile;  // = scale tiles per row-wise tile row
+  int64_t row0, tile_row;       // first token row; global token-tile index
+  int rows_valid;
+  int64_t col_scale_tile;       // column-wise scale tile index
+  if (!kGrouped) {
+    tile_row = blockIdx.y;
+    row0 = tile_row * kTile;
+    const int64_t left = rows - row0;
+    rows_valid = static_cast<int>(left < kTile ? left : kTile);
+    col_scale_tile = static_cast<int64_t>(blockIdx.x) * ((rows + kTile - 1) / kTile) + tile_row;
+  } else {
+    const int t = blockIdx.y;
+    if (!seg->ok || t >= seg->tile_base[E]) return;
+    const int e = find_expert(*seg, E, t);
+    const int64_t i = t - seg->tile_base[e];
+    tile_row = t;
+    row0 = seg->off[e] + i * kTile;
+    const int64_t left = seg->off[e + 1] - row0;
+    rows_valid = static_cast<int>(left < kTile ? left : kTile);
+    const int64_t cnt = seg->off[e + 1] - seg->off[e];
+    col_scale_tile = n_col_tiles * seg->tile_base[e] +
+                     static_cast<int64_t>(blockIdx.x) * ((cnt + kTile - 1) / kTile) + i;
+  }
+  const int64_t row_scale_tile = tile_row * n_col_tiles + blockIdx.x;
 
   const int64_t item = blockIdx.z;
   src += item * rows * cols;
-  out += item * rows * cols;
-  scales += item * scale_bytes_per_item;
+  if (kRow) {
+    ro.codes += item * rows * cols;
+    ro.scales += item * ro.scale_item_bytes;
+  }
+  if (kCol) {
+    co.codes += item * rows * cols;
+    co.scales += item * co.scale_item_bytes;
+  }
 
   const int t = threadIdx.x;
   const int v = t & 15;             // 16-byte vector (8 elements) within the tile row
   const int rsub = t >> 4;          // rows rsub + 16 j
   const int64_t col0 = static_cast<int64_t>(blockIdx.x) * kTile;
-  const int64_t col = col0 + 8 * v;
-  const bool col_ok = col < cols;   // cols % 32 == 0: whole 4-lane groups agree
+  const int64_t cols_left = cols - col0;
+  const int cols_valid = static_cast<int>(cols_left < kTile ? cols_left : kTile);
+  const bool col_ok = 8 * v < cols_valid;   // cols % 8 == 0 (% 32 == 0 with kRow)
 
+  // ---- load: eight 16-byte loads per thread, all issued before any is used
   uint4 x[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int r = rsub + 16 * j;
-    if (col_ok && r < ti.rows_valid)
-      x[j] = ld_nc_v4(src + (ti.row0 + r) * cols + col);
+    if (col_ok && r < rows_valid)
+      x[j] = ld_nc_v4(src + (row0 + r) * cols + col0 + 8 * v);
     else
       x[j] = make_uint4(0, 0, 0, 0);
   }
 
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int r = rsub + 16 * j;
-    uint32_t m = bf16_absmax8(x[j]);
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-    const bool valid = col_ok && r < ti.rows_valid;
-    const uint32_t s = scale_byte(m);
-    const float mul = inv_scale(s == 0xFFu ? 127u : s);
-    if (valid) {
-      uint2 o;
-      o.x = e4m3x4(x[j].x, x[j].y, mul, s == 0xFFu);
-      o.y = e4m3x4(x[j].z, x[j].w, mul, s == 0xFFu);
-      *reinterpret_cast<uint2*>(out + (ti.row0 + r) * cols + col) = o;
-    }
-    if ((v & 3) == 0) {
-      const int b = v >> 2;  // block within the tile row
-      if (kSwizzled) {
-        stile[(r & 31) * 16 + (r >> 5) * 4 + b] = valid ? static_cast<uint8_t>(s) : 0;
-      } else if (valid) {
-        scales[(ti.row0 + r) * s_cols + col0 / 32 + b] = static_cast<uint8_t>(s);
-      }
-    }
-  }
-  if (kSwizzled) {
-    __syncthreads();
-    if (t < 32)
-      reinterpret_cast<uint4*>(scales + ti.scale_tile * 512)[t] =
-          reinterpret_cast<const uint4*>(stile)[t];
-  }
-}
-
-// ------------------------------------------------------- column-wise (transposing) kernel
-
-template <bool kSwizzled, bool kGrouped>
-__global__ void __launch_bounds__(kThreads)
-quantize_cols_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t cols,
-                     uint8_t* __restrict__ out, uint8_t* __restrict__ scales,
-                     int64_t scale_bytes_per_item, const int32_t* __restrict__ offsets,
-                     int E, int* status) {
-  __shared__ __align__(16) uint16_t tile[kTile][kTile];
-  __shared__ __align__(16) uint8_t stile[512];
-  extern __shared__ __align__(16) uint8_t dyn[];
-  Segments* seg = reinterpret_cast<Segments*>(dyn);
-  if (kGrouped) load_segments(*seg, offsets, E, rows, status);
-
-  // tile rows = tokens (input rows), tile cols = input cols = output rows
-  TileInfo ti;
-  int64_t n_tok_tiles_e = (rows + kTile - 1) / kTile;  // scale tile columns of the block
-  int64_t scale_base_tile = 0;                          // first scale tile of the block
-  int64_t tok_tile = blockIdx.y;                        // token tile within the block
-  const int64_t n_rt = (cols + kTile - 1) / kTile;      // scale tile rows (input cols)
-  if (!kGrouped) {
-    ti.row0 = static_cast<int64_t>(blockIdx.y) * kTile;
-    const int64_t left = rows - ti.row0;
-    ti.rows_valid = static_cast<int>(left < kTile ? left : kTile);
-    ti.live = true;
-  } else {
-    const int t = blockIdx.y;
-    ti.live = seg->ok && t < seg->tile_base[E];
-    if (!ti.live) return;
-    const int e = find_expert(*seg, E, t);
-    tok_tile = t - seg->tile_base[e];
-    ti.row0 = seg->off[e] + tok_tile * kTile;
-    const int64_t left = seg->off[e + 1] - ti.row0;
-    ti.rows_valid = static_cast<int>(left < kTile ? left : kTile);
-    const int64_t cnt = seg->off[e + 1] - seg->off[e];
-    n_tok_tiles_e = (cnt + kTile - 1) / kTile;
-    scale_base_tile = n_rt * seg->tile_base[e];
-  }
-  ti.scale_tile = scale_base_tile + static_cast<int64_t>(blockIdx.x) * n_tok_tiles_e + tok_tile;
-
-  const int64_t item = blockIdx.z;
-  src += item * rows * cols;
-  out += item * rows * cols;
-  scales += item * scale_bytes_per_item;
-
-  const int t = threadIdx.x;
-  const int64_t col0 = static_cast<int64_t>(blockIdx.x) * kTile;
-  const int64_t cols_left = cols - col0;
-  const int cols_valid = static_cast<int>(cols_left < kTile ? cols_left : kTile);
-
-  // load: 128 rows x 128 cols, 8 vectors per thread, all issued before the smem stores
-  {
-    const int v = t & 15, rsub = t >> 4;
-    const bool col_ok = 8 * v < cols_valid;  // cols % 8 == 0
-    uint4 x[8];
+  // ---- row-wise copy straight from registers: the 4 lanes of a 32-block share amax
+  if (kRow) {
+    const int64_t s_cols = cols / 32;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int r = rsub + 16 * j;
-      if (col_ok && r < ti.rows_valid)
-        x[j] = ld_nc_v4(src + (ti.row0 + r) * cols + col0 + 8 * v);
-      else
-        x[j] = make_uint4(0, 0, 0, 0);
+      uint32_t m = bf16_absmax8(x[j]);
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      const bool valid = col_ok && r < rows_valid;
+      const uint32_t s = scale_byte(m);
+      const float mul = inv_scale(s == 0xFFu ? 127u : s);
+      if (valid) {
+        uint2 o;
+        o.x = e4m3x4(x[j].x, x[j].y, mul, s == 0xFFu);
+        o.y = e4m3x4(x[j].z, x[j].w, mul, s == 0xFFu);
+        *reinterpret_cast<uint2*>(ro.codes + (row0 + r) * cols + col0 + 8 * v) = o;
+      }
+      if ((v & 3) == 0) {
+        const int b = v >> 2;  // block within the tile row
+        if (kSwizzled)
+          stile_r[(r & 31) * 16 + (r >> 5) * 4 + b] = valid ? static_cast<uint8_t>(s) : 0;
+        else if (valid)
+          ro.scales[(row0 + r) * s_cols + col0 / 32 + b] = static_cast<uint8_t>(s);
+      }
     }
+  }
+
+  // ---- column-wise copy through shared memory (transpose)
+  if (kCol) {
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       *reinterpret_cast<uint4*>(&tile[rsub + 16 * j][8 * v]) = x[j];
-  }
-  __syncthreads();
-
-  // transpose + quantize: thread = column pair (2cp, 2cp+1) x token block j
-  const int w = t >> 5, lane = t & 31;
-  const int cp = (w & 1) * 32 + lane;
-  const int j = w >> 1;
-  const int c = 2 * cp;
-  const bool valid = c < cols_valid && 32 * j < ti.rows_valid;
-  uint32_t word[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i)
-    word[i] = *reinterpret_cast<const uint32_t*>(&tile[32 * j + i][c]);
-  uint32_t m0 = 0, m1 = 0;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    m0 = max(m0, word[i] & 0x7FFFu);
-    m1 = max(m1, (word[i] >> 16) & 0x7FFFu);
-  }
-  const uint32_t s0 = scale_byte(m0), s1 = scale_byte(m1);
-  if (valid) {
-    const float mul0 = inv_scale(s0 == 0xFFu ? 127u : s0);
-    const float mul1 = inv_scale(s1 == 0xFFu ? 127u : s1);
-    uint32_t o0[8], o1[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const uint32_t a0 = word[4 * q], a1 = word[4 * q + 1], a2 = word[4 * q + 2],
-                     a3 = word[4 * q + 3];
-      // column c: low halves; column c+1: high halves
-      o0[q] = e4m3x4((a0 & 0xFFFFu) | (a1 << 16), (a2 & 0xFFFFu) | (a3 << 16), mul0,
-                     s0 == 0xFFu);
-      o1[q] = e4m3x4((a0 >> 16) | (a1 & 0xFFFF0000u), (a2 >> 16) | (a3 & 0xFFFF0000u), mul1,
-                     s1 == 0xFFu);
-    }
-    uint8_t* d0 = out + (col0 + c) * rows + ti.row0 + 32 * j;
-    uint8_t* d1 = d0 + rows;
-    reinterpret_cast<uint4*>(d0)[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-    reinterpret_cast<uint4*>(d0)[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
-    reinterpret_cast<uint4*>(d1)[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-    reinterpret_cast<uint4*>(d1)[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
-  }
-  if (kSwizzled) {
-    stile[(c & 31) * 16 + (c >> 5) * 4 + j] = valid ? static_cast<uint8_t>(s0) : 0;
-    stile[((c + 1) & 31) * 16 + ((c + 1) >> 5) * 4 + j] = valid ? static_cast<uint8_t>(s1) : 0;
     __syncthreads();
-    if (t < 32)
-      reinterpret_cast<uint4*>(scales + ti.scale_tile * 512)[t] =
-          reinterpret_cast<const uint4*>(stile)[t];
-  } else if (valid) {
-    const int64_t s_cols = rows / 32;
-    scales[(col0 + c) * s_cols + ti.row0 / 32 + j] = static_cast<uint8_t>(s0);
-    scales[(col0 + c + 1) * s_cols + ti.row0 / 32 + j] = static_cast<uint8_t>(s1);
+    // thread = column pair (2cp, 2cp+1) x token block j (32 rows)
+    const int w = t >> 5, lane = t & 31;
+    const int cp = (w & 1) * 32 + lane;
+    const int j = w >> 1;
+    const int c = 2 * cp;
+    const bool valid = c < cols_valid && 32 * j < rows_valid;
+    uint32_t word[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      word[i] = *reinterpret_cast<const uint32_t*>(&tile[32 * j + i][c]);
+    uint32_t m0 = 0, m1 = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      m0 = max(m0, word[i] & 0x7FFFu);
+      m1 = max(m1, (word[i] >> 16) & 0x7FFFu);
+    }
+    const uint32_t s0 = scale_byte(m0), s1 = scale_byte(m1);
+    if (valid) {
+      const float mul0 = inv_scale(s0 == 0xFFu ? 127u : s0);
+      const float mul1 = inv_scale(s1 == 0xFFu ? 127u : s1);
+      uint32_t o0[8], o1[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t a0 = word[4 * q], a1 = word[4 * q + 1], a2 = word[4 * q + 2],
+                       a3 = word[4 * q + 3];
+        // column c: low halves; column c+1: high halves
+        o0[q] = e4m3x4((a0 & 0xFFFFu) | (a1 << 16), (a2 & 0xFFFFu) | (a3 << 16), mul0,
+                       s0 == 0xFFu);
+        o1[q] = e4m3x4((a0 >> 16) | (a1 & 0xFFFF0000u), (a2 >> 16) | (a3 & 0xFFFF0000u), mul1,
+                       s1 == 0xFFu);
+      }
+      uint8_t* d0 = co.codes + (col0 + c) * rows + row0 + 32 * j;
+      uint8_t* d1 = d0 + rows;
+      reinterpret_cast<uint4*>(d0)[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+      reinterpret_cast<uint4*>(d0)[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
+      reinterpret_cast<uint4*>(d1)[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+      reinterpret_cast<uint4*>(d1)[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+    }
+    if (kSwizzled) {
+      stile_c[(c & 31) * 16 + (c >> 5) * 4 + j] = valid ? static_cast<uint8_t>(s0) : 0;
+      stile_c[((c + 1) & 31) * 16 + ((c + 1) >> 5) * 4 + j] = valid ? static_cast<uint8_t>(s1) : 0;
+    } else if (valid) {
+      const int64_t s_cols = rows / 32;
+      co.scales[(col0 + c) * s_cols + row0 / 32 + j] = static_cast<uint8_t>(s0);
+      co.scales[(col0 + c + 1) * s_cols + row0 / 32 + j] = static_cast<uint8_t>(s1);
+    }
+  }
+
+  // ---- the tile's swizzled scale tiles, 16 bytes per thread
+  if (kSwizzled) {
+    __syncthreads();
+    if (kRow && t < 32)
+      reinterpret_cast<uint4*>(ro.scales + row_scale_tile * 512)[t] =
+          reinterpret_cast<const uint4*>(stile_r)[t];
+    if (kCol && t >= 32 && t < 64)
+      reinterpret_cast<uint4*>(co.scales + col_scale_tile * 512)[t - 32] =
+          reinterpret_cast<const uint4*>(stile_c)[t - 32];
   }
 }
 
-template <bool kSw, bool kGr>
-cudaError_t launch_one(const QuantizeArgs& a, cudaStream_t stream, int64_t scale_item) {
+template <bool kRow, bool kCol, bool kSw, bool kGr>
+cudaError_t launch_tiles(const QuantizeArgs& a, cudaStream_t stream) {
   const int64_t col_tiles = (a.cols + kTile - 1) / kTile;
   int64_t row_tiles = (a.rows + kTile - 1) / kTile;
   if (kGr) row_tiles += a.num_experts;  // upper bound: each expert adds one partial tile
-  if (row_tiles > 0x7FFFFFFF || col_tiles > 0x7FFFFFFF || a.batch > 65535)
+  if (row_tiles > 65535 || col_tiles > 0x7FFFFFFF || a.batch > 65535)
     return cudaErrorInvalidValue;
-  // grid.x = column tiles (up to 2^31-1), grid.y = row tiles (<= 65535 per launch)
   const size_t dyn = kGr ? sizeof(Segments) : 0;
-  const uint16_t* src = static_cast<const uint16_t*>(a.src);
-  uint8_t* out = static_cast<uint8_t*>(a.out);
-  uint8_t* sc = static_cast<uint8_t*>(a.scales);
-  if (row_tiles > 65535) return cudaErrorInvalidValue;
+  auto k = quantize_tile_kernel<kRow, kCol, kSw, kGr>;
+  if (dyn) {
+    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(dyn));
+    if (e != cudaSuccess) return e;
+  }
+  const QOut ro{static_cast<uint8_t*>(a.out), static_cast<uint8_t*>(a.scales),
+                a.scale_item_bytes};
+  const QOut co{static_cast<uint8_t*>(a.out_col), static_cast<uint8_t*>(a.scales_col),
+                a.scale_item_bytes_col};
   dim3 grid(static_cast<unsigned>(col_tiles), static_cast<unsigned>(row_tiles),
             static_cast<unsigned>(a.batch));
-  if (a.axis == MXFP8_AXIS_ROW) {
-    auto k = quantize_rows_kernel<kSw, kGr>;
-    if (dyn) {
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(dyn));
-      if (e != cudaSuccess) return e;
-    }
-    k<<<grid, kThreads, dyn, stream>>>(src, a.rows, a.cols, out, sc, scale_item, a.offsets,
-                                        a.num_experts, a.status);
-  } else {
-    auto k = quantize_cols_kernel<kSw, kGr>;
-    if (dyn) {
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(dyn));
-      if (e != cudaSuccess) return e;
-    }
-    k<<<grid, kThreads, dyn, stream>>>(src, a.rows, a.cols, out, sc, scale_item, a.offsets,
-                                        a.num_experts, a.status);
-  }
+  k<<<grid, kThreads, dyn, stream>>>(static_cast<const uint16_t*>(a.src), a.rows, a.cols, ro, co,
+                                      a.offsets, a.num_experts, a.status);
   return cudaGetLastError();
+}
+
+template <bool kRow, bool kCol>
+cudaError_t launch_axes(const QuantizeArgs& a, cudaStream_t stream) {
+  if (a.offsets) return launch_tiles<kRow, kCol, true, true>(a, stream);
+  if (a.layout == MXFP8_SCALES_SWIZZLED) return launch_tiles<kRow, kCol, true, false>(a, stream);
+  return launch_tiles<kRow, kCol, false, false>(a, stream);
 }
 
 }  // namespace
@@ -380,10 +322,9 @@ int64_t scale_bytes_host(int64_t rows, int64_t cols, int axis, int layout);
 
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream) {
   if (a.rows == 0 || a.cols == 0 || a.batch == 0) return cudaSuccess;
-  if (a.offsets) return launch_one<true, true>(a, stream, 0);
-  const int64_t item = scale_bytes_host(a.rows, a.cols, a.axis, a.layout);
-  if (a.layout == MXFP8_SCALES_SWIZZLED) return launch_one<true, false>(a, stream, item);
-  return launch_one<false, false>(a, stream, item);
+  if (a.axis == kAxisBoth) return launch_axes<true, true>(a, stream);
+  if (a.axis == MXFP8_AXIS_ROW) return launch_axes<true, false>(a, stream);
+  return launch_axes<false, true>(a, stream);
 }
 
 }  // namespace mxfp8

@@ -1,0 +1,255 @@
+"""GPU parity of the MXFP8 block-scaled GEMMs against the float64 oracle, within
+|C - C_ref| <= 2^-9 * sum_k |a_k b_k| (plus half a BF16 ulp for BF16 outputs)
+("End-to-End MXFP8 RL on Blackwell", section "The pipeline": format paragraph and the
+learner's three GEMMs; MoE experts: section "A held-out workload, and end to end")."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.mxfp8_oracle as O
+from mxfp8_block_scaled_05_gb300 import workloads as W
+from tests.oracle_helpers import assert_gemm_within, bf16_bits, bits_to_bf16, gpu_ready
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def m():
+    mod = gpu_ready()
+    yield mod
+    assert mod.device_status() == mod.OK
+
+
+def _up(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _run(m, qa, sa, qb, sb, out_dtype, op=0):
+    """GPU GEMM on oracle-quantized operands (linear scales swizzled by the oracle)."""
+    return m.gemm(_up(qa), _up(O.swizzle_scales(sa)), _up(qb), _up(O.swizzle_scales(sb)), op,
+                  out_dtype)
+
+
+def _rand_q(g, rows, k, lo=110, hi=140):
+    q = g.integers(0, 256, size=(rows, k)).astype(np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x38
+    s = g.integers(lo, hi, size=(rows, k // 32)).astype(np.uint8)
+    return q, s
+
+
+def test_tiny_config_fprop(m):
+    a, w = W.tiny("cpu", seed=0)
+    qa, sa = O.quantize(bf16_bits(a), O.ROW)
+    qw, sw = O.quantize(bf16_bits(w), O.ROW)
+    ref, ab = O.gemm(qa, sa, qw, sw), O.gemm_abs(qa, sa, qw, sw)
+    for out_dtype, bf in ((m.OUT_BF16, True), (m.OUT_FP32, False)):
+        c = _run(m, qa, sa, qw, sw, out_dtype)
+        assert_gemm_within(c.double().cpu().numpy(), ref, ab, bf, "tiny")
+
+
+@pytest.mark.parametrize("mnk", [(128, 128, 32), (128, 128, 128), (144, 272, 96), (256, 256, 256),
+                                 (16, 16, 32), (400, 528, 1056), (2048, 4096, 256),
+                                 (512, 384, 4096), (1040, 112, 160)])
+def test_shapes_random_operands(m, mnk):
+    """Random finite codes and scales spanning 2^-17..2^12: any mistake in the scale
+    layout, a tile origin or a tail mask shows up as a gross error."""
+    mm, n, k = mnk
+    g = np.random.default_rng(mm * 7 + n * 3 + k)
+    qa, sa = _rand_q(g, mm, k)
+    qb, sb = _rand_q(g, n, k)
+    ref, ab = O.gemm(qa, sa, qb, sb), O.gemm_abs(qa, sa, qb, sb)
+    c = _run(m, qa, sa, qb, sb, m.OUT_FP32)
+    assert_gemm_within(c.double().cpu().numpy(), ref, ab, False, f"{mnk}")
+    cb = _run(m, qa, sa, qb, sb, m.OUT_BF16)
+    assert_gemm_within(cb.double().cpu().numpy(), ref, ab, True, f"{mnk} bf16")
+
+
+def test_extreme_scales(m):
+    """Scale bytes near both ends of what BF16 inputs produce (0..246)."""
+    g = np.random.default_rng(11)
+    qa, sa = _rand_q(g, 256, 256, 0, 20)
+    qb, sb = _rand_q(g, 256, 256, 200, 240)
+    ref, ab = O.gemm(qa, sa, qb, sb), O.gemm_abs(qa, sa, qb, sb)
+    c = _run(m, qa, sa, qb, sb, m.OUT_FP32)
+    assert_gemm_within(c.double().cpu().numpy(), ref, ab, False, "extreme")
+
+
+def test_gpu_quantize_then_gemm_small_layer(m):
+    """fprop, dgrad and wgrad of one small layer with every operand quantized on the GPU,
+    against the oracle computed from the same BF16 tensors."""
+    t, n, k = 256, 384, 512
+    g = torch.Generator().manual_seed(21)
+    x = (torch.randn(t, k, generator=g)).to(torch.bfloat16)
+    w = (torch.randn(n, k, generator=g) * 0.02).to(torch.bfloat16)
+    dy = torch.randn(t, n, generator=g).to(torch.bfloat16)
+    xb, wb, dyb = bf16_bits(x), bf16_bits(w), bf16_bits(dy)
+    xd, wd, dyd = x.to(DEV), w.to(DEV), dy.to(DEV)
+    cases = {
+        "fprop": (m.FPROP, (xd, m.ROW), (wd, m.ROW), (xb, O.ROW), (wb, O.ROW)),
+        "dgrad": (m.DGRAD, (dyd, m.ROW), (wd, m.COL), (dyb, O.ROW), (wb, O.COL)),
+        "wgrad": (m.WGRAD, (dyd, m.COL), (xd, m.COL), (dyb, O.COL), (xb, O.COL)),
+    }
+    for name, (op, (ga, gax), (gb, gbx), (ra, rax), (rb, rbx)) in cases.items():
+        qa, sa = m.quantize(ga, gax, m.SWIZZLED)
+        qb, sb = m.quantize(gb, gbx, m.SWIZZLED)
+        c = m.gemm(qa, sa, qb, sb, op, m.OUT_FP32)
+        oa, osa = O.quantize(ra, rax)
+        ob, osb = O.quantize(rb, rbx)
+        assert_gemm_within(c.double().cpu().numpy(), O.gemm(oa, osa, ob, osb),
+                           O.gemm_abs(oa, osa, ob, osb), False, name)
+
+
+def _sampled_check(m, c_gpu, a_rows_fn, b_rows_fn, mdim, ndim, seed, bf16_out, what):
+    """Checks two full 128 x 128 tiles (first and an interior one) and a 64 x 128 grid of
+    random entries of a full-size GEMM output; a_rows_fn(idx) / b_rows_fn(idx) give the
+    oracle-quantized rows (codes, linear scales) of the two K-major operands."""
+    g = np.random.default_rng(seed)
+    mt, nt = (mdim // 2) // 128 * 128, (ndim // 2) // 128 * 128
+    samples = [(np.arange(0, 128), np.arange(0, 128)),
+               (np.arange(mt, mt + 128), np.arange(nt, nt + 128)),
+               (np.sort(g.choice(mdim, 64, replace=False)), np.sort(g.choice(ndim, 128, replace=False)))]
+    for mi, ni in samples:
+        qa, sa = a_rows_fn(mi)
+        qb, sb = b_rows_fn(ni)
+        ref, ab = O.gemm(qa, sa, qb, sb), O.gemm_abs(qa, sa, qb, sb)
+        got = c_gpu[torch.from_numpy(mi).to(DEV)][:, torch.from_numpy(ni).to(DEV)]
+        assert_gemm_within(got.double().cpu().numpy(), ref, ab, bf16_out, what)
+
+
+def test_qwen3_8b_layer_set_full_size(m):
+    """Config: the Qwen3-8B linear layer set at 4096 tokens: every operand quantized on
+    the GPU, fprop / dgrad / wgrad at full size (BF16 out), sampled against the oracle."""
+    for name, n, k, x, w, dy in W.qwen3_8b_layer_set(4096, DEV, seed=1):
+        xc, wc, dyc = bf16_bits(x), bf16_bits(w), bf16_bits(dy)
+        t = x.shape[0]
+        qx, sx = m.quantize(x, m.ROW)
+        qw, sw = m.quantize(w, m.ROW)
+        y = m.gemm(qx, sx, qw, sw, m.FPROP)
+        _sampled_check(m, y, lambda i: O.quantize(xc[i], O.ROW), lambda i: O.quantize(wc[i], O.ROW),
+                       t, n, 1, True, f"{name} fprop")
+        del y
+        qdy, sdy = m.quantize(dy, m.ROW)
+        qwt, swt = m.quantize(w, m.COL)
+        dx = m.gemm(qdy, sdy, qwt, swt, m.DGRAD)
+        _sampled_check(m, dx, lambda i: O.quantize(dyc[i], O.ROW),
+                       lambda i: O.quantize(np.ascontiguousarray(wc[:, i]), O.COL),
+                       t, k, 2, True, f"{name} dgrad")
+        del dx
+        qdyt, sdyt = m.quantize(dy, m.COL)
+        qxt, sxt = m.quantize(x, m.COL)
+        dw = m.gemm(qdyt, sdyt, qxt, sxt, m.WGRAD)
+        _sampled_check(m, dw, lambda i: O.quantize(np.ascontiguousarray(dyc[:, i]), O.COL),
+                       lambda i: O.quantize(np.ascontiguousarray(xc[:, i]), O.COL),
+                       n, k, 3, True, f"{name} wgrad")
+        del dw, x, w, dy
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------------ grouped (MoE)
+
+def _grouped_case(counts, k, n, seed):
+    off = np.concatenate([[0], np.cumsum([W.pad32(c) for c in counts])]).astype(np.int32)
+    g = torch.Generator().manual_seed(seed)
+    total = int(off[-1])
+    x = torch.zeros(total, k, dtype=torch.bfloat16)
+    dy = torch.zeros(total, n, dtype=torch.bfloat16)
+    for e, c in enumerate(counts):
+        x[off[e]:off[e] + c] = torch.randn(c, k, generator=g).to(torch.bfloat16)
+        dy[off[e]:off[e] + c] = torch.randn(c, n, generator=g).to(torch.bfloat16)
+    w = (torch.randn(len(counts), n, k, generator=g) * 0.02).to(torch.bfloat16)
+    return off, x, w, dy
+
+
+@pytest.mark.parametrize("counts", [[64, 0, 160, 32, 0, 256, 96, 7], [300], [0, 0, 40]])
+def test_grouped_fprop_dgrad_wgrad_small(m, counts):
+    k, n = 256, 384
+    off, x, w, dy = _grouped_case(counts, k, n, seed=len(counts))
+    E = len(counts)
+    offs = torch.from_numpy(off).to(DEV)
+    xb, wb, dyb = bf16_bits(x), bf16_bits(w), bf16_bits(dy)
+    # fprop: Y = X_e W_e^T
+    qx, sx = m.quantize_grouped(x.to(DEV), offs, m.ROW)
+    qw, sw = m.quantize_batched(w.to(DEV), m.ROW, m.SWIZZLED)
+    y = m.grouped_gemm(qx, sx, qw, sw, offs, m.FPROP, m.OUT_FP32)
+    oq, osx = O.quantize(xb, O.ROW)
+    ow = [O.quantize(wb[e], O.ROW) for e in range(E)]
+    ref, ab = O.grouped_gemm_rows(oq, osx, np.stack([c for c, _ in ow]),
+                                  np.stack([s for _, s in ow]), off)
+    assert_gemm_within(y.double().cpu().numpy(), ref, ab, False, "grouped fprop")
+    # dgrad: dX = dY_e W_e  (B = W_e^T, column-wise per expert)
+    qdy, sdy = m.quantize_grouped(dy.to(DEV), offs, m.ROW)
+    qwt, swt = m.quantize_batched(w.to(DEV), m.COL, m.SWIZZLED)
+    dx = m.grouped_gemm(qdy, sdy, qwt, swt, offs, m.DGRAD, m.OUT_FP32)
+    od, osd = O.quantize(dyb, O.ROW)
+    owt = [O.quantize(wb[e], O.COL) for e in range(E)]
+    ref, ab = O.grouped_gemm_rows(od, osd, np.stack([c for c, _ in owt]),
+                                  np.stack([s for _, s in owt]), off)
+    assert_gemm_within(dx.double().cpu().numpy(), ref, ab, False, "grouped dgrad")
+    # wgrad: dW_e = dY_e^T X_e over the expert's tokens
+    qdyt, sdyt = m.quantize_grouped(dy.to(DEV), offs, m.COL)
+    qxt, sxt = m.quantize_grouped(x.to(DEV), offs, m.COL)
+    dw = m.grouped_gemm(qdyt, sdyt, qxt, sxt, offs, m.WGRAD, m.OUT_FP32)
+    oa, osa = O.quantize(dyb, O.COL)
+    ob, osb = O.quantize(xb, O.COL)
+    ref, ab = O.grouped_gemm_wgrad(oa, osa, ob, osb, off)
+    assert_gemm_within(dw.double().cpu().numpy(), ref, ab, False, "grouped wgrad")
+    for e, c in enumerate(counts):
+        if c == 0:
+            assert torch.all(dw[e] == 0)
+    assert m.device_status() == m.OK
+
+
+def test_grouped_bad_offsets_latched(m):
+    qa = torch.zeros((128, 64), dtype=torch.uint8, device=DEV)
+    sa = torch.zeros(m.grouped_scale_bytes(128, 64, 2, m.ROW), dtype=torch.uint8, device=DEV)
+    qb = torch.zeros((2, 128, 64), dtype=torch.uint8, device=DEV)
+    sb = torch.zeros(2 * m.scale_bytes(128, 64), dtype=torch.uint8, device=DEV)
+    offs = torch.tensor([0, 96, 64], dtype=torch.int32, device=DEV)   # decreasing
+    out = torch.full((128, 128), 7.0, dtype=torch.float32, device=DEV)
+    m.grouped_gemm(qa, sa, qb, sb, offs, m.FPROP, m.OUT_FP32, out=out)
+    assert m.device_status() == m.ERR_BAD_OFFSETS
+    assert torch.all(out == 7.0)
+    assert m.device_status() == m.OK
+
+
+def test_qwen3_30b_a3b_experts_full_size_sampled(m):
+    """Config: 128 experts, 8192 tokens routed top-8 with Zipf(1.1) counts, segments
+    padded to 32; gate_up (2048 -> 1536) fprop / dgrad / wgrad at full size, sampled
+    against the oracle for the most and least loaded non-empty experts."""
+    d = W.moe_expert_layer(DEV)
+    counts, off = d["counts"].numpy(), d["offsets"].numpy()
+    offs = d["offsets"].to(DEV)
+    x, w, dy = d["x"], d["w_gate_up"], d["dy_gate_up"]
+    E, n, k = w.shape
+    qx, sx = m.quantize_grouped(x, offs, m.ROW)
+    qw, sw = m.quantize_batched(w, m.ROW)
+    y = m.grouped_gemm(qx, sx, qw, sw, offs, m.FPROP)
+    qdyt, sdyt = m.quantize_grouped(dy, offs, m.COL)
+    qxt, sxt = m.quantize_grouped(x, offs, m.COL)
+    dw = m.grouped_gemm(qdyt, sdyt, qxt, sxt, offs, m.WGRAD)
+    assert m.device_status() == m.OK
+    nz = np.nonzero(counts)[0]
+    picks = [nz[np.argmax(counts[nz])], nz[np.argmin(counts[nz])]]
+    rng = np.random.default_rng(4)
+    for e in picks:
+        lo, hi = int(off[e]), int(off[e + 1])
+        xe = bf16_bits(x[lo:hi])
+        we = bf16_bits(w[e])
+        dye = bf16_bits(dy[lo:hi])
+        rows = np.sort(rng.choice(hi - lo, min(64, hi - lo), replace=False))
+        cols = np.sort(rng.choice(n, 128, replace=False))
+        qa, sa = O.quantize(xe[rows], O.ROW)
+        qb, sb = O.quantize(we[cols], O.ROW)
+        got = y[torch.from_numpy(lo + rows).to(DEV)][:, torch.from_numpy(cols).to(DEV)]
+        assert_gemm_within(got.double().cpu().numpy(), O.gemm(qa, sa, qb, sb),
+                           O.gemm_abs(qa, sa, qb, sb), True, f"moe fprop e{e}")
+        ni = np.sort(rng.choice(n, 64, replace=False))
+        ki = np.sort(rng.choice(k, 128, replace=False))
+        qa, sa = O.quantize(np.ascontiguousarray(dye[:, ni]), O.COL)
+        qb, sb = O.quantize(np.ascontiguousarray(xe[:, ki]), O.COL)
+        got = dw[e][torch.from_numpy(ni).to(DEV)][:, torch.from_numpy(ki).to(DEV)]
+        assert_gemm_within(got.double().cpu().numpy(), O.gemm(qa, sa, qb, sb),
+                           O.gemm_abs(qa, sa, qb, sb), True, f"moe wgrad e{e}")
+    for e in np.nonzero(counts == 0)[0]:
+        assert torch.all(dw[int(e)] == 0)
