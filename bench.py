@@ -229,7 +229,8 @@ def recorded_traffic(kernel_key: str):
     sha = gemm_source_sha()
     for line in open(p):
         f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
-        if f.get("kernel") == kernel_key and f.get("source_sha") == sha:
+        if (f.get("kernel") == kernel_key and f.get("source_sha") == sha
+                and f.get("workload") == "step_average"):
             return float(f["dram_bytes_per_launch"])
     return None
 

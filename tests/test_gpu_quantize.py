@@ -130,7 +130,7 @@ def test_grouped_segments(m, axis):
     counts = [64, 0, 160, 32, 0, 256, 96, 0]
     off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     total = int(off[-1])
-    x = _rand_bf16(np.random.default_rng(7), (total, 200))
+    x = _rand_bf16(np.random.default_rng(7), (total, 224))
     offs = torch.from_numpy(off).to(DEV)
     q, s = m.quantize_grouped(x.to(DEV), offs, axis)
     rq, rs = O.quantize(bf16_bits(x), axis)
