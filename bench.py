@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "quantize GB/s + MXFP8 GEMM TFLOP/s on Qwen3-8B linears, % of GB300 roofline"
 FP8_OVER_BF16 = 2.0   # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
 QBYTES_PER_ELEM = 2.0 + 1.0 + 1.0 / 32.0   # BF16 read + E4M3 + E8M0/32 written
+DUAL_BYTES_PER_ELEM = 2.0 + 2 * (1.0 + 1.0 / 32.0)   # one BF16 read, two quantized copies
 REF_ROW_FRAC = 1.0 / 8192   # reference arm: 32 rows of every operand per step
 REF_BLOCK = (8, 16)         # reference arm: output block sampled per GEMM
 
@@ -158,9 +159,10 @@ def layer_quant_elems(t, n, k):
 class DenseStep:
     """Buffers and launches of one step; every launch goes through the C ABI."""
 
-    def __init__(self, m, tokens: int, seed: int, dev):
+    def __init__(self, m, tokens: int, seed: int, dev, dual: bool = True):
         from mxfp8_block_scaled_05_gb300 import workloads as W
         self.m = m
+        self.dual = dual
         self.layers = []
         for name, n, k, x, w, dy in W.qwen3_8b_layer_set(tokens, dev, seed):
             t = x.shape[0]
@@ -178,32 +180,44 @@ class DenseStep:
             self.layers.append(L)
         self.flops = sum(layer_flops(L["t"], L["n"], L["k"]) for L in self.layers)
         self.qelems = sum(layer_quant_elems(L["t"], L["n"], L["k"]) for L in self.layers)
-        self.launches = 9 * len(self.layers)
+        self.launches = (6 if dual else 9) * len(self.layers)
 
     def run(self, stream, events=None):
         """Enqueues one step. With `events` (a list), appends (kind, units, start, end)."""
         m = self.m
         for L in self.layers:
-            for key in ("xr", "xc", "wr", "wc", "dyr", "dyc"):
-                q, s, src, axis = L[key]
-                ev = self._ev(events, stream, "quantize", src.numel())
-                m.quantize(src, axis, m.SWIZZLED, out=q, scales=s, stream=stream)
-                self._end(events, stream, ev)
+            if self.dual:
+                # one read of each BF16 tensor gives both of its quantized copies
+                for src_key, rk, ck in (("x", "xr", "xc"), ("w", "wr", "wc"), ("dy", "dyr", "dyc")):
+                    src = L[src_key]
+                    ev = self._ev(events, stream, "quantize", src.numel() * DUAL_BYTES_PER_ELEM,
+                                  f"{L['name']}.{src_key} dual {src.shape[0]}x{src.shape[1]}")
+                    m.quantize_dual(src, m.SWIZZLED, row_out=L[rk][0], row_scales=L[rk][1],
+                                    col_out=L[ck][0], col_scales=L[ck][1], stream=stream)
+                    self._end(events, stream, ev)
+            else:
+                for key in ("xr", "xc", "wr", "wc", "dyr", "dyc"):
+                    q, s, src, axis = L[key]
+                    ev = self._ev(events, stream, "quantize", src.numel() * QBYTES_PER_ELEM,
+                                  f"{L['name']}.{key} {src.shape[0]}x{src.shape[1]}")
+                    m.quantize(src, axis, m.SWIZZLED, out=q, scales=s, stream=stream)
+                    self._end(events, stream, ev)
             t, n, k = L["t"], L["n"], L["k"]
             for op, a, b, out, mnk in ((m.FPROP, "xr", "wr", L["y"], (t, n, k)),
                                        (m.DGRAD, "dyr", "wc", L["dx"], (t, k, n)),
                                        (m.WGRAD, "dyc", "xc", L["dw"], (n, k, t))):
-                ev = self._ev(events, stream, "gemm", 2.0 * mnk[0] * mnk[1] * mnk[2])
+                ev = self._ev(events, stream, "gemm", 2.0 * mnk[0] * mnk[1] * mnk[2],
+                              f"{L['name']}.{('fprop', 'dgrad', 'wgrad')[op]} {mnk[0]}x{mnk[1]}x{mnk[2]}")
                 m.gemm(L[a][0], L[a][1], L[b][0], L[b][1], op, m.OUT_BF16, out=out, stream=stream)
                 self._end(events, stream, ev)
 
     @staticmethod
-    def _ev(events, stream, kind, units):
+    def _ev(events, stream, kind, units, label=""):
         if events is None:
             return None
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
-        return (kind, units, s, e)
+        return (kind, units, s, e, label)
 
     @staticmethod
     def _end(events, stream, ev):
@@ -328,7 +342,7 @@ def run_ours(args, rank, ws):
     import mxfp8_block_scaled_05_gb300 as m
     dev = torch.device("cuda", torch.cuda.current_device())
     pk = peaks()
-    step = DenseStep(m, args.tokens, seed=1 + rank, dev=dev)
+    step = DenseStep(m, args.tokens, seed=1 + rank, dev=dev, dual=args.quant == "dual")
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         step.run(stream)
@@ -351,15 +365,26 @@ def run_ours(args, rank, ws):
     if status != m.OK:
         raise RuntimeError(f"device status {status} after the timed region")
 
-    q_ms = sum(s.elapsed_time(e) for k, _, s, e in events if k == "quantize")
-    g_ms = sum(s.elapsed_time(e) for k, _, s, e in events if k == "gemm")
-    g_units = sum(u for k, u, _, _ in events if k == "gemm")
+    q_ms = sum(s.elapsed_time(e) for k, _, s, e, _ in events if k == "quantize")
+    g_ms = sum(s.elapsed_time(e) for k, _, s, e, _ in events if k == "gemm")
+    g_units = sum(u for k, u, _, _, _ in events if k == "gemm")
     g_launches = sum(1 for k, *_ in events if k == "gemm")
-    q_units = sum(u for k, u, _, _ in events if k == "quantize")
+    q_units = sum(u for k, u, _, _, _ in events if k == "quantize")
+    per = {}
+    for k, u, s, e, label in events:
+        d = per.setdefault(label, [k, u, 0.0, 0])
+        d[2] += s.elapsed_time(e)
+        d[3] += 1
+    breakdown = {}
+    for label, (k, u, tot, cnt) in per.items():
+        ms = tot / cnt
+        breakdown[label] = ({"us": round(ms * 1e3, 1), "TFLOP/s": round(u / (ms * 1e-3) / 1e12, 1)}
+                            if k == "gemm" else
+                            {"us": round(ms * 1e3, 1), "GB/s": round(u / (ms * 1e-3) / 1e9, 1)})
     step_ms = ms_max / args.steps
     value = ws * step.flops / (step_ms * 1e-3) / 1e12
     gemm_tflops = g_units / (g_ms * 1e-3) / 1e12
-    quant_gbs = q_units * QBYTES_PER_ELEM / (q_ms * 1e-3) / 1e9
+    quant_gbs = q_units / (q_ms * 1e-3) / 1e9
     fp8_peak = pk["bf16_sus"] * FP8_OVER_BF16
     traffic = recorded_traffic("mxfp8_gemm_kernel")
     e2e = run_e2e(args, m, step, dev, stream, ws)
@@ -373,8 +398,10 @@ def run_ours(args, rank, ws):
         "gpu_launches": step.launches * args.steps,
         "quantize": {"GB/s": quant_gbs, "frac_of_hbm": quant_gbs / pk["hbm"],
                      "ms_per_step": q_ms / args.steps,
-                     "bytes_per_elem": QBYTES_PER_ELEM, "peak_GB/s": pk["hbm"],
-                     "peak_src": pk["src"]},
+                     "mode": "dual (one read, both copies)" if step.dual else "separate",
+                     "bytes_per_elem": DUAL_BYTES_PER_ELEM if step.dual else QBYTES_PER_ELEM,
+                     "bytes_per_step": q_units / args.steps,
+                     "peak_GB/s": pk["hbm"], "peak_src": pk["src"]},
         "gemm": {"TFLOP/s": gemm_tflops, "frac_of_mxfp8": gemm_tflops / fp8_peak,
                  "ms_per_step": g_ms / args.steps, "flops_per_step": step.flops},
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
@@ -386,6 +413,7 @@ def run_ours(args, rank, ws):
                      "flops_per_launch": g_units / g_launches},
         "clocks": clk.summary(),
         "e2e": e2e,
+        "per_launch": breakdown,
     }
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline_obj()
@@ -551,6 +579,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--tokens", type=int, default=4096)
     ap.add_argument("--workload", choices=("dense", "moe", "sync", "sweep"), default="dense")
+    ap.add_argument("--quant", choices=("dual", "separate"), default="dual",
+                    help="quantize each tensor once for both copies (dual) or per copy")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

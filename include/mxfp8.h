@@ -210,6 +210,35 @@ int mxfp8_grouped_gemm(const void* A_dev, const void* sA_dev, const void* B_dev,
                        int out_dtype, void* stream);
 
 /*
+ * Workspace bytes mxfp8_selfcheck needs for `tokens` random input rows against an
+ * [N][K] weight (0 for invalid sizes: tokens % 16, N % 16 and K % 32 must be 0).
+ */
+size_t mxfp8_selfcheck_workspace_bytes(int64_t tokens, int64_t N, int64_t K);
+
+/*
+ * Post-synchronization self-check of one quantized weight (section "Correctness: how it
+ * fails", the post-sync self-check, condition C3). The BF16 input x [tokens][K] is
+ * quantized and multiplied, by this library's kernels, with the weight exactly as the
+ * GEMM reads it: w_codes_dev (E4M3 [N][K]) and w_scales_dev (SWIZZLED), i.e. the derived
+ * layout - one dense layer, or one expert's slice of a batched expert weight. The result
+ * is compared with a reference that multiplies the BF16 input with the canonical
+ * synchronized weight, ref_codes_dev (E4M3 [N][K]) and ref_scales_dev (LINEAR
+ * [N][K/32]), dequantized, with FP32 accumulation. Writes
+ * ||Y - Y_ref||_F / ||Y_ref||_F to *rel_err_dev (device float). A healthy weight gives a
+ * few percent (the activations' quantization error); a derived layout that is stale or
+ * misplaced relative to the synchronized weight gives order 1; the pages' tolerance is
+ * 0.25. Requires tokens % 16 == 0, N % 16 == 0, K % 32 == 0.
+ *   workspace_dev  caller-owned, >= mxfp8_selfcheck_workspace_bytes(tokens, N, K)
+ *                  bytes, 256-byte aligned; holds the quantized input, the FP32 output
+ *                  and the two reduction sums. Overwritten.
+ * Asynchronous on `stream` like the other calls.
+ */
+int mxfp8_selfcheck(const void* w_codes_dev, const void* w_scales_dev,
+                    const void* ref_codes_dev, const void* ref_scales_dev, int64_t N, int64_t K,
+                    const void* x_bf16_dev, int64_t tokens, void* workspace_dev,
+                    size_t workspace_bytes, float* rel_err_dev, void* stream);
+
+/*
  * Synchronizes `stream`, then returns and clears the current device's status word:
  * MXFP8_OK, or the first device-side error latched since the last call
  * (MXFP8_ERR_BAD_OFFSETS, MXFP8_ERR_TIMEOUT), or MXFP8_ERR_CUDA if the synchronization

@@ -39,6 +39,8 @@ SIGNATURES = {
     "mxfp8_quantize_grouped": (_I, [_P, _I64, _I64, _I, _P, _I, _P, _P, _P]),
     "mxfp8_gemm": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _P]),
     "mxfp8_grouped_gemm": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _P]),
+    "mxfp8_selfcheck_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
+    "mxfp8_selfcheck": (_I, [_P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _SZ, _P, _P]),
     "mxfp8_get_device_status": (_I, [_P]),
 }
 
@@ -256,6 +258,34 @@ def grouped_gemm(a, sa, b, sb, offsets: torch.Tensor, op: int = FPROP,
     _check(lib().mxfp8_grouped_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out),
                                     _ptr(offsets), e, total, n_, k_, op, out_dtype,
                                     _stream(stream)), "mxfp8_grouped_gemm")
+    return out
+
+
+SELF_CHECK_TOLERANCE = 0.25  # section "Correctness: how it fails": the self-check's tolerance
+
+
+def selfcheck(w_codes: torch.Tensor, w_scales: torch.Tensor, ref_codes: torch.Tensor,
+              ref_scales: torch.Tensor, x: torch.Tensor, workspace=None,
+              stream=None) -> torch.Tensor:
+    """Relative error ||Y - Y_ref|| / ||Y_ref|| of the MXFP8 layer as the GEMM reads it
+    (w_codes + swizzled w_scales) on the quantized input x, against x times the canonical
+    synchronized weight (ref_codes + linear ref_scales) dequantized. Returns a one-element
+    float32 CUDA tensor (no host synchronization); compare with SELF_CHECK_TOLERANCE."""
+    _require(w_codes, torch.uint8, "w_codes")
+    _require(ref_codes, torch.uint8, "ref_codes")
+    _require(x, torch.bfloat16, "x")
+    n, k = w_codes.shape
+    t = x.shape[0]
+    need = lib().mxfp8_selfcheck_workspace_bytes(t, n, k)
+    if need == 0:
+        raise ValueError(f"no self-check for tokens={t} N={n} K={k}")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    out = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(lib().mxfp8_selfcheck(_ptr(w_codes), _ptr(w_scales), _ptr(ref_codes),
+                                 _ptr(ref_scales), n, k, _ptr(x), t, _ptr(workspace),
+                                 workspace.numel(), _ptr(out), _stream(stream)),
+           "mxfp8_selfcheck")
     return out
 
 

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmxfp8.so")
-SOURCES = ("api.cu", "quantize.cu", "gemm.cu")
+SOURCES = ("api.cu", "quantize.cu", "gemm.cu", "selfcheck.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -41,7 +41,8 @@ namespace {
 
 constexpr int BM = 128;           // accumulator rows = TMEM lanes
 constexpr int BK = 128;           // K elements (bytes) per pipeline stage
-constexpr int kThreads = 192;     // 6 warps
+constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, each half of the columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxExperts = 1024;
 
 enum Mode : int { kDense = 0, kGroupRows = 1, kGroupWgrad = 2 };
@@ -103,6 +104,7 @@ struct Tile {
   int64_t sfb_row_tiles_stride;  // tiles between consecutive 128-row B tiles
   int64_t c_off;         // element offset of the problem's C
   int64_t ldc;
+  bool a_valid;          // the A row tile exists (a CTA pair may overhang M by one tile)
   bool live;
 };
 
@@ -125,6 +127,7 @@ template <int BN, int kMode>
 __device__ Tile make_tile(const Params& p, const SegShared* seg, int64_t id) {
   Tile t;
   t.live = false;
+  t.a_valid = true;
   const int64_t n_kt_dense = (p.K + BK - 1) / BK;
   if (kMode == kDense) {
     if (id >= p.num_tiles) return t;
@@ -211,11 +214,60 @@ __device__ Tile make_tile(const Params& p, const SegShared* seg, int64_t id) {
   return t;
 }
 
-template <int BN, int kMode>
+// Dense tiles of a CTA pair (cluster of 2): the pair shares one N tile and takes two
+// adjacent M tiles; CTA rank r of the cluster owns M tile 2 * pm + r.
+template <int BN>
+__device__ Tile make_tile_pair(const Params& p, int64_t pid, uint32_t crank) {
+  Tile t;
+  t.live = false;
+  const int64_t n_pm = (p.num_m_tiles + 1) / 2;
+  if (pid >= n_pm * p.num_n_tiles) return t;
+  constexpr int64_t GP = 4;  // bands of 4 pairs (8 M tiles) sweep across N
+  const int64_t band = GP * p.num_n_tiles;
+  const int64_t first = (pid / band) * GP;
+  const int64_t gp = (n_pm - first) < GP ? (n_pm - first) : GP;
+  const int64_t pm = first + (pid % band) % gp;
+  const int64_t nt = (pid % band) / gp;
+  const int64_t mt = 2 * pm + crank;
+  const int64_t n_kt = (p.K + BK - 1) / BK;
+  t.m0 = mt * BM;
+  t.n0 = nt * BN;
+  const int64_t left = p.M - t.m0;
+  t.rows_valid = static_cast<int>(left <= 0 ? 0 : (left < BM ? left : BM));
+  t.cols_valid = static_cast<int>((p.N - t.n0) < BN ? (p.N - t.n0) : BN);
+  t.a_row = t.m0;
+  t.k_origin = 0;
+  t.nk = static_cast<int>(n_kt);
+  t.last_blocks = static_cast<int>(((p.K - (n_kt - 1) * BK) + 31) / 32);
+  t.b_z = 0;
+  t.sfa_tile0 = mt * n_kt;
+  t.sfa_kstride = 1;
+  t.sfb_base = p.sB + nt * (BN / 128) * n_kt * 512;
+  t.sfb_row_tiles_stride = n_kt;
+  t.c_off = 0;
+  t.ldc = p.N;
+  t.a_valid = mt < p.num_m_tiles;
+  t.live = true;
+  return t;
+}
+
+template <int BN, int kMode, bool kPair>
+__device__ __forceinline__ Tile tile_of(const Params& p, const SegShared* seg, int64_t id,
+                                        uint32_t crank) {
+  if (kPair) return make_tile_pair<BN>(p, id, crank);
+  return make_tile<BN, kMode>(p, seg, id);
+}
+
+template <int BN, int kMode, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                   const __grid_constant__ CUtensorMap map_b, const Params p) {
   using C = Cfg<BN>;
+  static_assert(!kPair || kMode == kDense, "CTA pairs are used for the dense GEMM only");
+  // persistent tile loop: CTAs (or CTA pairs) stride over the tile list
+  const uint32_t crank = kPair ? cluster_ctarank() : 0;
+  const int64_t first_id = kPair ? (blockIdx.x >> 1) : blockIdx.x;
+  const int64_t id_step = kPair ? (gridDim.x >> 1) : gridDim.x;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -236,10 +288,10 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kPair ? 2 : 1);  // a pair's stage is freed by both MMA issuers
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);
+    mbar_init(acc_empty, kEpiWarps);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -276,6 +328,8 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
+  // the peer's barriers must be initialised before any multicast copy or commit lands
+  if (kPair) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -283,26 +337,30 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     // ------------------------------------------------------------- TMA producer
     uint32_t it = 0;
     bool ok = true;
-    for (int64_t id = blockIdx.x; ok; id += gridDim.x) {
-      const Tile t = make_tile<BN, kMode>(p, seg, id);
+    for (int64_t id = first_id; ok; id += id_step) {
+      const Tile t = tile_of<BN, kMode, kPair>(p, seg, id, crank);
       if (!t.live) break;
       for (int kb = 0; kb < t.nk; ++kb, ++it) {
         const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1;
         if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
         int n_sfb = 0;
         for (int h = 0; h < C::kSfbTiles; ++h) n_sfb += (t.n0 + 128 * h < p.N);
-        const uint32_t bytes = C::kABytes + C::kBBytes + 512 + 512 * n_sfb;
+        const uint32_t bytes = C::kABytes + C::kBBytes + (t.a_valid ? 512 : 0) + 512 * n_sfb;
         mbar_arrive_expect_tx(&full[s], bytes);
         const int32_t kx = static_cast<int32_t>(t.k_origin + static_cast<int64_t>(kb) * BK);
         tma_load_2d(smem + C::kOffA + s * C::kABytes, &map_a, kx,
                     static_cast<int32_t>(t.a_row), &full[s]);
-        if (kMode == kGroupRows)
+        if (kPair)  // my half of the shared B tile, into both CTAs of the pair
+          tma_load_2d_mc(smem + C::kOffB + s * C::kBBytes + crank * (C::kBBytes / 2), &map_b, kx,
+                         static_cast<int32_t>(t.n0 + crank * (BN / 2)), &full[s], 0x3);
+        else if (kMode == kGroupRows)
           tma_load_3d(smem + C::kOffB + s * C::kBBytes, &map_b, kx, static_cast<int32_t>(t.n0),
                       t.b_z, &full[s]);
         else
           tma_load_2d(smem + C::kOffB + s * C::kBBytes, &map_b, kx, static_cast<int32_t>(t.n0),
                       &full[s]);
-        bulk_load(smem + C::kOffSfa + s * 512, p.sA + (t.sfa_tile0 + kb) * 512, 512, &full[s]);
+        if (t.a_valid)
+          bulk_load(smem + C::kOffSfa + s * 512, p.sA + (t.sfa_tile0 + kb) * 512, 512, &full[s]);
         for (int h = 0; h < n_sfb; ++h)
           bulk_load(smem + C::kOffSfb + s * C::kSfbBytes + h * 512,
                     t.sfb_base + (h * t.sfb_row_tiles_stride + kb) * 512, 512, &full[s]);
@@ -324,8 +382,8 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     bool ok = true;
     const uint32_t sa_base = smem_u32(smem + C::kOffA);
     const uint32_t sb_base = smem_u32(smem + C::kOffB);
-    for (int64_t id = blockIdx.x; ok; id += gridDim.x) {
-      const Tile t = make_tile<BN, kMode>(p, seg, id);
+    for (int64_t id = first_id; ok; id += id_step) {
+      const Tile t = tile_of<BN, kMode, kPair>(p, seg, id, crank);
       if (!t.live) break;
       if (t.nk == 0) continue;
       if (!mbar_wait_bounded(acc_empty, (acc_it & 1) ^ 1, abort_flag, p.wait_ns)) {
@@ -352,7 +410,10 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
           mma_mxf8(tmem, ad, bd, mxf8_idesc(BM, BN, k, k), sfa_t, sfb_t,
                    (kb > 0 || k > 0) ? 1u : 0u);
         }
-        mma_commit(&empty[s]);
+        if (kPair)
+          mma_commit_mc(&empty[s], 0x3);  // frees the stage in both CTAs of the pair
+        else
+          mma_commit(&empty[s]);
       }
       if (!ok) break;
       mma_commit(acc_full);
@@ -367,11 +428,13 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     mbar_wait_timed(mma_done, 0, p.wait_ns);
   } else if (warp >= 2) {
     // ------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // which half of the BN columns
+    constexpr int kChunks = BN / 64;   // 32-column chunks per warp
     uint32_t acc_it = 0;
     bool ok = true;
-    for (int64_t id = blockIdx.x; ok; id += gridDim.x) {
-      const Tile t = make_tile<BN, kMode>(p, seg, id);
+    for (int64_t id = first_id; ok; id += id_step) {
+      const Tile t = tile_of<BN, kMode, kPair>(p, seg, id, crank);
       if (!t.live) break;
       const int r = 32 * q + lane;
       const bool row_ok = r < t.rows_valid;
@@ -384,18 +447,24 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         if (!got) { ok = false; break; }
         tc_fence_after();
       }
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
+      for (int c2 = 0; c2 < kChunks; c2 += 2) {
+        uint32_t v[2][32];
         __syncwarp();
         if (t.nk > 0) {
-          tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * c, v);
+          const uint32_t base = tmem + (static_cast<uint32_t>(32 * q) << 16) +
+                                (half * kChunks + c2) * 32;
+          tmem_ld_32x32b_x32(base, v[0]);
+          tmem_ld_32x32b_x32(base + 32, v[1]);
           tmem_ld_wait();
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0;
+          for (int i = 0; i < 32; ++i) v[0][i] = v[1][i] = 0;
         }
-        const int cols_left = t.cols_valid - 32 * c;
-        if (row_ok && cols_left > 0) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int c = half * kChunks + c2 + u;
+          const int cols_left = t.cols_valid - 32 * c;
+          if (!row_ok || cols_left <= 0) continue;
           if (p.out_fp32) {
             float* dst = static_cast<float*>(p.C) + t.c_off + row * t.ldc + t.n0 + 32 * c;
             const int nvec = cols_left >= 32 ? 8 : cols_left / 4;
@@ -403,13 +472,13 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             for (int i = 0; i < 8; ++i)
               if (i < nvec)
                 reinterpret_cast<uint4*>(dst)[i] =
-                    make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    make_uint4(v[u][4 * i], v[u][4 * i + 1], v[u][4 * i + 2], v[u][4 * i + 3]);
           } else {
             uint16_t* dst = static_cast<uint16_t*>(p.C) + t.c_off + row * t.ldc + t.n0 + 32 * c;
             uint32_t b[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              b[i] = cvt_bf16x2(__uint_as_float(v[2 * i + 1]), __uint_as_float(v[2 * i]));
+              b[i] = cvt_bf16x2(__uint_as_float(v[u][2 * i + 1]), __uint_as_float(v[u][2 * i]));
             const int nvec = cols_left >= 32 ? 4 : cols_left / 8;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -434,6 +503,8 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 
   tc_fence_before();
   __syncthreads();
+  // no CTA of a pair may leave while its peer can still multicast into it or arrive on it
+  if (kPair) cluster_sync();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -489,14 +560,14 @@ uint64_t wait_limit_ns() {
   return ns;
 }
 
-template <int BN, int kMode>
+template <int BN, int kMode, bool kPair>
 int launch(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int64_t grid,
            cudaStream_t stream) {
   using C = Cfg<BN>;
-  auto k = mxfp8_gemm_kernel<BN, kMode>;
+  auto k = mxfp8_gemm_kernel<BN, kMode, kPair>;
   static bool attr_set[64] = {};  // per device
   int dev = 0;
-  cudaGetDevice(&dev);
+  if (cudaGetDevice(&dev) != cudaSuccess) return MXFP8_ERR_CUDA;
   if (dev < 64 && !attr_set[dev]) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
@@ -504,8 +575,59 @@ int launch(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int64_
     attr_set[dev] = true;
   }
   if (grid <= 0) return MXFP8_OK;
-  k<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(ma, mb, p);
-  return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
+  if (!kPair) {
+    k<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(ma, mb, p);
+    return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, ma, mb, p) == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
+}
+
+// How many CTA pairs of the dense kernel fit on the device at once (cached per device).
+template <int BN>
+int64_t max_pairs() {
+  static int64_t cached[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  using C = Cfg<BN>;
+  auto k = mxfp8_gemm_kernel<BN, kDense, true>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 256, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess || clusters <= 0)
+    clusters = num_sms() / 2;
+  if (dev >= 0 && dev < 64) cached[dev] = clusters;
+  return clusters;
+}
+
+bool pairs_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("MXFP8_GEMM_PAIRS");
+    return !(e && e[0] == '0');
+  }();
+  return on;
 }
 
 }  // namespace
@@ -528,10 +650,19 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.num_tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
   CUtensorMap ma, mb;
   if (!make_map(&ma, a.A, 2, a.K, a.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
+  // A CTA pair shares each B tile: each CTA loads half of it and multicasts it to both.
+  const bool pair = wide && pairs_enabled() && p.num_m_tiles >= 2;
+  if (pair) {
+    if (!make_map(&mb, a.B, 2, a.K, a.N, 1, BK, bn / 2)) return MXFP8_ERR_CUDA;
+    const int64_t pair_tiles = static_cast<int64_t>((p.num_m_tiles + 1) / 2) * p.num_n_tiles;
+    const int64_t mp = max_pairs<256>();
+    const int64_t pairs = pair_tiles < mp ? pair_tiles : mp;
+    return launch<256, kDense, true>(ma, mb, p, 2 * pairs, stream);
+  }
   if (!make_map(&mb, a.B, 2, a.K, a.N, 1, BK, bn)) return MXFP8_ERR_CUDA;
   const int64_t grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-  return wide ? launch<256, kDense>(ma, mb, p, grid, stream)
-              : launch<128, kDense>(ma, mb, p, grid, stream);
+  return wide ? launch<256, kDense, false>(ma, mb, p, grid, stream)
+              : launch<128, kDense, false>(ma, mb, p, grid, stream);
 }
 
 int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
@@ -561,8 +692,8 @@ int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     if (!make_map(&ma, a.A, 2, a.total_rows, p.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
     if (!make_map(&mb, a.B, 2, a.total_rows, p.N, 1, BK, bn)) return MXFP8_ERR_CUDA;
     const int64_t grid = tiles < num_sms() ? tiles : num_sms();
-    return wide ? launch<256, kGroupWgrad>(ma, mb, p, grid, stream)
-                : launch<128, kGroupWgrad>(ma, mb, p, grid, stream);
+    return wide ? launch<256, kGroupWgrad, false>(ma, mb, p, grid, stream)
+                : launch<128, kGroupWgrad, false>(ma, mb, p, grid, stream);
   }
   // fprop / dgrad: A [T][K] segmented by rows, B [E][N][K], C [T][N]
   p.M = a.total_rows;
@@ -579,8 +710,8 @@ int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   if (!make_map(&ma, a.A, 2, a.K, a.total_rows, 1, BK, BM)) return MXFP8_ERR_CUDA;
   if (!make_map(&mb, a.B, 3, a.K, a.N, a.num_experts, BK, bn)) return MXFP8_ERR_CUDA;
   const int64_t grid = tiles < num_sms() ? tiles : num_sms();
-  return wide ? launch<256, kGroupRows>(ma, mb, p, grid, stream)
-              : launch<128, kGroupRows>(ma, mb, p, grid, stream);
+  return wide ? launch<256, kGroupRows, false>(ma, mb, p, grid, stream)
+              : launch<128, kGroupRows, false>(ma, mb, p, grid, stream);
 }
 
 }  // namespace mxfp8

@@ -47,6 +47,22 @@ struct GemmArgs {
 int launch_gemm(const GemmArgs& a, cudaStream_t stream);
 int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream);
 
+struct SelfcheckArgs {
+  const void* w_codes;   // E4M3 [N][K] as the GEMM reads it
+  const void* w_scales;  // swizzled scales as the GEMM reads them
+  const void* ref_codes;   // canonical synchronized weight, E4M3 [N][K]
+  const void* ref_scales;  // its linear scales [N][K/32]
+  int64_t N, K;
+  const void* x;         // BF16 [T][K]
+  int64_t T;
+  void* workspace;       // selfcheck_workspace_bytes(T, N, K) bytes
+  float* rel_err;        // device, one float
+  int* status;
+};
+
+int64_t selfcheck_workspace_bytes(int64_t T, int64_t N, int64_t K);
+int launch_selfcheck(const SelfcheckArgs& a, cudaStream_t stream);
+
 int num_sms();  // of the current device (cached)
 
 }  // namespace mxfp8

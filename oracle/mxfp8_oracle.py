@@ -308,3 +308,17 @@ def grouped_gemm_wgrad(a_codes, a_scales, b_codes, b_scales, offsets):
             c[e] = gemm(a_codes[:, sl], a_scales[:, ss], b_codes[:, sl], b_scales[:, ss])
             cabs[e] = gemm_abs(a_codes[:, sl], a_scales[:, ss], b_codes[:, sl], b_scales[:, ss])
     return c, cabs
+
+
+# ------------------------------------------------------------------ post-sync self-check
+
+def selfcheck_rel_error(x_bits, k_codes, k_scales, r_codes, r_scales) -> float:
+    """The post-sync self-check ("End-to-End MXFP8 RL on Blackwell", section "Correctness:
+    how it fails", condition C3): the BF16 input x [T, K] is quantized and multiplied with
+    the weight as the kernel reads it (k_codes, linear k_scales); the reference multiplies
+    x itself with the canonical synchronized weight (r_codes, linear r_scales)
+    dequantized. Returns ||Y - Y_ref||_F / ||Y_ref||_F."""
+    qx, sx = quantize(x_bits, ROW)
+    y = gemm(qx, sx, k_codes, k_scales)
+    y_ref = bf16_to_f64(x_bits) @ dequantize(r_codes, r_scales).T
+    return float(np.linalg.norm(y - y_ref) / np.linalg.norm(y_ref))

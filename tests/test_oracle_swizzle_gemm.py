@@ -168,3 +168,26 @@ def test_grouped_scale_layout():
     with pytest.raises(ValueError):
         O.check_offsets([0, 40, 64], 64)
     O.check_offsets(offsets, 192)
+
+
+def test_selfcheck_oracle_pins():
+    """Self-check reference: zero when quantizing the input loses nothing; invariant under
+    a power-of-two scaling of the input; about sqrt(2) for an unrelated weight."""
+    g = np.random.default_rng(12)
+    # input whose blocks are exactly representable: +-2^j with j in [-6, 8] of the block
+    # scale 2^0 (amax 256 in every block)
+    e = g.integers(-6, 9, size=(32, 64))
+    x = np.where(g.random((32, 64)) < 0.5, -1.0, 1.0) * np.exp2(e)
+    x[:, ::32] = 256.0
+    xb = _bf16(x)
+    w = _bf16(g.standard_normal((48, 64)) * 0.02)
+    qw, sw = O.quantize(w, O.ROW)
+    assert O.selfcheck_rel_error(xb, qw, sw, qw, sw) < 1e-12
+    xr = _bf16(g.standard_normal((32, 64)))
+    r1 = O.selfcheck_rel_error(xr, qw, sw, qw, sw)
+    assert 0.005 < r1 < 0.1                       # the activations' quantization error
+    x2 = _bf16(O.bf16_to_f64(xr) * 4.0)
+    assert abs(O.selfcheck_rel_error(x2, qw, sw, qw, sw) - r1) < 1e-12
+    perm = g.permutation(48)
+    r_stale = O.selfcheck_rel_error(xr, qw[perm], sw[perm], qw, sw)
+    assert 1.1 < r_stale < 1.8
