@@ -239,6 +239,28 @@ int mxfp8_selfcheck(const void* w_codes_dev, const void* w_scales_dev,
                     size_t workspace_bytes, float* rel_err_dev, void* stream);
 
 /*
+ * mxfp8_selfcheck without a caller-provided workspace, for callers that cannot allocate
+ * device memory when the check runs - for instance a serving engine's post-update hook
+ * running while the engine's caching allocator holds all free device memory, or a
+ * plugin that has no handle to the host framework's allocator. This entry point has no
+ * counterpart on the pages; it exists for those callers.
+ *   Arguments and result as mxfp8_selfcheck. The workspace is a fixed 8 MiB array
+ *   inside the library (every device that loads the library holds it until the process
+ *   exits), so mxfp8_selfcheck_workspace_bytes(tokens, N, K) must not exceed
+ *   8 MiB (8388608 bytes); larger sizes return MXFP8_ERR_INVALID_ARG.
+ *   No device memory is allocated and no allocating library routine is called.
+ *   The first call on a device looks up the array's device address on that device;
+ *   make that first call before any stream capture.
+ *   All calls share the one array: calls that overlap on the GPU (other streams, other
+ *   host threads) race on it and must be serialised by the caller. Every call
+ *   rewrites what it reads, and clears its two reduction sums itself.
+ */
+int mxfp8_selfcheck_noalloc(const void* w_codes_dev, const void* w_scales_dev,
+                            const void* ref_codes_dev, const void* ref_scales_dev, int64_t N,
+                            int64_t K, const void* x_bf16_dev, int64_t tokens,
+                            float* rel_err_dev, void* stream);
+
+/*
  * Synchronizes `stream`, then returns and clears the current device's status word:
  * MXFP8_OK, or the first device-side error latched since the last call
  * (MXFP8_ERR_BAD_OFFSETS, MXFP8_ERR_TIMEOUT), or MXFP8_ERR_CUDA if the synchronization

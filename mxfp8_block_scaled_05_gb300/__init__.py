@@ -41,6 +41,7 @@ SIGNATURES = {
     "mxfp8_grouped_gemm": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _P]),
     "mxfp8_selfcheck_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "mxfp8_selfcheck": (_I, [_P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _SZ, _P, _P]),
+    "mxfp8_selfcheck_noalloc": (_I, [_P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _P]),
     "mxfp8_get_device_status": (_I, [_P]),
 }
 

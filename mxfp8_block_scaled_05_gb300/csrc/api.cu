@@ -306,6 +306,32 @@ int mxfp8_selfcheck(const void* w_codes_dev, const void* w_scales_dev,
   return launch_selfcheck(a, static_cast<cudaStream_t>(stream));
 }
 
+int mxfp8_selfcheck_noalloc(const void* w_codes_dev, const void* w_scales_dev,
+                            const void* ref_codes_dev, const void* ref_scales_dev, int64_t N,
+                            int64_t K, const void* x_bf16_dev, int64_t tokens,
+                            float* rel_err_dev, void* stream) {
+  if (!w_codes_dev || !w_scales_dev || !ref_codes_dev || !ref_scales_dev || !x_bf16_dev ||
+      !rel_err_dev)
+    return MXFP8_ERR_INVALID_ARG;
+  if (tokens <= 0 || N <= 0 || K <= 0) return MXFP8_ERR_INVALID_ARG;
+  if (K % 32 || N % 16 || tokens % 16) return MXFP8_ERR_ALIGNMENT;
+  if (tokens > 0x7FFFFF00 || N > 0x7FFFFF00 || K > 0x7FFFFF00) return MXFP8_ERR_INVALID_ARG;
+  if (selfcheck_workspace_bytes(tokens, N, K) > kSelfcheckNoallocMaxBytes)
+    return MXFP8_ERR_INVALID_ARG;
+  if (!aligned16(w_codes_dev) || !aligned16(w_scales_dev) || !aligned16(x_bf16_dev) ||
+      (reinterpret_cast<uintptr_t>(rel_err_dev) & 3u))
+    return MXFP8_ERR_ALIGNMENT;
+  DeviceState* d = nullptr;
+  int st = device_state(&d);
+  if (st != MXFP8_OK) return st;
+  void* ws = nullptr;
+  st = selfcheck_noalloc_workspace(&ws);
+  if (st != MXFP8_OK) return st;
+  SelfcheckArgs a{w_codes_dev, w_scales_dev, ref_codes_dev, ref_scales_dev, N, K, x_bf16_dev,
+                  tokens, ws, rel_err_dev, d->status};
+  return launch_selfcheck(a, static_cast<cudaStream_t>(stream));
+}
+
 int mxfp8_get_device_status(void* stream) {
   DeviceState* d = nullptr;
   const int st = device_state(&d);

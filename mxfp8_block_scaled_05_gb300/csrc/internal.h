@@ -61,6 +61,10 @@ struct SelfcheckArgs {
 };
 
 int64_t selfcheck_workspace_bytes(int64_t T, int64_t N, int64_t K);
+
+// Size of the fixed workspace behind mxfp8_selfcheck_noalloc (8 MiB).
+constexpr int64_t kSelfcheckNoallocMaxBytes = int64_t(8) << 20;
+int selfcheck_noalloc_workspace(void** out);
 int launch_selfcheck(const SelfcheckArgs& a, cudaStream_t stream);
 
 int num_sms();  // of the current device (cached)

@@ -122,6 +122,11 @@ __global__ void selfcheck_finish_kernel(const double* __restrict__ acc, float* _
   out[0] = acc[1] > 0.0 ? static_cast<float>(sqrt(acc[0] / acc[1])) : (acc[0] > 0.0 ? INFINITY : 0.f);
 }
 
+// Workspace of the allocation-free self-check (mxfp8_selfcheck_noalloc): a fixed array
+// in this module, present on every device that loads the library until the process
+// exits. All calls share it.
+static __device__ __align__(256) uint8_t g_selfcheck_scratch[kSelfcheckNoallocMaxBytes];
+
 }  // namespace
 
 int64_t selfcheck_workspace_bytes(int64_t T, int64_t N, int64_t K) {
@@ -161,6 +166,28 @@ int launch_selfcheck(const SelfcheckArgs& a, cudaStream_t stream) {
                                                   a.T, a.N, a.K, acc);
   selfcheck_finish_kernel<<<1, 1, 0, stream>>>(acc, a.rel_err);
   return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
+}
+
+}  // namespace mxfp8
+
+namespace mxfp8 {
+
+// Device address of the fixed workspace, looked up once per device with that device
+// current (host code must not use the array's name as a device address).
+int selfcheck_noalloc_workspace(void** out) {
+  static void* addr[64] = {};
+  static bool done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MXFP8_ERR_CUDA;
+  if (!done[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_selfcheck_scratch) != cudaSuccess || p == nullptr)
+      return MXFP8_ERR_CUDA;
+    addr[dev] = p;
+    done[dev] = true;
+  }
+  *out = addr[dev];
+  return MXFP8_OK;
 }
 
 }  // namespace mxfp8
