@@ -14,7 +14,7 @@ blocks along the token dimension (for the weight-gradient GEMM), and token count
 padded to multiples of 32. Weight-synchronization paragraph: the synced weights are the
 forward GEMM's weight quantization, byte for byte.
 
-Readings taken where the page is silent (each is listed in the design notes):
+Readings taken where the page is silent:
   * scale rule = the OCP one: shared exponent e = floor(log2(amax)) - 8 (8 is the E4M3
     emax, 448 = 1.75 * 2^8), clamped below at -127 (the E8M0 minimum); amax = 0 gives
     e = -127;
