@@ -111,6 +111,7 @@ struct Tile {
 struct SegShared {
   int32_t off[kMaxExperts + 1];
   int32_t tile_base[kMaxExperts + 1];
+  int16_t order[kMaxExperts];  // experts by decreasing token count (ties: lower index first)
   int ok;
 };
 
@@ -186,9 +187,11 @@ __device__ Tile make_tile(const Params& p, const SegShared* seg, int64_t id) {
   }
   // grouped weight gradient: problem e is [M = N_out] x [N = K_out], reduced over the
   // tokens of segment e
+  // Experts are visited heaviest first, so the CTAs' static round robin over the tiles
+  // spreads the long reductions evenly (longest-processing-time-first order).
   const int64_t per = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
   if (!seg->ok || id >= per * p.E) return t;
-  const int e = static_cast<int>(id / per);
+  const int e = seg->order[id / per];
   const int64_t r = id % per;
   const int64_t mt = r / p.num_n_tiles, nt = r % p.num_n_tiles;
   const int64_t cnt = seg->off[e + 1] - seg->off[e];
@@ -324,6 +327,18 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
       seg->tile_base[E] = acc;
       if (!seg->ok && blockIdx.x == 0) latch_error(p.status, MXFP8_ERR_BAD_OFFSETS);
     }
+    if (kMode == kGroupWgrad) {
+      // rank of expert e = experts with more tokens, or as many and a lower index
+      for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int32_t ce = seg->off[e + 1] - seg->off[e];
+        int rank = 0;
+        for (int f = 0; f < E; ++f) {
+          const int32_t cf = seg->off[f + 1] - seg->off[f];
+          rank += (cf > ce) || (cf == ce && f < e);
+        }
+        seg->order[rank] = static_cast<int16_t>(e);
+      }
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
@@ -447,52 +462,52 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         if (!got) { ok = false; break; }
         tc_fence_after();
       }
-      for (int c2 = 0; c2 < kChunks; c2 += 2) {
-        uint32_t v[2][32];
-        __syncwarp();
-        if (t.nk > 0) {
-          const uint32_t base = tmem + (static_cast<uint32_t>(32 * q) << 16) +
-                                (half * kChunks + c2) * 32;
-          tmem_ld_32x32b_x32(base, v[0]);
-          tmem_ld_32x32b_x32(base + 32, v[1]);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[0][i] = v[1][i] = 0;
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int c = half * kChunks + c2 + u;
-          const int cols_left = t.cols_valid - 32 * c;
-          if (!row_ok || cols_left <= 0) continue;
-          if (p.out_fp32) {
-            float* dst = static_cast<float*>(p.C) + t.c_off + row * t.ldc + t.n0 + 32 * c;
-            const int nvec = cols_left >= 32 ? 8 : cols_left / 4;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (i < nvec)
-                reinterpret_cast<uint4*>(dst)[i] =
-                    make_uint4(v[u][4 * i], v[u][4 * i + 1], v[u][4 * i + 2], v[u][4 * i + 3]);
-          } else {
-            uint16_t* dst = static_cast<uint16_t*>(p.C) + t.c_off + row * t.ldc + t.n0 + 32 * c;
-            uint32_t b[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              b[i] = cvt_bf16x2(__uint_as_float(v[u][2 * i + 1]), __uint_as_float(v[u][2 * i]));
-            const int nvec = cols_left >= 32 ? 4 : cols_left / 8;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              if (i < nvec)
-                reinterpret_cast<uint4*>(dst)[i] =
-                    make_uint4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
-          }
-        }
-      }
+      // The whole accumulator slice of this warp (32 rows x BN/2 columns) goes to
+      // registers first, and TMEM is handed back to the MMA issuer before any store, so
+      // the next tile's MMAs overlap this tile's conversion and stores.
+      uint32_t v[kChunks][32];
+      __syncwarp();
       if (t.nk > 0) {
+        const uint32_t base = tmem + (static_cast<uint32_t>(32 * q) << 16) + half * kChunks * 32;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) tmem_ld_32x32b_x32(base + 32 * c, v[c]);
+        tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acc_empty);
         ++acc_it;
+      } else {
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[c][i] = 0;
+      }
+#pragma unroll
+      for (int u = 0; u < kChunks; ++u) {
+        const int c = half * kChunks + u;
+        const int cols_left = t.cols_valid - 32 * c;
+        if (!row_ok || cols_left <= 0) continue;
+        if (p.out_fp32) {
+          float* dst = static_cast<float*>(p.C) + t.c_off + row * t.ldc + t.n0 + 32 * c;
+          const int nvec = cols_left >= 32 ? 8 : cols_left / 4;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i < nvec)
+              reinterpret_cast<uint4*>(dst)[i] =
+                  make_uint4(v[u][4 * i], v[u][4 * i + 1], v[u][4 * i + 2], v[u][4 * i + 3]);
+        } else {
+          uint16_t* dst = static_cast<uint16_t*>(p.C) + t.c_off + row * t.ldc + t.n0 + 32 * c;
+          uint32_t b[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            b[i] = cvt_bf16x2(__uint_as_float(v[u][2 * i + 1]), __uint_as_float(v[u][2 * i]));
+          const int nvec = cols_left >= 32 ? 4 : cols_left / 8;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (i < nvec)
+              reinterpret_cast<uint4*>(dst)[i] =
+                  make_uint4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
+        }
       }
     }
     if (!ok && lane == 0) {
