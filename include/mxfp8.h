@@ -71,6 +71,12 @@ typedef enum mxfp8_scale_layout {
   MXFP8_SCALES_SWIZZLED = 1
 } mxfp8_scale_layout;
 
+typedef enum mxfp8_scale_rule {
+  MXFP8_RULE_FLOOR = 0, /* OCP: e = floor(log2 amax) - 8; the largest elements may saturate */
+  MXFP8_RULE_CEIL = 1   /* round-up power of two: smallest e with amax <= 448 * 2^e; never
+                           saturates (block-wise FP8 recipes' power-of-two scales) */
+} mxfp8_scale_rule;
+
 typedef enum mxfp8_op {
   MXFP8_OP_FPROP = 0, /* Y  = X  . W^T   A = X  rows,  B = W  rows          */
   MXFP8_OP_DGRAD = 1, /* dX = dY . W     A = dY rows,  B = W  cols (= W^T)  */
@@ -114,6 +120,18 @@ size_t mxfp8_scale_bytes(int64_t rows, int64_t cols, int axis, int scale_layout)
  */
 int mxfp8_quantize(const void* src_dev, int64_t rows, int64_t cols, int axis,
                    void* out_dev, void* scales_dev, int scale_layout, void* stream);
+
+/*
+ * mxfp8_quantize with an explicit scale rule (mxfp8_scale_rule). The pages contrast the
+ * MXFP8 grid with block-wise FP8 recipes whose power-of-two scales round the other way
+ * (section "A different grid, and drift"); MXFP8_RULE_CEIL produces that grid on the same
+ * 1x32 blocks so the two can be compared byte for byte. Bytes differ from the floor rule
+ * exactly in blocks whose amax exceeds 448 * 2^e_floor (scale byte one higher there).
+ * MXFP8_RULE_FLOOR gives the bytes of mxfp8_quantize.
+ */
+int mxfp8_quantize_rule(const void* src_dev, int64_t rows, int64_t cols, int axis,
+                        void* out_dev, void* scales_dev, int scale_layout, int scale_rule,
+                        void* stream);
 
 /*
  * Both copies of one BF16 matrix from a single read of it: the row-wise copy (as

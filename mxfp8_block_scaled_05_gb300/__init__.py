@@ -18,6 +18,7 @@ import torch
 ROW, COL = 0, 1
 LINEAR, SWIZZLED = 0, 1
 FPROP, DGRAD, WGRAD = 0, 1, 2
+RULE_FLOOR, RULE_CEIL = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
 
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED_ARCH, ERR_CUDA, ERR_BAD_OFFSETS, \
@@ -33,6 +34,7 @@ SIGNATURES = {
     "mxfp8_scale_bytes": (_SZ, [_I64, _I64, _I, _I]),
     "mxfp8_grouped_scale_bytes": (_SZ, [_I64, _I64, _I, _I]),
     "mxfp8_quantize": (_I, [_P, _I64, _I64, _I, _P, _P, _I, _P]),
+    "mxfp8_quantize_rule": (_I, [_P, _I64, _I64, _I, _P, _P, _I, _I, _P]),
     "mxfp8_quantize_dual": (_I, [_P, _I64, _I64, _P, _P, _P, _P, _I, _P]),
     "mxfp8_quantize_batched": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _I, _P]),
     "mxfp8_quantize_grouped_dual": (_I, [_P, _I64, _I64, _P, _I, _P, _P, _P, _P, _P]),
@@ -109,7 +111,7 @@ def grouped_scale_bytes(total_rows: int, cols: int, num_experts: int, axis: int 
 
 
 def quantize(src: torch.Tensor, axis: int = ROW, layout: int = SWIZZLED, out=None, scales=None,
-             stream=None):
+             stream=None, rule: int = RULE_FLOOR):
     """MXFP8-quantize a BF16 [rows, cols] CUDA tensor. Returns (E4M3 codes as uint8, E8M0
     scale bytes as uint8): codes [rows, cols] (ROW) or [cols, rows] (COL); scales flat
     (SWIZZLED) or [S_rows, S_cols] (LINEAR)."""
@@ -125,8 +127,12 @@ def quantize(src: torch.Tensor, axis: int = ROW, layout: int = SWIZZLED, out=Non
             scales = torch.empty((s_rows, s_cols), dtype=torch.uint8, device=src.device)
         else:
             scales = torch.empty(nb, dtype=torch.uint8, device=src.device)
-    _check(lib().mxfp8_quantize(_ptr(src), rows, cols, axis, _ptr(out), _ptr(scales), layout,
-                                _stream(stream)), "mxfp8_quantize")
+    if rule == RULE_FLOOR:
+        _check(lib().mxfp8_quantize(_ptr(src), rows, cols, axis, _ptr(out), _ptr(scales), layout,
+                                    _stream(stream)), "mxfp8_quantize")
+    else:
+        _check(lib().mxfp8_quantize_rule(_ptr(src), rows, cols, axis, _ptr(out), _ptr(scales),
+                                         layout, rule, _stream(stream)), "mxfp8_quantize_rule")
     return out, scales
 
 

@@ -136,7 +136,9 @@ size_t mxfp8_grouped_scale_bytes(int64_t total_rows, int64_t cols, int num_exper
 // out2/scales2 = column-wise copy).
 static int quantize_common(const void* src, int64_t batch, int64_t rows, int64_t cols, int axis,
                            void* out, void* scales, void* out2, void* scales2, int layout,
-                           const int32_t* offsets, int E, void* stream) {
+                           const int32_t* offsets, int E, void* stream,
+                           int rule = MXFP8_RULE_FLOOR) {
+  if (rule != MXFP8_RULE_FLOOR && rule != MXFP8_RULE_CEIL) return MXFP8_ERR_INVALID_ARG;
   if (batch < 0 || rows < 0 || cols < 0) return MXFP8_ERR_INVALID_ARG;
   if (axis != MXFP8_AXIS_ROW && axis != MXFP8_AXIS_COL && axis != kAxisBoth)
     return MXFP8_ERR_INVALID_ARG;
@@ -167,6 +169,7 @@ static int quantize_common(const void* src, int64_t batch, int64_t rows, int64_t
   a.layout = layout;
   a.offsets = offsets;
   a.num_experts = E;
+  a.rule = rule;
   a.status = d->status;
   if (row) {
     a.out = out;
@@ -187,6 +190,14 @@ int mxfp8_quantize(const void* src_dev, int64_t rows, int64_t cols, int axis, vo
   if (axis != MXFP8_AXIS_ROW && axis != MXFP8_AXIS_COL) return MXFP8_ERR_INVALID_ARG;
   return quantize_common(src_dev, 1, rows, cols, axis, out_dev, scales_dev, nullptr, nullptr,
                          scale_layout, nullptr, 0, stream);
+}
+
+int mxfp8_quantize_rule(const void* src_dev, int64_t rows, int64_t cols, int axis,
+                        void* out_dev, void* scales_dev, int scale_layout, int scale_rule,
+                        void* stream) {
+  if (axis != MXFP8_AXIS_ROW && axis != MXFP8_AXIS_COL) return MXFP8_ERR_INVALID_ARG;
+  return quantize_common(src_dev, 1, rows, cols, axis, out_dev, scales_dev, nullptr, nullptr,
+                         scale_layout, nullptr, 0, stream, scale_rule);
 }
 
 int mxfp8_quantize_dual(const void* src_dev, int64_t rows, int64_t cols, void* row_out_dev,

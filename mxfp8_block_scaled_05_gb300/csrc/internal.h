@@ -22,6 +22,7 @@ struct QuantizeArgs {
   int layout;             // MXFP8_SCALES_LINEAR / SWIZZLED
   const int32_t* offsets; // grouped call: device [num_experts + 1], else nullptr
   int num_experts;
+  int rule;               // MXFP8_RULE_FLOOR / MXFP8_RULE_CEIL
   int* status;            // device status word
 };
 

@@ -88,9 +88,13 @@ __device__ __forceinline__ uint32_t bf16_absmax8(const uint4& v) {
 }
 
 // Scale byte from the largest |BF16| bits of a block; 0xFF for a NaN/Inf block.
-__device__ __forceinline__ uint32_t scale_byte(uint32_t amax_bits) {
+// Floor rule (OCP): floor(log2 amax) - 8 = biased exponent - 135, byte = E - 8.
+// Round-up rule: one more when the mantissa of amax exceeds 1.75 (amax > 448 * 2^e), so
+// that nothing saturates. Both clamp at byte 0 (e = -127).
+__device__ __forceinline__ uint32_t scale_byte(uint32_t amax_bits, int rule) {
   if (amax_bits >= 0x7F80u) return 0xFFu;
-  const int e = static_cast<int>(amax_bits >> 7) - 8;
+  int e = static_cast<int>(amax_bits >> 7) - 8;
+  if (rule == MXFP8_RULE_CEIL) e += (amax_bits & 0x7Fu) > 0x60u;
   return e > 0 ? static_cast<uint32_t>(e) : 0u;
 }
 
@@ -126,7 +130,8 @@ struct QOut {
 template <bool kRow, bool kCol, bool kSwizzled, bool kGrouped>
 __global__ void __launch_bounds__(kThreads)
 quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t cols, QOut ro,
-                     QOut co, const int32_t* __restrict__ offsets, int E, int* status) {
+                     QOut co, const int32_t* __restrict__ offsets, int E, int rule,
+                     int* status) {
   __shared__ __align__(16) uint16_t tile[kCol ? kTile : 1][kCol ? kTile : 8];
   __shared__ __align__(16) uint8_t stile_r[512];
   __shared__ __align__(16) uint8_t stile_c[512];
@@ -200,7 +205,7 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
       const bool valid = col_ok && r < rows_valid;
-      const uint32_t s = scale_byte(m);
+      const uint32_t s = scale_byte(m, rule);
       const float mul = inv_scale(s == 0xFFu ? 127u : s);
       if (valid) {
         uint2 o;
@@ -240,7 +245,8 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
       m0 = max(m0, word[i] & 0x7FFFu);
       m1 = max(m1, (word[i] >> 16) & 0x7FFFu);
     }
-    const uint32_t s0 = scale_byte(m0), s1 = scale_byte(m1);
+    const uint32_t s0 = scale_byte(m0, rule), s1 = scale_byte(m1, rule);
+    uint4 stage_o0[2], stage_o1[2];
     if (valid) {
       const float mul0 = inv_scale(s0 == 0xFFu ? 127u : s0);
       const float mul1 = inv_scale(s1 == 0xFFu ? 127u : s1);
@@ -255,12 +261,10 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
         o1[q] = e4m3x4((a0 >> 16) | (a1 & 0xFFFF0000u), (a2 >> 16) | (a3 & 0xFFFF0000u), mul1,
                        s1 == 0xFFu);
       }
-      uint8_t* d0 = co.codes + (col0 + c) * rows + row0 + 32 * j;
-      uint8_t* d1 = d0 + rows;
-      reinterpret_cast<uint4*>(d0)[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-      reinterpret_cast<uint4*>(d0)[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
-      reinterpret_cast<uint4*>(d1)[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-      reinterpret_cast<uint4*>(d1)[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+      stage_o0[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+      stage_o0[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
+      stage_o1[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+      stage_o1[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
     }
     if (kSwizzled) {
       stile_c[(c & 31) * 16 + (c >> 5) * 4 + j] = valid ? static_cast<uint8_t>(s0) : 0;
@@ -269,6 +273,27 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
       const int64_t s_cols = rows / 32;
       co.scales[(col0 + c) * s_cols + row0 / 32 + j] = static_cast<uint8_t>(s0);
       co.scales[(col0 + c + 1) * s_cols + row0 / 32 + j] = static_cast<uint8_t>(s1);
+    }
+    // The transposed codes go through shared memory so that each output row's 128 bytes
+    // leave in one coalesced piece: stage[row][chunk] holds 16-byte chunks, chunk index
+    // XOR (row & 7) against bank conflicts; the BF16 tile buffer is reused once every
+    // thread has its columns in registers.
+    __syncthreads();
+    uint4* stage = reinterpret_cast<uint4*>(&tile[0][0]);
+    if (valid) {
+      stage[c * 8 + ((2 * j) ^ (c & 7))] = stage_o0[0];
+      stage[c * 8 + ((2 * j + 1) ^ (c & 7))] = stage_o0[1];
+      stage[(c + 1) * 8 + ((2 * j) ^ ((c + 1) & 7))] = stage_o1[0];
+      stage[(c + 1) * 8 + ((2 * j + 1) ^ ((c + 1) & 7))] = stage_o1[1];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = (t >> 3) + 32 * i;  // output row = tile column
+      const int ch = t & 7;             // 16 tokens per chunk
+      if (r < cols_valid && 16 * ch < rows_valid)
+        *reinterpret_cast<uint4*>(co.codes + (col0 + r) * rows + row0 + 16 * ch) =
+            stage[r * 8 + (ch ^ (r & 7))];
     }
   }
 
@@ -305,7 +330,7 @@ cudaError_t launch_tiles(const QuantizeArgs& a, cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>(col_tiles), static_cast<unsigned>(row_tiles),
             static_cast<unsigned>(a.batch));
   k<<<grid, kThreads, dyn, stream>>>(static_cast<const uint16_t*>(a.src), a.rows, a.cols, ro, co,
-                                      a.offsets, a.num_experts, a.status);
+                                      a.offsets, a.num_experts, a.rule, a.status);
   return cudaGetLastError();
 }
 

@@ -47,6 +47,7 @@ E8M0_NAN = 0xFF
 E4M3_NAN = 0x7F
 ROW, COL = 0, 1
 LINEAR, SWIZZLED = 0, 1
+RULE_FLOOR, RULE_CEIL = 0, 1
 
 
 # --------------------------------------------------------------------------- decoding
@@ -84,12 +85,20 @@ def floor_log2(x) -> np.ndarray:
     return k.astype(np.int64) - 1
 
 
-def block_scale_exponent(amax) -> np.ndarray:
-    """Shared exponent of a block: floor(log2 amax) - emax(E4M3), clamped to E8M0's
-    minimum -127; an all-zero block takes -127."""
+def block_scale_exponent(amax, rule=RULE_FLOOR) -> np.ndarray:
+    """Shared exponent of a block, clamped to E8M0's minimum -127 (an all-zero block takes
+    -127).
+
+    RULE_FLOOR (OCP): floor(log2 amax) - emax(E4M3); the largest elements may saturate.
+    RULE_CEIL: the smallest e with amax <= 448 * 2^e, i.e. ceil(log2(amax / 448)) - the
+    power-of-two scale that never saturates, as block-wise FP8 recipes with power-of-two
+    scales use ("End-to-End MXFP8 RL on Blackwell", section "A different grid, and
+    drift"). It exceeds the floor rule by one exactly when amax > 448 * 2^e_floor."""
     a = np.asarray(amax, dtype=np.float64)
     safe = np.where(a > 0, a, 1.0)
     e = floor_log2(safe) - E4M3_EMAX
+    if rule == RULE_CEIL:
+        e = e + (safe > np.ldexp(E4M3_MAX, e)).astype(np.int64)
     return np.where(a > 0, np.maximum(e, E8M0_MIN_EXP), E8M0_MIN_EXP)
 
 
@@ -139,7 +148,7 @@ def e4m3_nearest_code(x) -> np.ndarray:
 
 # --------------------------------------------------------------------- quantization
 
-def quantize_blocks(v, cast=e4m3_round_code):
+def quantize_blocks(v, cast=e4m3_round_code, rule=RULE_FLOOR):
     """Quantize blocks of 32 values (float64 array [..., 32]).
 
     Returns (codes uint8 [..., 32], scale bytes uint8 [...]). Per block: amax = max|v|,
@@ -149,7 +158,7 @@ def quantize_blocks(v, cast=e4m3_round_code):
     assert v.shape[-1] == BLOCK
     special = ~np.all(np.isfinite(v), axis=-1)
     amax = np.max(np.abs(np.where(np.isfinite(v), v, 0.0)), axis=-1)
-    e = block_scale_exponent(amax)
+    e = block_scale_exponent(amax, rule)
     codes = cast(np.ldexp(np.where(np.isfinite(v), v, 0.0), -e[..., None]))
     nan_codes = (E4M3_NAN | (np.signbit(v).astype(np.int64) << 7)).astype(np.uint8)
     codes = np.where(special[..., None], nan_codes, codes).astype(np.uint8)
@@ -157,7 +166,7 @@ def quantize_blocks(v, cast=e4m3_round_code):
     return codes, scales
 
 
-def quantize(x_bits, axis=ROW, cast=e4m3_round_code):
+def quantize(x_bits, axis=ROW, cast=e4m3_round_code, rule=RULE_FLOOR):
     """MXFP8-quantize a BF16 matrix given as uint16 bit patterns [R, C].
 
     axis=ROW: blocks of 32 along the contiguous dim (C % 32 == 0); returns codes [R, C]
@@ -171,7 +180,7 @@ def quantize(x_bits, axis=ROW, cast=e4m3_round_code):
     rows, cols = x.shape
     if cols % BLOCK:
         raise ValueError("the blocked dimension must be a multiple of 32")
-    codes, scales = quantize_blocks(x.reshape(rows, cols // BLOCK, BLOCK), cast)
+    codes, scales = quantize_blocks(x.reshape(rows, cols // BLOCK, BLOCK), cast, rule)
     return codes.reshape(rows, cols), scales
 
 

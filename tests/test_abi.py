@@ -92,6 +92,8 @@ def test_argument_errors_need_no_device(lib):
     assert gg(p, p, p, p, p, p, 2000, 64, 128, 64, 0, 0, None) == m.ERR_INVALID_ARG
     assert gg(p, p, p, p, p, None, 4, 64, 128, 64, 0, 0, None) == m.ERR_INVALID_ARG
     assert gg(p, p, p, p, p, p, 4, 48, 128, 64, 0, 0, None) == m.ERR_ALIGNMENT
+    assert lib.mxfp8_quantize_rule(p, 64, 64, m.ROW, p, p, m.SWIZZLED, 7, None) == m.ERR_INVALID_ARG
+    assert lib.mxfp8_quantize_rule(p, 64, 48, m.ROW, p, p, m.SWIZZLED, 1, None) == m.ERR_ALIGNMENT
     qg = lib.mxfp8_quantize_grouped
     assert qg(p, 64, 64, m.ROW, None, 4, p, p, None) == m.ERR_INVALID_ARG
     assert qg(p, 48, 64, m.ROW, p, 4, p, p, None) == m.ERR_ALIGNMENT

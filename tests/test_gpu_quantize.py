@@ -251,3 +251,45 @@ def test_grouped_dual_equals_grouped(m):
     np.testing.assert_array_equal(u8(rs)[:want_r.size], want_r)
     np.testing.assert_array_equal(u8(cs)[:want_c.size], want_c)
     assert m.device_status() == m.OK
+
+
+@pytest.mark.parametrize("context", [0x0000, 0x3F80, 0x7180], ids=["alone", "beside1", "beside2^100"])
+def test_round_up_rule_brute_force_every_bf16(m, context):
+    """The round-up (never saturating) power-of-two rule, every BF16 value, both axes."""
+    allb = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = np.zeros((65536, 32), np.uint16)
+    x[:, 0] = allb
+    x[:, 1] = context
+    for axis, xs in ((O.ROW, x), (O.COL, np.ascontiguousarray(x.T))):
+        q, s = m.quantize(bits_to_bf16(xs).to(DEV), axis, m.LINEAR, rule=m.RULE_CEIL)
+        rq, rs = O.quantize(xs, axis, rule=O.RULE_CEIL)
+        np.testing.assert_array_equal(u8(q), rq)
+        np.testing.assert_array_equal(u8(s), rs)
+
+
+def test_round_up_rule_golden_blocks_and_grid_difference(m):
+    cases = load_golden("hand_blocks_ceil.json")["blocks"]
+    x = np.zeros((len(cases), 32), np.uint16)
+    want = np.zeros((len(cases), 32), np.uint8)
+    for i, c in enumerate(cases):
+        for j, h in enumerate(c["bf16"]):
+            x[i, j] = int(h, 16)
+        for j, h in enumerate(c["codes"]):
+            want[i, j] = int(h, 16)
+    q, s = m.quantize(bits_to_bf16(x).to(DEV), m.ROW, m.LINEAR, rule=m.RULE_CEIL)
+    np.testing.assert_array_equal(u8(q), want)
+    np.testing.assert_array_equal(u8(s)[:, 0], [int(c["scale"], 16) for c in cases])
+    # two grids on one weight: they differ exactly in the blocks whose amax exceeds
+    # 448 * 2^e_floor, where the round-up scale byte is one higher
+    w = W.sync_weight(0, "o_proj", 4096, 4096, DEV)
+    qf, sf = m.quantize(w, m.ROW, m.LINEAR)
+    qc, sc = m.quantize(w, m.ROW, m.LINEAR, rule=m.RULE_CEIL)
+    amax = w.float().abs().view(4096, 128, 32).amax(dim=2).double().cpu().numpy()
+    ef = u8(sf).astype(np.int64) - 127
+    over = amax > np.ldexp(448.0, ef)
+    diff = u8(sc).astype(np.int64) - u8(sf).astype(np.int64)
+    bad = np.argwhere(diff != over.astype(np.int64))
+    assert bad.size == 0, (bad[:3], amax[tuple(bad[0])], ef[tuple(bad[0])], diff[tuple(bad[0])])
+    blocks_differ = (u8(qf).reshape(4096, 128, 32) != u8(qc).reshape(4096, 128, 32)).any(axis=2)
+    assert not np.any(blocks_differ & ~over)
+    assert 0.01 < over.mean() < 0.9

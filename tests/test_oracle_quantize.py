@@ -212,3 +212,45 @@ def test_planted_mistakes_are_caught():
         assert run(O.e4m3_round_code) > 0
     finally:
         O.E4M3_EMAX = saved
+
+
+@pytest.mark.parametrize("case", load_golden("hand_blocks_ceil.json")["blocks"], ids=lambda c: c["name"])
+def test_hand_worked_blocks_round_up_rule(case):
+    bits = np.zeros(32, dtype=np.uint16)
+    for i, h in enumerate(case["bf16"]):
+        bits[i] = int(h, 16)
+    want = np.zeros(32, dtype=np.uint8)
+    for i, h in enumerate(case["codes"]):
+        want[i] = int(h, 16)
+    for cast in (O.e4m3_round_code, O.e4m3_nearest_code):
+        codes, scale = O.quantize_blocks(O.bf16_to_f64(bits)[None, :], cast, O.RULE_CEIL)
+        assert int(scale[0]) == int(case["scale"], 16), case["why"]
+        np.testing.assert_array_equal(codes[0], want, err_msg=case["why"])
+
+
+@pytest.mark.parametrize("context", [0.0, 1.0, 2.0 ** 100], ids=["alone", "beside1", "beside2^100"])
+def test_round_up_rule_brute_force(context):
+    """Every BF16 value: the round-up exponent equals ceil(log2(amax / 448)) from numpy,
+    nothing saturates (scaled amax <= 448), and the rules differ exactly when the block
+    amax exceeds 448 * 2^e_floor."""
+    v = _brute_blocks(context)
+    fin = np.all(np.isfinite(v), axis=1)
+    v = v[fin]
+    cf, sf = O.quantize_blocks(v, O.e4m3_round_code, O.RULE_FLOOR)
+    cc, sc = O.quantize_blocks(v, O.e4m3_round_code, O.RULE_CEIL)
+    c2, s2 = O.quantize_blocks(v, O.e4m3_nearest_code, O.RULE_CEIL)
+    np.testing.assert_array_equal(cc, c2)
+    np.testing.assert_array_equal(sc, s2)
+    amax = np.max(np.abs(v), axis=1)
+    pos = amax > 0
+    with np.errstate(divide="ignore"):
+        e_lib = np.maximum(np.ceil(np.log2(amax[pos] / 448.0)), -127).astype(np.int64)
+    np.testing.assert_array_equal(sc[pos].astype(np.int64) - 127, e_lib)
+    deq = O.e4m3_decode(cc) * O.e8m0_decode(sc)[:, None]
+    assert np.all(np.abs(deq) <= np.ldexp(448.0, sc.astype(np.int64) - 127)[:, None])
+    scaled_amax = np.ldexp(amax, -(sc.astype(np.int64) - 127))
+    assert np.all(scaled_amax <= 448.0)
+    differ = sf != sc
+    ef = sf.astype(np.int64) - 127
+    np.testing.assert_array_equal(differ, amax > np.ldexp(448.0, ef))
+    assert np.all(sc[differ].astype(np.int64) == sf[differ].astype(np.int64) + 1)
