@@ -388,7 +388,7 @@ def run_ours(args, rank, ws):
     fp8_peak = pk["bf16_sus"] * FP8_OVER_BF16
     traffic = recorded_traffic("mxfp8_gemm_kernel")
     e2e = run_e2e(args, m, step, dev, stream, ws)
-    g_ms, eager_ms, host_ms = run_graph(m, step, stream, max(10, args.steps // 4))
+    graph_ms, eager_ms, host_ms = run_graph(m, step, stream, max(10, args.steps // 4))
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
@@ -415,9 +415,9 @@ def run_ours(args, rank, ws):
         "clocks": clk.summary(),
         "e2e": e2e,
         "per_launch": breakdown,
-        "cuda_graph": {"ms_per_step": g_ms, "eager_ms_per_step": eager_ms,
+        "cuda_graph": {"ms_per_step": graph_ms, "eager_ms_per_step": eager_ms,
                        "host_enqueue_ms_per_step": host_ms,
-                       "value": ws * step.flops / (g_ms * 1e-3) / 1e12, "unit": "TFLOP/s"},
+                       "value": ws * step.flops / (graph_ms * 1e-3) / 1e12, "unit": "TFLOP/s"},
     }
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline_obj()
