@@ -85,6 +85,7 @@ struct Params {
   int64_t sb_item_bytes; // grouped rows: bytes of one expert's B scale block
   int64_t num_tiles;     // dense: all tiles; grouped: upper bound
   int num_m_tiles, num_n_tiles;
+  int band;              // dense: M tiles (CTA pairs: pairs of M tiles) per raster band
   int* status;
   uint64_t wait_ns;
 };
@@ -132,9 +133,9 @@ __device__ Tile make_tile(const Params& p, const SegShared* seg, int64_t id) {
   const int64_t n_kt_dense = (p.K + BK - 1) / BK;
   if (kMode == kDense) {
     if (id >= p.num_tiles) return t;
-    // grouped raster: bands of 8 M tiles sweep across N, so concurrent CTAs share
-    // operand tiles in L2
-    constexpr int64_t GM = 8;
+    // banded raster: bands of p.band M tiles sweep across N, M fastest within a band, so
+    // that concurrent CTAs share operand tiles in L2 (the band width is chosen on the host)
+    const int64_t GM = p.band;
     const int64_t band = GM * p.num_n_tiles;
     const int64_t g = id / band;
     const int64_t first_m = g * GM;
@@ -225,7 +226,7 @@ __device__ Tile make_tile_pair(const Params& p, int64_t pid, uint32_t crank) {
   t.live = false;
   const int64_t n_pm = (p.num_m_tiles + 1) / 2;
   if (pid >= n_pm * p.num_n_tiles) return t;
-  constexpr int64_t GP = 4;  // bands of 4 pairs (8 M tiles) sweep across N
+  const int64_t GP = p.band;  // bands of p.band pairs sweep across N
   const int64_t band = GP * p.num_n_tiles;
   const int64_t first = (pid / band) * GP;
   const int64_t gp = (n_pm - first) < GP ? (n_pm - first) : GP;
@@ -637,6 +638,23 @@ int64_t max_pairs() {
   return clusters;
 }
 
+// Raster band width, in M tiles. Tiles of a band are visited M tile first, so that while
+// the band sweeps across N, its A row tiles stay in L2 and each B tile is fetched from
+// DRAM once per band. When A is the smaller operand (M <= N) the band is as tall as
+// kBandBytes of A allows, up to all of M, so that B is streamed from DRAM about once.
+// Otherwise B is the smaller operand: narrow bands of 8 tiles keep all of B in L2 while
+// A streams through.
+constexpr int64_t kBandBytes = int64_t(48) << 20;
+
+int band_tiles(int64_t M, int64_t N, int64_t K, int num_m_tiles) {
+  int64_t gm = 8;
+  if (M <= N) {
+    const int64_t fit = kBandBytes / (static_cast<int64_t>(BM) * K);
+    gm = fit > gm ? fit : gm;
+  }
+  return static_cast<int>(gm < num_m_tiles ? gm : num_m_tiles);
+}
+
 bool pairs_enabled() {
   static const bool on = [] {
     const char* e = getenv("MXFP8_GEMM_PAIRS");
@@ -663,6 +681,7 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.num_m_tiles = static_cast<int>((a.M + BM - 1) / BM);
   p.num_n_tiles = static_cast<int>((a.N + bn - 1) / bn);
   p.num_tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+  p.band = band_tiles(a.M, a.N, a.K, p.num_m_tiles);
   CUtensorMap ma, mb;
   if (!make_map(&ma, a.A, 2, a.K, a.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
   // A CTA pair shares each B tile: each CTA loads half of it and multicasts it to both.
@@ -670,6 +689,7 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   if (pair) {
     if (!make_map(&mb, a.B, 2, a.K, a.N, 1, BK, bn / 2)) return MXFP8_ERR_CUDA;
     const int64_t pair_tiles = static_cast<int64_t>((p.num_m_tiles + 1) / 2) * p.num_n_tiles;
+    p.band = (p.band + 1) / 2;
     const int64_t mp = max_pairs<256>();
     const int64_t pairs = pair_tiles < mp ? pair_tiles : mp;
     return launch<256, kDense, true>(ma, mb, p, 2 * pairs, stream);

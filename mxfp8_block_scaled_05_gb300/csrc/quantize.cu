@@ -7,10 +7,16 @@
 // paragraph of the same section; scales written straight into the GEMM's layout instead
 // of a separate rearrangement pass: section "Where the time goes".
 //
-// Each CTA owns a 128 x 128 BF16 tile (32 KB): 256 threads issue all eight of their
-// 16-byte loads before using any, so a CTA keeps 32 KB in flight. A 128 x 128 tile
-// has exactly 128 x 4 blocks, i.e. one 512-byte swizzled scale tile, which the CTA
-// assembles in shared memory and stores with 16-byte writes.
+// Each CTA owns a 128 x 128 BF16 tile (32 KB) and keeps all of it in flight at once.
+// The row-wise kernel loads it into registers (eight 16-byte loads per thread, all issued
+// before any is used). Kernels that write the column-wise copy copy it into shared memory
+// with cp.async instead: no register is held while the loads are in flight, so six CTAs
+// fit on an SM, and both copies read the tile from there. A 128 x 128 tile has exactly
+// 128 x 4 blocks, i.e. one 512-byte swizzled scale tile, which the CTA assembles in
+// shared memory and stores with 16-byte writes.
+//
+// Block maxima are taken on the BF16 bits of two elements at once (|x| = bits & 0x7FFF,
+// compared as unsigned 16-bit pairs), which orders finite values, Inf and NaN correctly.
 //
 // The block exponent is taken from the integer bits of the block's largest |BF16|
 // (biased exponent E): scale byte = max(E - 8, 0) (floor(log2 amax) - 8, clamped at
@@ -76,15 +82,23 @@ __device__ int find_expert(const Segments& s, int E, int t) {
   return lo;
 }
 
-__device__ __forceinline__ uint32_t bf16_absmax8(const uint4& v) {
-  uint32_t m = 0;
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    m = max(m, w[i] & 0x7FFFu);
-    m = max(m, (w[i] >> 16) & 0x7FFFu);
-  }
-  return m;
+constexpr uint32_t kAbs2 = 0x7FFF7FFFu;  // clears both BF16 sign bits of a word
+
+// Per-half unsigned 16-bit maximum of two words.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// 16 bytes global -> shared, bypassing L1; `valid` false writes 16 zero bytes instead.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 16u : 0u) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // Scale byte from the largest |BF16| bits of a block; 0xFF for a NaN/Inf block.
@@ -128,7 +142,7 @@ struct QOut {
 };
 
 template <bool kRow, bool kCol, bool kSwizzled, bool kGrouped>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kCol ? 6 : 1)
 quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t cols, QOut ro,
                      QOut co, const int32_t* __restrict__ offsets, int E, int rule,
                      int* status) {
@@ -184,33 +198,49 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
   const int cols_valid = static_cast<int>(cols_left < kTile ? cols_left : kTile);
   const bool col_ok = 8 * v < cols_valid;   // cols % 8 == 0 (% 32 == 0 with kRow)
 
-  // ---- load: eight 16-byte loads per thread, all issued before any is used
-  uint4 x[8];
+  // ---- load the tile: into shared memory when a column-wise copy is made, else registers
+  uint4 x[kCol ? 1 : 8];
+  if constexpr (kCol) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int r = rsub + 16 * j;
-    if (col_ok && r < rows_valid)
-      x[j] = ld_nc_v4(src + (row0 + r) * cols + col0 + 8 * v);
-    else
-      x[j] = make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < 8; ++j) {
+      const int r = rsub + 16 * j;
+      const bool ok = col_ok && r < rows_valid;
+      cp_async16(&tile[r][8 * v], ok ? src + (row0 + r) * cols + col0 + 8 * v : src, ok);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = rsub + 16 * j;
+      if (col_ok && r < rows_valid)
+        x[j] = ld_nc_v4(src + (row0 + r) * cols + col0 + 8 * v);
+      else
+        x[j] = make_uint4(0, 0, 0, 0);
+    }
   }
 
-  // ---- row-wise copy straight from registers: the 4 lanes of a 32-block share amax
+  // ---- row-wise copy: the 4 lanes of a 32-block share amax
   if (kRow) {
     const int64_t s_cols = cols / 32;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int r = rsub + 16 * j;
-      uint32_t m = bf16_absmax8(x[j]);
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      uint4 xv;
+      if constexpr (kCol) xv = *reinterpret_cast<const uint4*>(&tile[r][8 * v]);
+      else xv = x[j];
+      uint32_t m2 = max_u16x2(max_u16x2(xv.x & kAbs2, xv.y & kAbs2),
+                              max_u16x2(xv.z & kAbs2, xv.w & kAbs2));
+      m2 = max_u16x2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 1));
+      m2 = max_u16x2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 2));
+      const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
       const bool valid = col_ok && r < rows_valid;
       const uint32_t s = scale_byte(m, rule);
       const float mul = inv_scale(s == 0xFFu ? 127u : s);
       if (valid) {
         uint2 o;
-        o.x = e4m3x4(x[j].x, x[j].y, mul, s == 0xFFu);
-        o.y = e4m3x4(x[j].z, x[j].w, mul, s == 0xFFu);
+        o.x = e4m3x4(xv.x, xv.y, mul, s == 0xFFu);
+        o.y = e4m3x4(xv.z, xv.w, mul, s == 0xFFu);
         *reinterpret_cast<uint2*>(ro.codes + (row0 + r) * cols + col0 + 8 * v) = o;
       }
       if ((v & 3) == 0) {
@@ -223,29 +253,21 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
     }
   }
 
-  // ---- column-wise copy through shared memory (transpose)
+  // ---- column-wise copy from the shared tile (transpose)
   if (kCol) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<uint4*>(&tile[rsub + 16 * j][8 * v]) = x[j];
-    __syncthreads();
-    // thread = column pair (2cp, 2cp+1) x token block j (32 rows)
+    // thread = column pair (2cp, 2cp+1) x token block j (32 rows); each word read holds
+    // both columns of one row (column c in the low half)
     const int w = t >> 5, lane = t & 31;
     const int cp = (w & 1) * 32 + lane;
     const int j = w >> 1;
     const int c = 2 * cp;
     const bool valid = c < cols_valid && 32 * j < rows_valid;
-    uint32_t word[32];
+    const uint32_t* colw = reinterpret_cast<const uint32_t*>(&tile[32 * j][c]);
+    constexpr int kRowWords = kTile / 2;
+    uint32_t m01 = 0;  // both columns' block maxima, one per half
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      word[i] = *reinterpret_cast<const uint32_t*>(&tile[32 * j + i][c]);
-    uint32_t m0 = 0, m1 = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      m0 = max(m0, word[i] & 0x7FFFu);
-      m1 = max(m1, (word[i] >> 16) & 0x7FFFu);
-    }
-    const uint32_t s0 = scale_byte(m0, rule), s1 = scale_byte(m1, rule);
+    for (int i = 0; i < 32; ++i) m01 = max_u16x2(m01, colw[i * kRowWords] & kAbs2);
+    const uint32_t s0 = scale_byte(m01 & 0xFFFFu, rule), s1 = scale_byte(m01 >> 16, rule);
     uint4 stage_o0[2], stage_o1[2];
     if (valid) {
       const float mul0 = inv_scale(s0 == 0xFFu ? 127u : s0);
@@ -253,12 +275,12 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
       uint32_t o0[8], o1[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const uint32_t a0 = word[4 * q], a1 = word[4 * q + 1], a2 = word[4 * q + 2],
-                       a3 = word[4 * q + 3];
+        const uint32_t a0 = colw[(4 * q) * kRowWords], a1 = colw[(4 * q + 1) * kRowWords];
+        const uint32_t a2 = colw[(4 * q + 2) * kRowWords], a3 = colw[(4 * q + 3) * kRowWords];
         // column c: low halves; column c+1: high halves
-        o0[q] = e4m3x4((a0 & 0xFFFFu) | (a1 << 16), (a2 & 0xFFFFu) | (a3 << 16), mul0,
+        o0[q] = e4m3x4(__byte_perm(a0, a1, 0x5410), __byte_perm(a2, a3, 0x5410), mul0,
                        s0 == 0xFFu);
-        o1[q] = e4m3x4((a0 >> 16) | (a1 & 0xFFFF0000u), (a2 >> 16) | (a3 & 0xFFFF0000u), mul1,
+        o1[q] = e4m3x4(__byte_perm(a0, a1, 0x7632), __byte_perm(a2, a3, 0x7632), mul1,
                        s1 == 0xFFu);
       }
       stage_o0[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
@@ -277,7 +299,7 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
     // The transposed codes go through shared memory so that each output row's 128 bytes
     // leave in one coalesced piece: stage[row][chunk] holds 16-byte chunks, chunk index
     // XOR (row & 7) against bank conflicts; the BF16 tile buffer is reused once every
-    // thread has its columns in registers.
+    // thread has read what it needs of it.
     __syncthreads();
     uint4* stage = reinterpret_cast<uint4*>(&tile[0][0]);
     if (valid) {
