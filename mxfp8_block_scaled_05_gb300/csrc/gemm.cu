@@ -356,12 +356,12 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     for (int64_t id = first_id; ok; id += id_step) {
       const Tile t = tile_of<BN, kMode, kPair>(p, seg, id, crank);
       if (!t.live) break;
+      int n_sfb = 0;
+      for (int h = 0; h < C::kSfbTiles; ++h) n_sfb += (t.n0 + 128 * h < p.N);
+      const uint32_t bytes = C::kABytes + C::kBBytes + (t.a_valid ? 512 : 0) + 512 * n_sfb;
       for (int kb = 0; kb < t.nk; ++kb, ++it) {
         const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1;
         if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
-        int n_sfb = 0;
-        for (int h = 0; h < C::kSfbTiles; ++h) n_sfb += (t.n0 + 128 * h < p.N);
-        const uint32_t bytes = C::kABytes + C::kBBytes + (t.a_valid ? 512 : 0) + 512 * n_sfb;
         mbar_arrive_expect_tx(&full[s], bytes);
         const int32_t kx = static_cast<int32_t>(t.k_origin + static_cast<int64_t>(kb) * BK);
         tma_load_2d(smem + C::kOffA + s * C::kABytes, &map_a, kx,
@@ -394,10 +394,17 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------- MMA issuer
+    // One thread issues every tensor-core instruction of the CTA, so its loop is kept
+    // short: descriptors are built once and advanced by adding 16-byte units to their
+    // start-address field (shared addresses stay below 2^18, so no carry leaves it).
     uint32_t it = 0, acc_it = 0;
     bool ok = true;
-    const uint32_t sa_base = smem_u32(smem + C::kOffA);
-    const uint32_t sb_base = smem_u32(smem + C::kOffB);
+    const uint64_t a_desc0 = smem_desc(smem_u32(smem + C::kOffA), 16, 1024, 2);
+    const uint64_t b_desc0 = smem_desc(smem_u32(smem + C::kOffB), 16, 1024, 2);
+    const uint64_t sfa_desc0 = smem_desc(smem_u32(smem + C::kOffSfa), 0, 128, 0);
+    const uint64_t sfb_desc0 = smem_desc(smem_u32(smem + C::kOffSfb), 0, 128, 0);
+    constexpr uint32_t kId0 = mxf8_idesc(BM, BN, 0, 0), kId1 = mxf8_idesc(BM, BN, 1, 1);
+    constexpr uint32_t kId2 = mxf8_idesc(BM, BN, 2, 2), kId3 = mxf8_idesc(BM, BN, 3, 3);
     for (int64_t id = first_id; ok; id += id_step) {
       const Tile t = tile_of<BN, kMode, kPair>(p, seg, id, crank);
       if (!t.live) break;
@@ -413,18 +420,22 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         tc_fence_after();
         const uint32_t sfa_t = tmem + C::kSfaCol + 4 * s;
         const uint32_t sfb_t = tmem + C::kSfbCol + (BN / 32) * s;
-        tmem_cp_32x128b_x4(sfa_t, smem_desc(smem_u32(smem + C::kOffSfa + s * 512), 0, 128, 0));
+        tmem_cp_32x128b_x4(sfa_t, sfa_desc0 + s * (512 >> 4));
 #pragma unroll
         for (int h = 0; h < C::kSfbTiles; ++h)
-          tmem_cp_32x128b_x4(sfb_t + 4 * h,
-                             smem_desc(smem_u32(smem + C::kOffSfb + s * C::kSfbBytes + h * 512),
-                                       0, 128, 0));
-        const int nblk = (kb == t.nk - 1) ? t.last_blocks : 4;
-        for (int k = 0; k < nblk; ++k) {
-          const uint64_t ad = smem_desc(sa_base + s * C::kABytes + 32 * k, 16, 1024, 2);
-          const uint64_t bd = smem_desc(sb_base + s * C::kBBytes + 32 * k, 16, 1024, 2);
-          mma_mxf8(tmem, ad, bd, mxf8_idesc(BM, BN, k, k), sfa_t, sfb_t,
-                   (kb > 0 || k > 0) ? 1u : 0u);
+          tmem_cp_32x128b_x4(sfb_t + 4 * h, sfb_desc0 + (s * C::kSfbBytes + h * 512) / 16);
+        const uint64_t ad = a_desc0 + s * (C::kABytes / 16);
+        const uint64_t bd = b_desc0 + s * (C::kBBytes / 16);
+        const uint32_t acc0 = kb > 0 ? 1u : 0u;
+        if (kb != t.nk - 1 || t.last_blocks == 4) {  // K step k starts 32 bytes further
+          mma_mxf8(tmem, ad, bd, kId0, sfa_t, sfb_t, acc0);
+          mma_mxf8(tmem, ad + 2, bd + 2, kId1, sfa_t, sfb_t, 1u);
+          mma_mxf8(tmem, ad + 4, bd + 4, kId2, sfa_t, sfb_t, 1u);
+          mma_mxf8(tmem, ad + 6, bd + 6, kId3, sfa_t, sfb_t, 1u);
+        } else {
+          for (int k = 0; k < t.last_blocks; ++k)
+            mma_mxf8(tmem, ad + 2 * k, bd + 2 * k, mxf8_idesc(BM, BN, k, k), sfa_t, sfb_t,
+                     (kb > 0 || k > 0) ? 1u : 0u);
         }
         if (kPair)
           mma_commit_mc(&empty[s], 0x3);  // frees the stage in both CTAs of the pair
@@ -525,6 +536,280 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
   if (warp == 1) {
     __syncwarp();
     tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------- dense GEMM on CTA pairs (2SM)
+//
+// A cluster of two CTAs on two SMs computes 256 x 256 output tiles with
+// tcgen05.mma.cta_group::2 (M = 256). Each CTA stages, per 128-wide K stage, its own 128
+// rows of A, its own 128 rows of the B tile (B is split between the pair), the scale tile
+// of its A rows and both scale tiles of B. Against one-SM 128 x 256 tiles this halves the
+// B bytes each SM stages and reads, and the scale copies per flop, so six stages fit.
+// Every copy of either CTA completes on the leader's `full` barrier; the leader's
+// tcgen05.commit frees a stage in both CTAs and hands the accumulator to both epilogues,
+// whose 16 warps return it on the leader's `acc_empty`.
+namespace duo {
+constexpr int kStages = 6;
+constexpr int kBN = 256;                  // output columns per pair tile
+constexpr int kABytes = BM * BK;          // own 128 A rows
+constexpr int kBBytes = (kBN / 2) * BK;   // own half of the B tile
+constexpr int kSfaBytes = 512;
+constexpr int kSfbBytes = 1024;           // both 128-row scale tiles of B
+constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kABytes;
+constexpr int kOffSfa = kOffB + kStages * kBBytes;
+constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
+constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
+constexpr int kNumBars = 2 * kStages + 3;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 64 + 1024;
+constexpr int kSfaCol = kBN;                 // TMEM: accumulator, then scale slots
+constexpr int kSfbCol = kSfaCol + 4 * kStages;
+constexpr int kTmemCols = 512;
+constexpr int kAccEmptyCount = 2 * kEpiWarps;  // epilogue warps of both CTAs
+static_assert(kSfbCol + 8 * kStages <= kTmemCols, "TMEM overflow");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory overflow");
+}  // namespace duo
+
+struct DuoTile {
+  int64_t m0;        // this CTA's first output row
+  int64_t n0;        // the pair tile's first output column
+  int64_t mt;        // this CTA's 128-row tile index (its A rows and their scales)
+  int64_t nt;        // the pair tile's 256-column index
+  int rows_valid, cols_valid;
+  bool live;
+};
+
+__device__ __forceinline__ DuoTile duo_tile(const Params& p, int64_t pid, uint32_t crank) {
+  DuoTile t;
+  const int64_t n_pm = (p.num_m_tiles + 1) / 2;
+  t.live = pid < n_pm * p.num_n_tiles;
+  if (!t.live) return t;
+  const int64_t GP = p.band;  // bands of p.band pair rows sweep across N, pair rows fastest
+  const int64_t band = GP * p.num_n_tiles;
+  const int64_t first = (pid / band) * GP;
+  const int64_t gp = (n_pm - first) < GP ? (n_pm - first) : GP;
+  const int64_t pm = first + (pid % band) % gp;
+  t.nt = (pid % band) / gp;
+  t.mt = 2 * pm + crank;
+  t.m0 = t.mt * BM;
+  t.n0 = t.nt * duo::kBN;
+  const int64_t left = p.M - t.m0;
+  t.rows_valid = static_cast<int>(left <= 0 ? 0 : (left < BM ? left : BM));
+  t.cols_valid = static_cast<int>((p.N - t.n0) < duo::kBN ? (p.N - t.n0) : duo::kBN);
+  return t;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
+                      const __grid_constant__ CUtensorMap map_b,
+                      const __grid_constant__ CUtensorMap map_sfa,
+                      const __grid_constant__ CUtensorMap map_sfb, const Params p) {
+  using namespace duo;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* full = bars;                  // the leader's count both CTAs' bytes
+  uint64_t* empty = bars + kStages;       // armed in both CTAs by the leader's commit
+  uint64_t* acc_full = bars + 2 * kStages;
+  uint64_t* acc_empty = acc_full + 1;     // the leader's is used
+  uint64_t* mma_done = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const bool leader = crank == 0;
+  const int64_t first_id = blockIdx.x >> 1;
+  const int64_t id_step = gridDim.x >> 1;
+  const int64_t n_kt = (p.K + BK - 1) / BK;
+  const int last_blocks = static_cast<int>(((p.K - (n_kt - 1) * BK) + 31) / 32);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, kAccEmptyCount);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b);
+    tma_prefetch_desc(&map_sfa);
+    tma_prefetch_desc(&map_sfb);
+  }
+  if (warp == 1) tmem_alloc_2sm(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any cross-CTA copy, arrive or commit
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------- TMA producer (both)
+    const uint32_t full0 = cluster_map(&full[0], 0);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t id = first_id; ok; id += id_step) {
+      const DuoTile t = duo_tile(p, id, crank);
+      if (!t.live) break;
+      for (int64_t kb = 0; kb < n_kt; ++kb, ++it) {
+        const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+        if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
+        const uint32_t bar = full0 + 8 * s;
+        if (leader) mbar_arrive_expect_tx(&full[s], 2 * kStageBytes);
+        const int32_t kx = static_cast<int32_t>(kb * BK);
+        tma_load_2d_2sm(smem + kOffA + s * kABytes, &map_a, kx, static_cast<int32_t>(t.m0), bar);
+        tma_load_2d_2sm(smem + kOffB + s * kBBytes, &map_b, kx,
+                        static_cast<int32_t>(t.n0 + crank * (kBN / 2)), bar);
+        tma_load_3d_2sm(smem + kOffSfa + s * kSfaBytes, &map_sfa, 0, static_cast<int32_t>(kb),
+                        static_cast<int32_t>(t.mt), bar);
+        tma_load_3d_2sm(smem + kOffSfb + s * kSfbBytes, &map_sfb, 0, static_cast<int32_t>(kb),
+                        static_cast<int32_t>(2 * t.nt), bar);
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      latch_error(p.status, MXFP8_ERR_TIMEOUT);
+    }
+    if (leader) {  // the leader's full barriers cover both CTAs' copies of a stage
+      const uint32_t n = it < static_cast<uint32_t>(kStages) ? it : kStages;
+      for (uint32_t j = 0; j < n; ++j) {
+        const uint32_t i2 = it - 1 - j;
+        mbar_wait_timed(&full[i2 % kStages], (i2 / kStages) & 1, p.wait_ns);
+      }
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ------------------------------------------------------------- MMA issuer (leader)
+    uint32_t it = 0, acc_it = 0;
+    bool ok = true;
+    const uint64_t a_desc0 = smem_desc(smem_u32(smem + kOffA), 16, 1024, 2);
+    const uint64_t b_desc0 = smem_desc(smem_u32(smem + kOffB), 16, 1024, 2);
+    const uint64_t sfa_desc0 = smem_desc(smem_u32(smem + kOffSfa), 0, 128, 0);
+    const uint64_t sfb_desc0 = smem_desc(smem_u32(smem + kOffSfb), 0, 128, 0);
+    constexpr uint32_t kId0 = mxf8_idesc(2 * BM, kBN, 0, 0), kId1 = mxf8_idesc(2 * BM, kBN, 1, 1);
+    constexpr uint32_t kId2 = mxf8_idesc(2 * BM, kBN, 2, 2), kId3 = mxf8_idesc(2 * BM, kBN, 3, 3);
+    for (int64_t id = first_id; ok; id += id_step) {
+      const DuoTile t = duo_tile(p, id, crank);
+      if (!t.live) break;
+      if (!mbar_wait_bounded(acc_empty, (acc_it & 1) ^ 1, abort_flag, p.wait_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int64_t kb = 0; kb < n_kt; ++kb, ++it) {
+        const uint32_t s = it % kStages, ph = (it / kStages) & 1;
+        if (!mbar_wait_bounded(&full[s], ph, abort_flag, p.wait_ns)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sfa_t = tmem + kSfaCol + 4 * s;
+        const uint32_t sfb_t = tmem + kSfbCol + 8 * s;
+        const uint64_t sbd = sfb_desc0 + s * (kSfbBytes / 16);
+        tmem_cp_32x128b_x4_2sm(sfa_t, sfa_desc0 + s * (kSfaBytes / 16));
+        tmem_cp_32x128b_x4_2sm(sfb_t, sbd);
+        tmem_cp_32x128b_x4_2sm(sfb_t + 4, sbd + 512 / 16);
+        const uint64_t ad = a_desc0 + s * (kABytes / 16);
+        const uint64_t bd = b_desc0 + s * (kBBytes / 16);
+        const uint32_t acc0 = kb > 0 ? 1u : 0u;
+        if (kb != n_kt - 1 || last_blocks == 4) {
+          mma_mxf8_2sm(tmem, ad, bd, kId0, sfa_t, sfb_t, acc0);
+          mma_mxf8_2sm(tmem, ad + 2, bd + 2, kId1, sfa_t, sfb_t, 1u);
+          mma_mxf8_2sm(tmem, ad + 4, bd + 4, kId2, sfa_t, sfb_t, 1u);
+          mma_mxf8_2sm(tmem, ad + 6, bd + 6, kId3, sfa_t, sfb_t, 1u);
+        } else {
+          for (int k = 0; k < last_blocks; ++k)
+            mma_mxf8_2sm(tmem, ad + 2 * k, bd + 2 * k, mxf8_idesc(2 * BM, kBN, k, k), sfa_t,
+                         sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit_2sm_mc(&empty[s], 0x3);
+      }
+      if (!ok) break;
+      mma_commit_2sm_mc(acc_full, 0x3);
+      ++acc_it;
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      latch_error(p.status, MXFP8_ERR_TIMEOUT);
+    }
+    // the pair's tensor-core work must be finished before either CTA frees its TMEM
+    mma_commit_2sm_mc(mma_done, 0x1);
+    mbar_wait_timed(mma_done, 0, p.wait_ns);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------- epilogue (both)
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // which half of the 256 columns
+    constexpr int kChunks = kBN / 64;  // 32-column chunks per warp
+    const uint32_t acc_empty0 = cluster_map(acc_empty, 0);
+    uint32_t acc_it = 0;
+    bool ok = true;
+    for (int64_t id = first_id; ok; id += id_step) {
+      const DuoTile t = duo_tile(p, id, crank);
+      if (!t.live) break;
+      const int r = 32 * q + lane;
+      const bool row_ok = r < t.rows_valid;
+      const int64_t row = t.m0 + r;
+      int got = 0;
+      if (lane == 0) got = mbar_wait_bounded(acc_full, acc_it & 1, abort_flag, p.wait_ns);
+      got = __shfl_sync(0xFFFFFFFFu, got, 0);
+      if (!got) { ok = false; break; }
+      tc_fence_after();
+      // The whole slice goes to registers and TMEM is handed back before any store.
+      uint32_t v[kChunks][32];
+      __syncwarp();
+      const uint32_t base = tmem + (static_cast<uint32_t>(32 * q) << 16) + half * kChunks * 32;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) tmem_ld_32x32b_x32(base + 32 * c, v[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty0);
+      ++acc_it;
+#pragma unroll
+      for (int u = 0; u < kChunks; ++u) {
+        const int c = half * kChunks + u;
+        const int cols_left = t.cols_valid - 32 * c;
+        if (!row_ok || cols_left <= 0) continue;
+        if (p.out_fp32) {
+          float* dst = static_cast<float*>(p.C) + row * p.N + t.n0 + 32 * c;
+          const int nvec = cols_left >= 32 ? 8 : cols_left / 4;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i < nvec)
+              reinterpret_cast<uint4*>(dst)[i] =
+                  make_uint4(v[u][4 * i], v[u][4 * i + 1], v[u][4 * i + 2], v[u][4 * i + 3]);
+        } else {
+          uint16_t* dst = static_cast<uint16_t*>(p.C) + row * p.N + t.n0 + 32 * c;
+          uint32_t b[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            b[i] = cvt_bf16x2(__uint_as_float(v[u][2 * i + 1]), __uint_as_float(v[u][2 * i]));
+          const int nvec = cols_left >= 32 ? 4 : cols_left / 8;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (i < nvec)
+              reinterpret_cast<uint4*>(dst)[i] =
+                  make_uint4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      latch_error(p.status, MXFP8_ERR_TIMEOUT);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still copy into it or arrive on it
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc_2sm(tmem, kTmemCols);
   }
 }
 
@@ -655,6 +940,89 @@ int band_tiles(int64_t M, int64_t N, int64_t K, int num_m_tiles) {
   return static_cast<int>(gm < num_m_tiles ? gm : num_m_tiles);
 }
 
+// The swizzled scales of an operand as a 3-D tensor [row tiles][K tiles][512 bytes], read
+// as 16-bit elements so that one 512-byte scale tile is a single box row.
+bool make_sf_map(CUtensorMap* map, const void* base, int64_t row_tiles, int64_t k_tiles,
+                 uint32_t tiles_per_box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {256, static_cast<cuuint64_t>(k_tiles), static_cast<cuuint64_t>(row_tiles)};
+  cuuint64_t strides[2] = {512, static_cast<cuuint64_t>(k_tiles) * 512};
+  cuuint32_t box[3] = {256, 1, tiles_per_box};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaLaunchConfig_t cluster2_config(int64_t grid, int smem, cudaStream_t stream,
+                                   cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// How many clusters of the 2SM kernel fit on the device at once (cached per device).
+int64_t max_duo_clusters() {
+  static int64_t cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  auto k = mxfp8_gemm_2sm_kernel;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, duo::kSmemBytes) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster2_config(2 * 256, duo::kSmemBytes, nullptr, attr);
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess || clusters <= 0)
+    clusters = num_sms() / 2;
+  if (dev >= 0 && dev < 64) cached[dev] = clusters;
+  return clusters;
+}
+
+// The 2SM kernel is selected with MXFP8_GEMM_2SM=1; by default the one-SM pairs run, which
+// are faster on the measured shapes.
+bool duo_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("MXFP8_GEMM_2SM");
+    return e && e[0] == '1';
+  }();
+  return on;
+}
+
+// Dense GEMM on CTA pairs with 256 x 256 tiles (tcgen05 cta_group::2).
+int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
+  const int64_t n_kt = (a.K + BK - 1) / BK;
+  CUtensorMap ma, mb, msa, msb;
+  if (!make_map(&ma, a.A, 2, a.K, a.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
+  if (!make_map(&mb, a.B, 2, a.K, a.N, 1, BK, duo::kBN / 2)) return MXFP8_ERR_CUDA;
+  if (!make_sf_map(&msa, a.sA, (a.M + 127) / 128, n_kt, 1)) return MXFP8_ERR_CUDA;
+  if (!make_sf_map(&msb, a.sB, (a.N + 127) / 128, n_kt, 2)) return MXFP8_ERR_CUDA;
+  p.num_n_tiles = static_cast<int>((a.N + duo::kBN - 1) / duo::kBN);
+  p.num_tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+  p.band = (band_tiles(a.M, a.N, a.K, p.num_m_tiles) + 1) / 2;
+  const int64_t pair_tiles = static_cast<int64_t>((p.num_m_tiles + 1) / 2) * p.num_n_tiles;
+  const int64_t mc = max_duo_clusters();
+  if (mc <= 0) return MXFP8_ERR_CUDA;
+  const int64_t clusters = pair_tiles < mc ? pair_tiles : mc;
+  if (clusters <= 0) return MXFP8_OK;
+  auto k = mxfp8_gemm_2sm_kernel;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster2_config(2 * clusters, duo::kSmemBytes, stream, attr);
+  return cudaLaunchKernelEx(&cfg, k, ma, mb, msa, msb, p) == cudaSuccess ? MXFP8_OK
+                                                                          : MXFP8_ERR_CUDA;
+}
+
 bool pairs_enabled() {
   static const bool on = [] {
     const char* e = getenv("MXFP8_GEMM_PAIRS");
@@ -682,6 +1050,7 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.num_n_tiles = static_cast<int>((a.N + bn - 1) / bn);
   p.num_tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
   p.band = band_tiles(a.M, a.N, a.K, p.num_m_tiles);
+  if (wide && p.num_m_tiles >= 2 && duo_enabled()) return launch_duo(a, p, stream);
   CUtensorMap ma, mb;
   if (!make_map(&ma, a.A, 2, a.K, a.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
   // A CTA pair shares each B tile: each CTA loads half of it and multicasts it to both.
