@@ -86,6 +86,25 @@ __device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Whole-warp wait: every lane polls the barrier, and all follow lane 0's verdict so that
+// the warp stays converged.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns) {
+  const bool ok = mbar_wait_bounded(bar, parity, abort, limit_ns);
+  return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+}
+
+// True in exactly one lane of the (fully active) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r));
+  return r != 0;
+}
+
 // ------------------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -349,8 +349,10 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------- TMA producer
+    // whole warp in the loop (warp-uniform addresses), one elected lane issues the copies
+    const bool issuer = elect_one();
     uint32_t it = 0;
     bool ok = true;
     for (int64_t id = first_id; ok; id += id_step) {
@@ -361,42 +363,50 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
       const uint32_t bytes = C::kABytes + C::kBBytes + (t.a_valid ? 512 : 0) + 512 * n_sfb;
       for (int kb = 0; kb < t.nk; ++kb, ++it) {
         const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1;
-        if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
-        mbar_arrive_expect_tx(&full[s], bytes);
-        const int32_t kx = static_cast<int32_t>(t.k_origin + static_cast<int64_t>(kb) * BK);
-        tma_load_2d(smem + C::kOffA + s * C::kABytes, &map_a, kx,
-                    static_cast<int32_t>(t.a_row), &full[s]);
-        if (kPair)  // my half of the shared B tile, into both CTAs of the pair
-          tma_load_2d_mc(smem + C::kOffB + s * C::kBBytes + crank * (C::kBBytes / 2), &map_b, kx,
-                         static_cast<int32_t>(t.n0 + crank * (BN / 2)), &full[s], 0x3);
-        else if (kMode == kGroupRows)
-          tma_load_3d(smem + C::kOffB + s * C::kBBytes, &map_b, kx, static_cast<int32_t>(t.n0),
-                      t.b_z, &full[s]);
-        else
-          tma_load_2d(smem + C::kOffB + s * C::kBBytes, &map_b, kx, static_cast<int32_t>(t.n0),
-                      &full[s]);
-        if (t.a_valid)
-          bulk_load(smem + C::kOffSfa + s * 512, p.sA + (t.sfa_tile0 + kb) * 512, 512, &full[s]);
-        for (int h = 0; h < n_sfb; ++h)
-          bulk_load(smem + C::kOffSfb + s * C::kSfbBytes + h * 512,
-                    t.sfb_base + (h * t.sfb_row_tiles_stride + kb) * 512, 512, &full[s]);
+        if (!warp_wait(&empty[s], ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
+        if (issuer) {
+          mbar_arrive_expect_tx(&full[s], bytes);
+          const int32_t kx = static_cast<int32_t>(t.k_origin + static_cast<int64_t>(kb) * BK);
+          tma_load_2d(smem + C::kOffA + s * C::kABytes, &map_a, kx,
+                      static_cast<int32_t>(t.a_row), &full[s]);
+          if (kPair)  // my half of the shared B tile, into both CTAs of the pair
+            tma_load_2d_mc(smem + C::kOffB + s * C::kBBytes + crank * (C::kBBytes / 2), &map_b, kx,
+                           static_cast<int32_t>(t.n0 + crank * (BN / 2)), &full[s], 0x3);
+          else if (kMode == kGroupRows)
+            tma_load_3d(smem + C::kOffB + s * C::kBBytes, &map_b, kx, static_cast<int32_t>(t.n0),
+                        t.b_z, &full[s]);
+          else
+            tma_load_2d(smem + C::kOffB + s * C::kBBytes, &map_b, kx, static_cast<int32_t>(t.n0),
+                        &full[s]);
+          if (t.a_valid)
+            bulk_load(smem + C::kOffSfa + s * 512, p.sA + (t.sfa_tile0 + kb) * 512, 512, &full[s]);
+          for (int h = 0; h < n_sfb; ++h)
+            bulk_load(smem + C::kOffSfb + s * C::kSfbBytes + h * 512,
+                      t.sfb_base + (h * t.sfb_row_tiles_stride + kb) * 512, 512, &full[s]);
+        }
+        __syncwarp();
       }
     }
-    if (!ok) {
+    if (!ok && issuer) {
       *abort_flag = 1;
       latch_error(p.status, MXFP8_ERR_TIMEOUT);
     }
     // whatever happened, no copy may still be landing when the CTA exits
-    const uint32_t n = it < static_cast<uint32_t>(C::kStages) ? it : C::kStages;
-    for (uint32_t j = 0; j < n; ++j) {
-      const uint32_t i2 = it - 1 - j;
-      mbar_wait_timed(&full[i2 % C::kStages], (i2 / C::kStages) & 1, p.wait_ns);
+    if (issuer) {
+      const uint32_t n = it < static_cast<uint32_t>(C::kStages) ? it : C::kStages;
+      for (uint32_t j = 0; j < n; ++j) {
+        const uint32_t i2 = it - 1 - j;
+        mbar_wait_timed(&full[i2 % C::kStages], (i2 / C::kStages) & 1, p.wait_ns);
+      }
     }
-  } else if (warp == 1 && lane == 0) {
+    __syncwarp();
+  } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
-    // One thread issues every tensor-core instruction of the CTA, so its loop is kept
-    // short: descriptors are built once and advanced by adding 16-byte units to their
-    // start-address field (shared addresses stay below 2^18, so no carry leaves it).
+    // The whole warp runs the loop, so that every descriptor and address is warp-uniform
+    // (uniform registers); one elected lane issues the tensor-core instructions. The loop
+    // is kept short: descriptors are built once and advanced by adding 16-byte units to
+    // their start-address field (shared addresses stay below 2^18, so no carry leaves it).
+    const bool issuer = elect_one();
     uint32_t it = 0, acc_it = 0;
     bool ok = true;
     const uint64_t a_desc0 = smem_desc(smem_u32(smem + C::kOffA), 16, 1024, 2);
@@ -409,50 +419,57 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
       const Tile t = tile_of<BN, kMode, kPair>(p, seg, id, crank);
       if (!t.live) break;
       if (t.nk == 0) continue;
-      if (!mbar_wait_bounded(acc_empty, (acc_it & 1) ^ 1, abort_flag, p.wait_ns)) {
+      if (!warp_wait(acc_empty, (acc_it & 1) ^ 1, abort_flag, p.wait_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
       for (int kb = 0; kb < t.nk; ++kb, ++it) {
         const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1;
-        if (!mbar_wait_bounded(&full[s], ph, abort_flag, p.wait_ns)) { ok = false; break; }
+        if (!warp_wait(&full[s], ph, abort_flag, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sfa_t = tmem + C::kSfaCol + 4 * s;
         const uint32_t sfb_t = tmem + C::kSfbCol + (BN / 32) * s;
-        tmem_cp_32x128b_x4(sfa_t, sfa_desc0 + s * (512 >> 4));
-#pragma unroll
-        for (int h = 0; h < C::kSfbTiles; ++h)
-          tmem_cp_32x128b_x4(sfb_t + 4 * h, sfb_desc0 + (s * C::kSfbBytes + h * 512) / 16);
         const uint64_t ad = a_desc0 + s * (C::kABytes / 16);
         const uint64_t bd = b_desc0 + s * (C::kBBytes / 16);
         const uint32_t acc0 = kb > 0 ? 1u : 0u;
-        if (kb != t.nk - 1 || t.last_blocks == 4) {  // K step k starts 32 bytes further
-          mma_mxf8(tmem, ad, bd, kId0, sfa_t, sfb_t, acc0);
-          mma_mxf8(tmem, ad + 2, bd + 2, kId1, sfa_t, sfb_t, 1u);
-          mma_mxf8(tmem, ad + 4, bd + 4, kId2, sfa_t, sfb_t, 1u);
-          mma_mxf8(tmem, ad + 6, bd + 6, kId3, sfa_t, sfb_t, 1u);
-        } else {
-          for (int k = 0; k < t.last_blocks; ++k)
-            mma_mxf8(tmem, ad + 2 * k, bd + 2 * k, mxf8_idesc(BM, BN, k, k), sfa_t, sfb_t,
-                     (kb > 0 || k > 0) ? 1u : 0u);
+        if (issuer) {
+          tmem_cp_32x128b_x4(sfa_t, sfa_desc0 + s * (512 >> 4));
+#pragma unroll
+          for (int h = 0; h < C::kSfbTiles; ++h)
+            tmem_cp_32x128b_x4(sfb_t + 4 * h, sfb_desc0 + (s * C::kSfbBytes + h * 512) / 16);
+          if (kb != t.nk - 1 || t.last_blocks == 4) {  // K step k starts 32 bytes further
+            mma_mxf8(tmem, ad, bd, kId0, sfa_t, sfb_t, acc0);
+            mma_mxf8(tmem, ad + 2, bd + 2, kId1, sfa_t, sfb_t, 1u);
+            mma_mxf8(tmem, ad + 4, bd + 4, kId2, sfa_t, sfb_t, 1u);
+            mma_mxf8(tmem, ad + 6, bd + 6, kId3, sfa_t, sfb_t, 1u);
+          } else {
+            for (int k = 0; k < t.last_blocks; ++k)
+              mma_mxf8(tmem, ad + 2 * k, bd + 2 * k, mxf8_idesc(BM, BN, k, k), sfa_t, sfb_t,
+                       (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          if (kPair)
+            mma_commit_mc(&empty[s], 0x3);  // frees the stage in both CTAs of the pair
+          else
+            mma_commit(&empty[s]);
         }
-        if (kPair)
-          mma_commit_mc(&empty[s], 0x3);  // frees the stage in both CTAs of the pair
-        else
-          mma_commit(&empty[s]);
+        __syncwarp();
       }
       if (!ok) break;
-      mma_commit(acc_full);
+      if (issuer) mma_commit(acc_full);
+      __syncwarp();
       ++acc_it;
     }
-    if (!ok) {
+    if (!ok && issuer) {
       *abort_flag = 1;
       latch_error(p.status, MXFP8_ERR_TIMEOUT);
     }
     // all issued tensor-core work must be finished before TMEM is released
-    mma_commit(mma_done);
-    mbar_wait_timed(mma_done, 0, p.wait_ns);
+    if (issuer) {
+      mma_commit(mma_done);
+      mbar_wait_timed(mma_done, 0, p.wait_ns);
+    }
+    __syncwarp();
   } else if (warp >= 2) {
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;            // TMEM lane quarter this warp may access
@@ -651,8 +668,9 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------- TMA producer (both)
+    const bool issuer = elect_one();
     const uint32_t full0 = cluster_map(&full[0], 0);
     uint32_t it = 0;
     bool ok = true;
@@ -661,32 +679,38 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
       if (!t.live) break;
       for (int64_t kb = 0; kb < n_kt; ++kb, ++it) {
         const uint32_t s = it % kStages, ph = (it / kStages) & 1;
-        if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
+        if (!warp_wait(&empty[s], ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
         const uint32_t bar = full0 + 8 * s;
-        if (leader) mbar_arrive_expect_tx(&full[s], 2 * kStageBytes);
         const int32_t kx = static_cast<int32_t>(kb * BK);
-        tma_load_2d_2sm(smem + kOffA + s * kABytes, &map_a, kx, static_cast<int32_t>(t.m0), bar);
-        tma_load_2d_2sm(smem + kOffB + s * kBBytes, &map_b, kx,
-                        static_cast<int32_t>(t.n0 + crank * (kBN / 2)), bar);
-        tma_load_3d_2sm(smem + kOffSfa + s * kSfaBytes, &map_sfa, 0, static_cast<int32_t>(kb),
-                        static_cast<int32_t>(t.mt), bar);
-        tma_load_3d_2sm(smem + kOffSfb + s * kSfbBytes, &map_sfb, 0, static_cast<int32_t>(kb),
-                        static_cast<int32_t>(2 * t.nt), bar);
+        if (issuer) {
+          if (leader) mbar_arrive_expect_tx(&full[s], 2 * kStageBytes);
+          tma_load_2d_2sm(smem + kOffA + s * kABytes, &map_a, kx, static_cast<int32_t>(t.m0), bar);
+          tma_load_2d_2sm(smem + kOffB + s * kBBytes, &map_b, kx,
+                          static_cast<int32_t>(t.n0 + crank * (kBN / 2)), bar);
+          tma_load_3d_2sm(smem + kOffSfa + s * kSfaBytes, &map_sfa, 0, static_cast<int32_t>(kb),
+                          static_cast<int32_t>(t.mt), bar);
+          tma_load_3d_2sm(smem + kOffSfb + s * kSfbBytes, &map_sfb, 0, static_cast<int32_t>(kb),
+                          static_cast<int32_t>(2 * t.nt), bar);
+        }
+        __syncwarp();
       }
     }
-    if (!ok) {
+    if (!ok && issuer) {
       *abort_flag = 1;
       latch_error(p.status, MXFP8_ERR_TIMEOUT);
     }
-    if (leader) {  // the leader's full barriers cover both CTAs' copies of a stage
+    if (leader && issuer) {  // the leader's full barriers cover both CTAs' copies of a stage
       const uint32_t n = it < static_cast<uint32_t>(kStages) ? it : kStages;
       for (uint32_t j = 0; j < n; ++j) {
         const uint32_t i2 = it - 1 - j;
         mbar_wait_timed(&full[i2 % kStages], (i2 / kStages) & 1, p.wait_ns);
       }
     }
-  } else if (warp == 1 && lane == 0 && leader) {
+    __syncwarp();
+  } else if (warp == 1 && leader) {
     // ------------------------------------------------------------- MMA issuer (leader)
+    // whole warp in the loop (warp-uniform descriptors), one elected lane issues
+    const bool issuer = elect_one();
     uint32_t it = 0, acc_it = 0;
     bool ok = true;
     const uint64_t a_desc0 = smem_desc(smem_u32(smem + kOffA), 16, 1024, 2);
@@ -698,47 +722,54 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     for (int64_t id = first_id; ok; id += id_step) {
       const DuoTile t = duo_tile(p, id, crank);
       if (!t.live) break;
-      if (!mbar_wait_bounded(acc_empty, (acc_it & 1) ^ 1, abort_flag, p.wait_ns)) {
+      if (!warp_wait(acc_empty, (acc_it & 1) ^ 1, abort_flag, p.wait_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
       for (int64_t kb = 0; kb < n_kt; ++kb, ++it) {
         const uint32_t s = it % kStages, ph = (it / kStages) & 1;
-        if (!mbar_wait_bounded(&full[s], ph, abort_flag, p.wait_ns)) { ok = false; break; }
+        if (!warp_wait(&full[s], ph, abort_flag, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sfa_t = tmem + kSfaCol + 4 * s;
         const uint32_t sfb_t = tmem + kSfbCol + 8 * s;
         const uint64_t sbd = sfb_desc0 + s * (kSfbBytes / 16);
-        tmem_cp_32x128b_x4_2sm(sfa_t, sfa_desc0 + s * (kSfaBytes / 16));
-        tmem_cp_32x128b_x4_2sm(sfb_t, sbd);
-        tmem_cp_32x128b_x4_2sm(sfb_t + 4, sbd + 512 / 16);
         const uint64_t ad = a_desc0 + s * (kABytes / 16);
         const uint64_t bd = b_desc0 + s * (kBBytes / 16);
         const uint32_t acc0 = kb > 0 ? 1u : 0u;
-        if (kb != n_kt - 1 || last_blocks == 4) {
-          mma_mxf8_2sm(tmem, ad, bd, kId0, sfa_t, sfb_t, acc0);
-          mma_mxf8_2sm(tmem, ad + 2, bd + 2, kId1, sfa_t, sfb_t, 1u);
-          mma_mxf8_2sm(tmem, ad + 4, bd + 4, kId2, sfa_t, sfb_t, 1u);
-          mma_mxf8_2sm(tmem, ad + 6, bd + 6, kId3, sfa_t, sfb_t, 1u);
-        } else {
-          for (int k = 0; k < last_blocks; ++k)
-            mma_mxf8_2sm(tmem, ad + 2 * k, bd + 2 * k, mxf8_idesc(2 * BM, kBN, k, k), sfa_t,
-                         sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
+        if (issuer) {
+          tmem_cp_32x128b_x4_2sm(sfa_t, sfa_desc0 + s * (kSfaBytes / 16));
+          tmem_cp_32x128b_x4_2sm(sfb_t, sbd);
+          tmem_cp_32x128b_x4_2sm(sfb_t + 4, sbd + 512 / 16);
+          if (kb != n_kt - 1 || last_blocks == 4) {
+            mma_mxf8_2sm(tmem, ad, bd, kId0, sfa_t, sfb_t, acc0);
+            mma_mxf8_2sm(tmem, ad + 2, bd + 2, kId1, sfa_t, sfb_t, 1u);
+            mma_mxf8_2sm(tmem, ad + 4, bd + 4, kId2, sfa_t, sfb_t, 1u);
+            mma_mxf8_2sm(tmem, ad + 6, bd + 6, kId3, sfa_t, sfb_t, 1u);
+          } else {
+            for (int k = 0; k < last_blocks; ++k)
+              mma_mxf8_2sm(tmem, ad + 2 * k, bd + 2 * k, mxf8_idesc(2 * BM, kBN, k, k), sfa_t,
+                           sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit_2sm_mc(&empty[s], 0x3);
         }
-        mma_commit_2sm_mc(&empty[s], 0x3);
+        __syncwarp();
       }
       if (!ok) break;
-      mma_commit_2sm_mc(acc_full, 0x3);
+      if (issuer) mma_commit_2sm_mc(acc_full, 0x3);
+      __syncwarp();
       ++acc_it;
     }
-    if (!ok) {
+    if (!ok && issuer) {
       *abort_flag = 1;
       latch_error(p.status, MXFP8_ERR_TIMEOUT);
     }
     // the pair's tensor-core work must be finished before either CTA frees its TMEM
-    mma_commit_2sm_mc(mma_done, 0x1);
-    mbar_wait_timed(mma_done, 0, p.wait_ns);
+    if (issuer) {
+      mma_commit_2sm_mc(mma_done, 0x1);
+      mbar_wait_timed(mma_done, 0, p.wait_ns);
+    }
+    __syncwarp();
   } else if (warp >= 2) {
     // ------------------------------------------------------------- epilogue (both)
     const int q = warp & 3;            // TMEM lane quarter this warp may access
@@ -990,12 +1021,12 @@ int64_t max_duo_clusters() {
   return clusters;
 }
 
-// The 2SM kernel is selected with MXFP8_GEMM_2SM=1; by default the one-SM pairs run, which
-// are faster on the measured shapes.
+// Dense GEMMs with N > 128 and at least two M tiles run on the 2SM kernel;
+// MXFP8_GEMM_2SM=0 selects the one-SM CTA pairs instead.
 bool duo_enabled() {
   static const bool on = [] {
     const char* e = getenv("MXFP8_GEMM_2SM");
-    return e && e[0] == '1';
+    return !(e && e[0] == '0');
   }();
   return on;
 }
