@@ -24,6 +24,7 @@
 // Every wait is bounded: past the limit the CTA latches MXFP8_ERR_TIMEOUT, all roles
 // leave their loops, outstanding copies and MMAs are waited for, TMEM is freed.
 
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -558,47 +559,62 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 
 // ------------------------------------------------------- dense GEMM on CTA pairs (2SM)
 //
-// A cluster of two CTAs on two SMs computes 256 x 256 output tiles with
+// A cluster of two CTAs on two SMs computes 256 x BN output tiles with
 // tcgen05.mma.cta_group::2 (M = 256). Each CTA stages, per 128-wide K stage, its own 128
-// rows of A, its own 128 rows of the B tile (B is split between the pair), the scale tile
-// of its A rows and both scale tiles of B. Against one-SM 128 x 256 tiles this halves the
-// B bytes each SM stages and reads, and the scale copies per flop, so six stages fit.
-// Every copy of either CTA completes on the leader's `full` barrier; the leader's
-// tcgen05.commit frees a stage in both CTAs and hands the accumulator to both epilogues,
-// whose 16 warps return it on the leader's `acc_empty`.
-namespace duo {
-constexpr int kStages = 6;
-constexpr int kBN = 256;                  // output columns per pair tile
-constexpr int kABytes = BM * BK;          // own 128 A rows
-constexpr int kBBytes = (kBN / 2) * BK;   // own half of the B tile
-constexpr int kSfaBytes = 512;
-constexpr int kSfbBytes = 1024;           // both 128-row scale tiles of B
-constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kABytes;
-constexpr int kOffSfa = kOffB + kStages * kBBytes;
-constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
-constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
-constexpr int kNumBars = 2 * kStages + 3;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 64 + 1024;
-constexpr int kSfaCol = kBN;                 // TMEM: accumulator, then scale slots
-constexpr int kSfbCol = kSfaCol + 4 * kStages;
-constexpr int kTmemCols = 512;
-constexpr int kAccEmptyCount = 2 * kEpiWarps;  // epilogue warps of both CTAs
-static_assert(kSfbCol + 8 * kStages <= kTmemCols, "TMEM overflow");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory overflow");
-}  // namespace duo
+// rows of A, its own BN/2 rows of the B tile (B is split between the pair), the scale tile
+// of its A rows and the two 128-row scale tiles of B that cover the tile's BN columns.
+// Against one-SM 128 x 256 tiles this halves the B bytes each SM stages and reads, and the
+// scale copies per flop. Every copy of either CTA completes on the leader's `full` barrier;
+// the leader's tcgen05.commit frees a stage in both CTAs and hands an accumulator to both
+// epilogues, whose 16 warps return it on the leader's `acc_empty`.
+//
+// BN = 256 keeps one accumulator (256 of the 512 TMEM columns, the rest hold the scale
+// slots). BN = 192 fits two accumulators and seven stages' scale slots, so the next
+// tile's MMAs run while the epilogue drains the previous one. A 192-column tile starts
+// either on a 128-row scale tile or 64 rows into one. Both scale tiles are always copied
+// to the slot's 4-aligned columns; in the second case the MMA's B-scale address is two
+// columns further on, where the scales of the tile's B rows 0-31 are.
+template <int BN>
+struct Duo {
+  static constexpr int kAcc = BN == 256 ? 1 : 2;       // accumulator buffers
+  static constexpr int kStages = BN == 256 ? 6 : 7;
+  static constexpr int kABytes = BM * BK;              // own 128 A rows
+  static constexpr int kBBytes = (BN / 2) * BK;        // own half of the B tile
+  static constexpr int kSfaBytes = 512;
+  static constexpr int kSfbBytes = 1024;               // two 128-row scale tiles of B
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffSfa = kOffB + kStages * kBBytes;
+  static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
+  static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
+  static constexpr int kNumBars = 2 * kStages + 2 * kAcc + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  // epilogue staging: one 32-row x 64-byte box (2 KB) per epilogue warp, 1024-aligned
+  static constexpr int kStageBoxBytes = 32 * 64;
+  static constexpr int kOffOut = (kOffMisc + 64 + 1023) / 1024 * 1024;
+  static constexpr int kSmemBytes = kOffOut + kEpiWarps * kStageBoxBytes + 1024;
+  static constexpr int kSfaCol = kAcc * BN;            // TMEM: accumulators, then scales
+  static constexpr int kSfbSlot = 8;                   // columns per B scale slot
+  static constexpr int kSfbCol = kSfaCol + 4 * kStages;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kAccEmptyCount = 2 * kEpiWarps;  // epilogue warps of both CTAs
+  static_assert(kSfbCol + kSfbSlot * kStages <= kTmemCols, "TMEM overflow");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory overflow");
+  static_assert(kBBytes % 1024 == 0, "B stages must keep the 1024-byte swizzle alignment");
+};
 
 struct DuoTile {
   int64_t m0;        // this CTA's first output row
   int64_t n0;        // the pair tile's first output column
   int64_t mt;        // this CTA's 128-row tile index (its A rows and their scales)
-  int64_t nt;        // the pair tile's 256-column index
+  int64_t sfb_tile;  // first 128-row scale tile of B the pair tile touches
+  int sfb_shift;     // 0, or 2 when the tile starts 64 rows into that scale tile
   int rows_valid, cols_valid;
   bool live;
 };
 
+template <int BN>
 __device__ __forceinline__ DuoTile duo_tile(const Params& p, int64_t pid, uint32_t crank) {
   DuoTile t;
   const int64_t n_pm = (p.num_m_tiles + 1) / 2;
@@ -609,33 +625,38 @@ __device__ __forceinline__ DuoTile duo_tile(const Params& p, int64_t pid, uint32
   const int64_t first = (pid / band) * GP;
   const int64_t gp = (n_pm - first) < GP ? (n_pm - first) : GP;
   const int64_t pm = first + (pid % band) % gp;
-  t.nt = (pid % band) / gp;
+  const int64_t nt = (pid % band) / gp;
   t.mt = 2 * pm + crank;
   t.m0 = t.mt * BM;
-  t.n0 = t.nt * duo::kBN;
+  t.n0 = nt * BN;
+  t.sfb_tile = t.n0 / 128;
+  t.sfb_shift = static_cast<int>((t.n0 % 128) / 32);
   const int64_t left = p.M - t.m0;
   t.rows_valid = static_cast<int>(left <= 0 ? 0 : (left < BM ? left : BM));
-  t.cols_valid = static_cast<int>((p.N - t.n0) < duo::kBN ? (p.N - t.n0) : duo::kBN);
+  t.cols_valid = static_cast<int>((p.N - t.n0) < BN ? (p.N - t.n0) : BN);
   return t;
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
 mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
                       const __grid_constant__ CUtensorMap map_b,
                       const __grid_constant__ CUtensorMap map_sfa,
-                      const __grid_constant__ CUtensorMap map_sfb, const Params p) {
-  using namespace duo;
+                      const __grid_constant__ CUtensorMap map_sfb,
+                      const __grid_constant__ CUtensorMap map_c, const Params p) {
+  using D = Duo<BN>;
+  constexpr int kStages = D::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* full = bars;                  // the leader's count both CTAs' bytes
-  uint64_t* empty = bars + kStages;       // armed in both CTAs by the leader's commit
-  uint64_t* acc_full = bars + 2 * kStages;
-  uint64_t* acc_empty = acc_full + 1;     // the leader's is used
-  uint64_t* mma_done = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + D::kOffBar);
+  uint64_t* full = bars;                    // the leader's count both CTAs' bytes
+  uint64_t* empty = bars + kStages;         // armed in both CTAs by the leader's commit
+  uint64_t* acc_full = bars + 2 * kStages;  // [kAcc], armed in both CTAs
+  uint64_t* acc_empty = acc_full + D::kAcc; // [kAcc], the leader's are used
+  uint64_t* mma_done = acc_empty + D::kAcc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + D::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + D::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -651,8 +672,10 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, kAccEmptyCount);
+    for (int b = 0; b < D::kAcc; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], D::kAccEmptyCount);
+    }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -660,8 +683,9 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     tma_prefetch_desc(&map_b);
     tma_prefetch_desc(&map_sfa);
     tma_prefetch_desc(&map_sfb);
+    tma_prefetch_desc(&map_c);
   }
-  if (warp == 1) tmem_alloc_2sm(tmem_slot, kTmemCols);
+  if (warp == 1) tmem_alloc_2sm(tmem_slot, D::kTmemCols);
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // both CTAs' barriers exist before any cross-CTA copy, arrive or commit
@@ -670,12 +694,13 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
 
   if (warp == 0) {
     // ------------------------------------------------------------- TMA producer (both)
+    // whole warp in the loop (warp-uniform addresses), one elected lane issues the copies
     const bool issuer = elect_one();
     const uint32_t full0 = cluster_map(&full[0], 0);
     uint32_t it = 0;
     bool ok = true;
     for (int64_t id = first_id; ok; id += id_step) {
-      const DuoTile t = duo_tile(p, id, crank);
+      const DuoTile t = duo_tile<BN>(p, id, crank);
       if (!t.live) break;
       for (int64_t kb = 0; kb < n_kt; ++kb, ++it) {
         const uint32_t s = it % kStages, ph = (it / kStages) & 1;
@@ -683,14 +708,15 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
         const uint32_t bar = full0 + 8 * s;
         const int32_t kx = static_cast<int32_t>(kb * BK);
         if (issuer) {
-          if (leader) mbar_arrive_expect_tx(&full[s], 2 * kStageBytes);
-          tma_load_2d_2sm(smem + kOffA + s * kABytes, &map_a, kx, static_cast<int32_t>(t.m0), bar);
-          tma_load_2d_2sm(smem + kOffB + s * kBBytes, &map_b, kx,
-                          static_cast<int32_t>(t.n0 + crank * (kBN / 2)), bar);
-          tma_load_3d_2sm(smem + kOffSfa + s * kSfaBytes, &map_sfa, 0, static_cast<int32_t>(kb),
-                          static_cast<int32_t>(t.mt), bar);
-          tma_load_3d_2sm(smem + kOffSfb + s * kSfbBytes, &map_sfb, 0, static_cast<int32_t>(kb),
-                          static_cast<int32_t>(2 * t.nt), bar);
+          if (leader) mbar_arrive_expect_tx(&full[s], 2 * D::kStageBytes);
+          tma_load_2d_2sm(smem + D::kOffA + s * D::kABytes, &map_a, kx,
+                          static_cast<int32_t>(t.m0), bar);
+          tma_load_2d_2sm(smem + D::kOffB + s * D::kBBytes, &map_b, kx,
+                          static_cast<int32_t>(t.n0 + crank * (BN / 2)), bar);
+          tma_load_3d_2sm(smem + D::kOffSfa + s * D::kSfaBytes, &map_sfa, 0,
+                          static_cast<int32_t>(kb), static_cast<int32_t>(t.mt), bar);
+          tma_load_3d_2sm(smem + D::kOffSfb + s * D::kSfbBytes, &map_sfb, 0,
+                          static_cast<int32_t>(kb), static_cast<int32_t>(t.sfb_tile), bar);
         }
         __syncwarp();
       }
@@ -713,42 +739,46 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     const bool issuer = elect_one();
     uint32_t it = 0, acc_it = 0;
     bool ok = true;
-    const uint64_t a_desc0 = smem_desc(smem_u32(smem + kOffA), 16, 1024, 2);
-    const uint64_t b_desc0 = smem_desc(smem_u32(smem + kOffB), 16, 1024, 2);
-    const uint64_t sfa_desc0 = smem_desc(smem_u32(smem + kOffSfa), 0, 128, 0);
-    const uint64_t sfb_desc0 = smem_desc(smem_u32(smem + kOffSfb), 0, 128, 0);
-    constexpr uint32_t kId0 = mxf8_idesc(2 * BM, kBN, 0, 0), kId1 = mxf8_idesc(2 * BM, kBN, 1, 1);
-    constexpr uint32_t kId2 = mxf8_idesc(2 * BM, kBN, 2, 2), kId3 = mxf8_idesc(2 * BM, kBN, 3, 3);
+    const uint64_t a_desc0 = smem_desc(smem_u32(smem + D::kOffA), 16, 1024, 2);
+    const uint64_t b_desc0 = smem_desc(smem_u32(smem + D::kOffB), 16, 1024, 2);
+    const uint64_t sfa_desc0 = smem_desc(smem_u32(smem + D::kOffSfa), 0, 128, 0);
+    const uint64_t sfb_desc0 = smem_desc(smem_u32(smem + D::kOffSfb), 0, 128, 0);
+    constexpr uint32_t kId0 = mxf8_idesc(2 * BM, BN, 0, 0), kId1 = mxf8_idesc(2 * BM, BN, 1, 1);
+    constexpr uint32_t kId2 = mxf8_idesc(2 * BM, BN, 2, 2), kId3 = mxf8_idesc(2 * BM, BN, 3, 3);
     for (int64_t id = first_id; ok; id += id_step) {
-      const DuoTile t = duo_tile(p, id, crank);
+      const DuoTile t = duo_tile<BN>(p, id, crank);
       if (!t.live) break;
-      if (!warp_wait(acc_empty, (acc_it & 1) ^ 1, abort_flag, p.wait_ns)) {
+      const uint32_t buf = acc_it % D::kAcc, aph = (acc_it / D::kAcc) & 1;
+      if (!warp_wait(&acc_empty[buf], aph ^ 1, abort_flag, p.wait_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      const uint32_t d_t = tmem + buf * BN;
+      const uint32_t shift = static_cast<uint32_t>(t.sfb_shift);
       for (int64_t kb = 0; kb < n_kt; ++kb, ++it) {
         const uint32_t s = it % kStages, ph = (it / kStages) & 1;
         if (!warp_wait(&full[s], ph, abort_flag, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sfa_t = tmem + kSfaCol + 4 * s;
-        const uint32_t sfb_t = tmem + kSfbCol + 8 * s;
-        const uint64_t sbd = sfb_desc0 + s * (kSfbBytes / 16);
-        const uint64_t ad = a_desc0 + s * (kABytes / 16);
-        const uint64_t bd = b_desc0 + s * (kBBytes / 16);
+        const uint32_t sfa_t = tmem + D::kSfaCol + 4 * s;
+        const uint32_t sfb_slot = tmem + D::kSfbCol + D::kSfbSlot * s;
+        const uint32_t sfb_t = sfb_slot + shift;  // B rows 0-31 of the tile
+        const uint64_t sbd = sfb_desc0 + s * (D::kSfbBytes / 16);
+        const uint64_t ad = a_desc0 + s * (D::kABytes / 16);
+        const uint64_t bd = b_desc0 + s * (D::kBBytes / 16);
         const uint32_t acc0 = kb > 0 ? 1u : 0u;
         if (issuer) {
-          tmem_cp_32x128b_x4_2sm(sfa_t, sfa_desc0 + s * (kSfaBytes / 16));
-          tmem_cp_32x128b_x4_2sm(sfb_t, sbd);
-          tmem_cp_32x128b_x4_2sm(sfb_t + 4, sbd + 512 / 16);
+          tmem_cp_32x128b_x4_2sm(sfa_t, sfa_desc0 + s * (D::kSfaBytes / 16));
+          tmem_cp_32x128b_x4_2sm(sfb_slot, sbd);
+          tmem_cp_32x128b_x4_2sm(sfb_slot + 4, sbd + 512 / 16);
           if (kb != n_kt - 1 || last_blocks == 4) {
-            mma_mxf8_2sm(tmem, ad, bd, kId0, sfa_t, sfb_t, acc0);
-            mma_mxf8_2sm(tmem, ad + 2, bd + 2, kId1, sfa_t, sfb_t, 1u);
-            mma_mxf8_2sm(tmem, ad + 4, bd + 4, kId2, sfa_t, sfb_t, 1u);
-            mma_mxf8_2sm(tmem, ad + 6, bd + 6, kId3, sfa_t, sfb_t, 1u);
+            mma_mxf8_2sm(d_t, ad, bd, kId0, sfa_t, sfb_t, acc0);
+            mma_mxf8_2sm(d_t, ad + 2, bd + 2, kId1, sfa_t, sfb_t, 1u);
+            mma_mxf8_2sm(d_t, ad + 4, bd + 4, kId2, sfa_t, sfb_t, 1u);
+            mma_mxf8_2sm(d_t, ad + 6, bd + 6, kId3, sfa_t, sfb_t, 1u);
           } else {
             for (int k = 0; k < last_blocks; ++k)
-              mma_mxf8_2sm(tmem, ad + 2 * k, bd + 2 * k, mxf8_idesc(2 * BM, kBN, k, k), sfa_t,
+              mma_mxf8_2sm(d_t, ad + 2 * k, bd + 2 * k, mxf8_idesc(2 * BM, BN, k, k), sfa_t,
                            sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit_2sm_mc(&empty[s], 0x3);
@@ -756,7 +786,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
         __syncwarp();
       }
       if (!ok) break;
-      if (issuer) mma_commit_2sm_mc(acc_full, 0x3);
+      if (issuer) mma_commit_2sm_mc(&acc_full[buf], 0x3);
       __syncwarp();
       ++acc_it;
     }
@@ -773,61 +803,80 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
   } else if (warp >= 2) {
     // ------------------------------------------------------------- epilogue (both)
     const int q = warp & 3;            // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;  // which half of the 256 columns
-    constexpr int kChunks = kBN / 64;  // 32-column chunks per warp
-    const uint32_t acc_empty0 = cluster_map(acc_empty, 0);
+    const int half = (warp - 2) >> 2;  // which half of the BN columns
+    constexpr int kChunks = BN / 64;   // 32-column chunks per warp
+    const uint32_t acc_empty0 = cluster_map(&acc_empty[0], 0);
+    uint8_t* box = smem + D::kOffOut + (warp - 2) * D::kStageBoxBytes;
     uint32_t acc_it = 0;
     bool ok = true;
     for (int64_t id = first_id; ok; id += id_step) {
-      const DuoTile t = duo_tile(p, id, crank);
+      const DuoTile t = duo_tile<BN>(p, id, crank);
       if (!t.live) break;
-      const int r = 32 * q + lane;
-      const bool row_ok = r < t.rows_valid;
-      const int64_t row = t.m0 + r;
+      const uint32_t buf = acc_it % D::kAcc, aph = (acc_it / D::kAcc) & 1;
       int got = 0;
-      if (lane == 0) got = mbar_wait_bounded(acc_full, acc_it & 1, abort_flag, p.wait_ns);
+      if (lane == 0) got = mbar_wait_bounded(&acc_full[buf], aph, abort_flag, p.wait_ns);
       got = __shfl_sync(0xFFFFFFFFu, got, 0);
       if (!got) { ok = false; break; }
       tc_fence_after();
       // The whole slice goes to registers and TMEM is handed back before any store.
       uint32_t v[kChunks][32];
       __syncwarp();
-      const uint32_t base = tmem + (static_cast<uint32_t>(32 * q) << 16) + half * kChunks * 32;
+      const uint32_t base =
+          tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + half * kChunks * 32;
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) tmem_ld_32x32b_x32(base + 32 * c, v[c]);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc_empty0);
+      if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8 * buf);
       ++acc_it;
+      // Stores leave through shared memory: each 64-byte column group of the warp's 32 rows
+      // is written into the warp's staging box (16-byte chunks XOR-swizzled as the tensor
+      // map's 64-byte swizzle expects, so the 32 lanes hit distinct banks) and sent with one
+      // TMA store, which clips rows and columns past the matrix. One thread-row per lane
+      // would otherwise touch 32 cache lines per store instruction.
+      if (32 * q < t.rows_valid) {
 #pragma unroll
-      for (int u = 0; u < kChunks; ++u) {
-        const int c = half * kChunks + u;
-        const int cols_left = t.cols_valid - 32 * c;
-        if (!row_ok || cols_left <= 0) continue;
-        if (p.out_fp32) {
-          float* dst = static_cast<float*>(p.C) + row * p.N + t.n0 + 32 * c;
-          const int nvec = cols_left >= 32 ? 8 : cols_left / 4;
+        for (int u = 0; u < kChunks; ++u) {
+          const int c = half * kChunks + u;
+          if (32 * c >= t.cols_valid) continue;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (i < nvec)
-              reinterpret_cast<uint4*>(dst)[i] =
-                  make_uint4(v[u][4 * i], v[u][4 * i + 1], v[u][4 * i + 2], v[u][4 * i + 3]);
-        } else {
-          uint16_t* dst = static_cast<uint16_t*>(p.C) + row * p.N + t.n0 + 32 * c;
-          uint32_t b[16];
+          for (int g = 0; g < (p.out_fp32 ? 2 : 1); ++g) {
+            uint4 w[4];
+            if (p.out_fp32) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            b[i] = cvt_bf16x2(__uint_as_float(v[u][2 * i + 1]), __uint_as_float(v[u][2 * i]));
-          const int nvec = cols_left >= 32 ? 4 : cols_left / 8;
+              for (int j = 0; j < 4; ++j)
+                w[j] = make_uint4(v[u][16 * g + 4 * j], v[u][16 * g + 4 * j + 1],
+                                  v[u][16 * g + 4 * j + 2], v[u][16 * g + 4 * j + 3]);
+            } else {
+              uint32_t b[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (i < nvec)
-              reinterpret_cast<uint4*>(dst)[i] =
-                  make_uint4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
+              for (int i = 0; i < 16; ++i)
+                b[i] = cvt_bf16x2(__uint_as_float(v[u][2 * i + 1]), __uint_as_float(v[u][2 * i]));
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                w[j] = make_uint4(b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
+            }
+            const int col = 32 * c + 16 * g;  // first column of this group
+            if (p.out_fp32 && col >= t.cols_valid) continue;
+            if (lane == 0) bulk_wait_read_all();  // the box is free again
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(box + lane * 64 + 16 * (j ^ ((lane >> 1) & 3))) = w[j];
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&map_c, box, static_cast<int32_t>(t.n0 + col),
+                           static_cast<int32_t>(t.m0 + 32 * q));
+              bulk_commit_group();
+            }
+          }
         }
       }
     }
+    if (lane == 0) bulk_wait_all();  // every store has landed before the CTA can exit
+    __syncwarp();
     if (!ok && lane == 0) {
       *abort_flag = 1;
       latch_error(p.status, MXFP8_ERR_TIMEOUT);
@@ -840,7 +889,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc_2sm(tmem, kTmemCols);
+    tmem_dealloc_2sm(tmem, D::kTmemCols);
   }
 }
 
@@ -986,6 +1035,22 @@ bool make_sf_map(CUtensorMap* map, const void* base, int64_t row_tiles, int64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The output C [M][N] (BF16 or FP32) for TMA stores of 32-row x 64-byte boxes, 64-byte
+// swizzle.
+bool make_out_map(CUtensorMap* map, void* base, int64_t M, int64_t N, bool fp32) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const uint32_t elem = fp32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * elem};
+  cuuint32_t box[2] = {64 / elem, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaLaunchConfig_t cluster2_config(int64_t grid, int smem, cudaStream_t stream,
                                    cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
@@ -1003,17 +1068,18 @@ cudaLaunchConfig_t cluster2_config(int64_t grid, int smem, cudaStream_t stream,
 }
 
 // How many clusters of the 2SM kernel fit on the device at once (cached per device).
+template <int BN>
 int64_t max_duo_clusters() {
   static int64_t cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
-  auto k = mxfp8_gemm_2sm_kernel;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, duo::kSmemBytes) !=
-      cudaSuccess)
+  auto k = mxfp8_gemm_2sm_kernel<BN>;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Duo<BN>::kSmemBytes) != cudaSuccess)
     return 0;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster2_config(2 * 256, duo::kSmemBytes, nullptr, attr);
+  cudaLaunchConfig_t cfg = cluster2_config(2 * 256, Duo<BN>::kSmemBytes, nullptr, attr);
   int clusters = 0;
   if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess || clusters <= 0)
     clusters = num_sms() / 2;
@@ -1031,27 +1097,52 @@ bool duo_enabled() {
   return on;
 }
 
-// Dense GEMM on CTA pairs with 256 x 256 tiles (tcgen05 cta_group::2).
+// Tile width of the 2SM kernel for one problem. A 256-wide tile does 4/3 the work of a
+// 192-wide one in about the same stage time, but tile counts that leave the last wave of
+// clusters nearly empty waste up to a sixth of the launch; 192 is taken when its fuller
+// last wave outweighs the narrower tile: 0.75 x wave efficiency(192) > 0.85 x wave
+// efficiency(256) (the factor was fitted on the Qwen3-8B layer shapes). MXFP8_GEMM_BN=256
+// or 192 forces a width.
+int duo_width(int64_t M, int64_t N) {
+  static const int forced = [] {
+    const char* e = getenv("MXFP8_GEMM_BN");
+    const int w = e ? atoi(e) : 0;
+    return (w == 256 || w == 192) ? w : 0;
+  }();
+  if (forced) return forced;
+  const double clusters = static_cast<double>(num_sms() / 2);
+  auto eff = [&](int bn) {
+    const double tiles = static_cast<double>(((M + 255) / 256) * ((N + bn - 1) / bn));
+    const double waves = tiles / clusters;
+    return waves / std::ceil(waves);
+  };
+  return 0.75 * eff(192) > 0.85 * eff(256) ? 192 : 256;
+}
+
+// Dense GEMM on CTA pairs with 256 x BN tiles (tcgen05 cta_group::2).
+template <int BN>
 int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
+  using D = Duo<BN>;
   const int64_t n_kt = (a.K + BK - 1) / BK;
-  CUtensorMap ma, mb, msa, msb;
+  CUtensorMap ma, mb, msa, msb, mc;
   if (!make_map(&ma, a.A, 2, a.K, a.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
-  if (!make_map(&mb, a.B, 2, a.K, a.N, 1, BK, duo::kBN / 2)) return MXFP8_ERR_CUDA;
+  if (!make_map(&mb, a.B, 2, a.K, a.N, 1, BK, BN / 2)) return MXFP8_ERR_CUDA;
+  if (!make_out_map(&mc, a.C, a.M, a.N, a.out_dtype == MXFP8_OUT_FP32)) return MXFP8_ERR_CUDA;
   if (!make_sf_map(&msa, a.sA, (a.M + 127) / 128, n_kt, 1)) return MXFP8_ERR_CUDA;
   if (!make_sf_map(&msb, a.sB, (a.N + 127) / 128, n_kt, 2)) return MXFP8_ERR_CUDA;
-  p.num_n_tiles = static_cast<int>((a.N + duo::kBN - 1) / duo::kBN);
+  p.num_n_tiles = static_cast<int>((a.N + BN - 1) / BN);
   p.num_tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
   p.band = (band_tiles(a.M, a.N, a.K, p.num_m_tiles) + 1) / 2;
   const int64_t pair_tiles = static_cast<int64_t>((p.num_m_tiles + 1) / 2) * p.num_n_tiles;
-  const int64_t mc = max_duo_clusters();
-  if (mc <= 0) return MXFP8_ERR_CUDA;
-  const int64_t clusters = pair_tiles < mc ? pair_tiles : mc;
+  const int64_t fit = max_duo_clusters<BN>();
+  if (fit <= 0) return MXFP8_ERR_CUDA;
+  const int64_t clusters = pair_tiles < fit ? pair_tiles : fit;
   if (clusters <= 0) return MXFP8_OK;
-  auto k = mxfp8_gemm_2sm_kernel;
+  auto k = mxfp8_gemm_2sm_kernel<BN>;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster2_config(2 * clusters, duo::kSmemBytes, stream, attr);
-  return cudaLaunchKernelEx(&cfg, k, ma, mb, msa, msb, p) == cudaSuccess ? MXFP8_OK
-                                                                          : MXFP8_ERR_CUDA;
+  cudaLaunchConfig_t cfg = cluster2_config(2 * clusters, D::kSmemBytes, stream, attr);
+  return cudaLaunchKernelEx(&cfg, k, ma, mb, msa, msb, mc, p) == cudaSuccess ? MXFP8_OK
+                                                                              : MXFP8_ERR_CUDA;
 }
 
 bool pairs_enabled() {
@@ -1081,7 +1172,9 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.num_n_tiles = static_cast<int>((a.N + bn - 1) / bn);
   p.num_tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
   p.band = band_tiles(a.M, a.N, a.K, p.num_m_tiles);
-  if (wide && p.num_m_tiles >= 2 && duo_enabled()) return launch_duo(a, p, stream);
+  if (wide && p.num_m_tiles >= 2 && duo_enabled())
+    return duo_width(a.M, a.N) == 256 ? launch_duo<256>(a, p, stream)
+                                      : launch_duo<192>(a, p, stream);
   CUtensorMap ma, mb;
   if (!make_map(&ma, a.A, 2, a.K, a.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
   // A CTA pair shares each B tile: each CTA loads half of it and multicasts it to both.
