@@ -63,7 +63,10 @@ struct Cfg {
   static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
   static constexpr int kNumBars = 2 * kStages + 3;  // full, empty, acc_full, acc_empty, done
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+  // epilogue staging: one 32-row x 64-byte box (2 KB) per epilogue warp, 1024-aligned
+  static constexpr int kStageBoxBytes = 32 * 64;
+  static constexpr int kOffOut = (kOffMisc + 64 + 1023) / 1024 * 1024;
+  static constexpr int kSmemBytes = kOffOut + kEpiWarps * kStageBoxBytes + 1024;  // + slack
   // TMEM columns: accumulator, then per-stage scale slots
   static constexpr int kSfaCol = BN;
   static constexpr int kSfbCol = BN + 4 * kStages;
@@ -104,8 +107,7 @@ struct Tile {
   int64_t sfa_kstride;   // tiles between consecutive stages (1)
   const uint8_t* sfb_base;
   int64_t sfb_row_tiles_stride;  // tiles between consecutive 128-row B tiles
-  int64_t c_off;         // element offset of the problem's C
-  int64_t ldc;
+  int c_z;               // the problem's index in the output map (expert for wgrad)
   bool a_valid;          // the A row tile exists (a CTA pair may overhang M by one tile)
   bool live;
 };
@@ -156,8 +158,7 @@ __device__ Tile make_tile(const Params& p, const SegShared* seg, int64_t id) {
     t.sfa_kstride = 1;
     t.sfb_base = p.sB + nt * (BN / 128) * n_kt_dense * 512;
     t.sfb_row_tiles_stride = n_kt_dense;
-    t.c_off = 0;
-    t.ldc = p.N;
+    t.c_z = 0;
     t.live = true;
     return t;
   }
@@ -182,8 +183,7 @@ __device__ Tile make_tile(const Params& p, const SegShared* seg, int64_t id) {
     t.sfa_kstride = 1;
     t.sfb_base = p.sB + e * p.sb_item_bytes + nt * (BN / 128) * n_kt_dense * 512;
     t.sfb_row_tiles_stride = n_kt_dense;
-    t.c_off = 0;
-    t.ldc = p.N;
+    t.c_z = 0;
     t.live = true;
     return t;
   }
@@ -213,8 +213,7 @@ __device__ Tile make_tile(const Params& p, const SegShared* seg, int64_t id) {
   t.sfa_kstride = 1;
   t.sfb_base = p.sB + (n_rt_b * tb + nt * (BN / 128) * nk) * 512;
   t.sfb_row_tiles_stride = nk;
-  t.c_off = static_cast<int64_t>(e) * p.M * p.N;
-  t.ldc = p.N;
+  t.c_z = e;
   t.live = true;
   return t;
 }
@@ -249,8 +248,7 @@ __device__ Tile make_tile_pair(const Params& p, int64_t pid, uint32_t crank) {
   t.sfa_kstride = 1;
   t.sfb_base = p.sB + nt * (BN / 128) * n_kt * 512;
   t.sfb_row_tiles_stride = n_kt;
-  t.c_off = 0;
-  t.ldc = p.N;
+  t.c_z = 0;
   t.a_valid = mt < p.num_m_tiles;
   t.live = true;
   return t;
@@ -266,7 +264,8 @@ __device__ __forceinline__ Tile tile_of(const Params& p, const SegShared* seg, i
 template <int BN, int kMode, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
-                  const __grid_constant__ CUtensorMap map_b, const Params p) {
+                  const __grid_constant__ CUtensorMap map_b,
+                  const __grid_constant__ CUtensorMap map_c, const Params p) {
   using C = Cfg<BN>;
   static_assert(!kPair || kMode == kDense, "CTA pairs are used for the dense GEMM only");
   // persistent tile loop: CTAs (or CTA pairs) stride over the tile list
@@ -302,6 +301,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     fence_barrier_init();
     tma_prefetch_desc(&map_a);
     tma_prefetch_desc(&map_b);
+    tma_prefetch_desc(&map_c);
   }
   if (kMode != kDense) {
     // segment table: offsets checked (0-based, non-decreasing, 32-aligned, ending at
@@ -476,14 +476,12 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;  // which half of the BN columns
     constexpr int kChunks = BN / 64;   // 32-column chunks per warp
+    uint8_t* box = smem + C::kOffOut + (warp - 2) * C::kStageBoxBytes;
     uint32_t acc_it = 0;
     bool ok = true;
     for (int64_t id = first_id; ok; id += id_step) {
       const Tile t = tile_of<BN, kMode, kPair>(p, seg, id, crank);
       if (!t.live) break;
-      const int r = 32 * q + lane;
-      const bool row_ok = r < t.rows_valid;
-      const int64_t row = t.m0 + r;
       if (t.nk > 0) {
         // one lane waits, the warp follows its verdict (keeps the warp converged)
         int got = 0;
@@ -512,34 +510,52 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[c][i] = 0;
       }
+      // Stores leave through shared memory: each 64-byte column group of the warp's 32 rows
+      // is written into the warp's staging box (16-byte chunks XOR-swizzled as the tensor
+      // map's 64-byte swizzle expects) and sent with one TMA store, clipped at the matrix
+      // edge. Segments are 32-row aligned, so a box never crosses into another expert.
+      if (32 * q < t.rows_valid) {
 #pragma unroll
-      for (int u = 0; u < kChunks; ++u) {
-        const int c = half * kChunks + u;
-        const int cols_left = t.cols_valid - 32 * c;
-        if (!row_ok || cols_left <= 0) continue;
-        if (p.out_fp32) {
-          float* dst = static_cast<float*>(p.C) + t.c_off + row * t.ldc + t.n0 + 32 * c;
-          const int nvec = cols_left >= 32 ? 8 : cols_left / 4;
+        for (int u = 0; u < kChunks; ++u) {
+          const int c = half * kChunks + u;
+          if (32 * c >= t.cols_valid) continue;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (i < nvec)
-              reinterpret_cast<uint4*>(dst)[i] =
-                  make_uint4(v[u][4 * i], v[u][4 * i + 1], v[u][4 * i + 2], v[u][4 * i + 3]);
-        } else {
-          uint16_t* dst = static_cast<uint16_t*>(p.C) + t.c_off + row * t.ldc + t.n0 + 32 * c;
-          uint32_t b[16];
+          for (int g = 0; g < (p.out_fp32 ? 2 : 1); ++g) {
+            const int col = 32 * c + 16 * g;  // first column of this group
+            if (col >= t.cols_valid) continue;
+            uint4 w[4];
+            if (p.out_fp32) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            b[i] = cvt_bf16x2(__uint_as_float(v[u][2 * i + 1]), __uint_as_float(v[u][2 * i]));
-          const int nvec = cols_left >= 32 ? 4 : cols_left / 8;
+              for (int j = 0; j < 4; ++j)
+                w[j] = make_uint4(v[u][16 * g + 4 * j], v[u][16 * g + 4 * j + 1],
+                                  v[u][16 * g + 4 * j + 2], v[u][16 * g + 4 * j + 3]);
+            } else {
+              uint32_t b[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (i < nvec)
-              reinterpret_cast<uint4*>(dst)[i] =
-                  make_uint4(b[4 * i], b[4 * i + 1], b[4 * i + 2], b[4 * i + 3]);
+              for (int i = 0; i < 16; ++i)
+                b[i] = cvt_bf16x2(__uint_as_float(v[u][2 * i + 1]), __uint_as_float(v[u][2 * i]));
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                w[j] = make_uint4(b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
+            }
+            if (lane == 0) bulk_wait_read_all();  // the box is free again
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(box + lane * 64 + 16 * (j ^ ((lane >> 1) & 3))) = w[j];
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&map_c, box, static_cast<int32_t>(t.n0 + col),
+                           static_cast<int32_t>(t.m0 + 32 * q), t.c_z);
+              bulk_commit_group();
+            }
+          }
         }
       }
     }
+    if (lane == 0) bulk_wait_all();  // every store has landed before the CTA can exit
+    __syncwarp();
     if (!ok && lane == 0) {
       *abort_flag = 1;
       latch_error(p.status, MXFP8_ERR_TIMEOUT);
@@ -942,8 +958,8 @@ uint64_t wait_limit_ns() {
 }
 
 template <int BN, int kMode, bool kPair>
-int launch(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int64_t grid,
-           cudaStream_t stream) {
+int launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const Params& p,
+           int64_t grid, cudaStream_t stream) {
   using C = Cfg<BN>;
   auto k = mxfp8_gemm_kernel<BN, kMode, kPair>;
   static bool attr_set[64] = {};  // per device
@@ -957,7 +973,7 @@ int launch(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int64_
   }
   if (grid <= 0) return MXFP8_OK;
   if (!kPair) {
-    k<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(ma, mb, p);
+    k<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(ma, mb, mc, p);
     return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
   }
   cudaLaunchConfig_t cfg = {};
@@ -972,7 +988,7 @@ int launch(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int64_
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, ma, mb, p) == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, k, ma, mb, mc, p) == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
 }
 
 // How many CTA pairs of the dense kernel fit on the device at once (cached per device).
@@ -1035,20 +1051,23 @@ bool make_sf_map(CUtensorMap* map, const void* base, int64_t row_tiles, int64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The output C [M][N] (BF16 or FP32) for TMA stores of 32-row x 64-byte boxes, 64-byte
-// swizzle.
-bool make_out_map(CUtensorMap* map, void* base, int64_t M, int64_t N, bool fp32) {
+// The output C [Z][rows][N] (BF16 or FP32; rank 2 when Z == 1 and rank == 2) for TMA
+// stores of 32-row x 64-byte boxes with the 64-byte swizzle.
+bool make_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t N, int64_t Z, bool fp32,
+                  int rank) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const uint32_t elem = fp32 ? 4 : 2;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * elem};
-  cuuint32_t box[2] = {64 / elem, 32};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-            base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(Z)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * elem,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(rows) * elem};
+  cuuint32_t box[3] = {64 / elem, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+            static_cast<cuuint32_t>(rank), base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaLaunchConfig_t cluster2_config(int64_t grid, int smem, cudaStream_t stream,
@@ -1127,7 +1146,7 @@ int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
   CUtensorMap ma, mb, msa, msb, mc;
   if (!make_map(&ma, a.A, 2, a.K, a.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
   if (!make_map(&mb, a.B, 2, a.K, a.N, 1, BK, BN / 2)) return MXFP8_ERR_CUDA;
-  if (!make_out_map(&mc, a.C, a.M, a.N, a.out_dtype == MXFP8_OUT_FP32)) return MXFP8_ERR_CUDA;
+  if (!make_out_map(&mc, a.C, a.M, a.N, 1, a.out_dtype == MXFP8_OUT_FP32, 2)) return MXFP8_ERR_CUDA;
   if (!make_sf_map(&msa, a.sA, (a.M + 127) / 128, n_kt, 1)) return MXFP8_ERR_CUDA;
   if (!make_sf_map(&msb, a.sB, (a.N + 127) / 128, n_kt, 2)) return MXFP8_ERR_CUDA;
   p.num_n_tiles = static_cast<int>((a.N + BN - 1) / BN);
@@ -1175,8 +1194,9 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   if (wide && p.num_m_tiles >= 2 && duo_enabled())
     return duo_width(a.M, a.N) == 256 ? launch_duo<256>(a, p, stream)
                                       : launch_duo<192>(a, p, stream);
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mc;
   if (!make_map(&ma, a.A, 2, a.K, a.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
+  if (!make_out_map(&mc, a.C, a.M, a.N, 1, p.out_fp32 != 0, 3)) return MXFP8_ERR_CUDA;
   // A CTA pair shares each B tile: each CTA loads half of it and multicasts it to both.
   const bool pair = wide && pairs_enabled() && p.num_m_tiles >= 2;
   if (pair) {
@@ -1185,12 +1205,12 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
     p.band = (p.band + 1) / 2;
     const int64_t mp = max_pairs<256>();
     const int64_t pairs = pair_tiles < mp ? pair_tiles : mp;
-    return launch<256, kDense, true>(ma, mb, p, 2 * pairs, stream);
+    return launch<256, kDense, true>(ma, mb, mc, p, 2 * pairs, stream);
   }
   if (!make_map(&mb, a.B, 2, a.K, a.N, 1, BK, bn)) return MXFP8_ERR_CUDA;
   const int64_t grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-  return wide ? launch<256, kDense, false>(ma, mb, p, grid, stream)
-              : launch<128, kDense, false>(ma, mb, p, grid, stream);
+  return wide ? launch<256, kDense, false>(ma, mb, mc, p, grid, stream)
+              : launch<128, kDense, false>(ma, mb, mc, p, grid, stream);
 }
 
 int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
@@ -1205,7 +1225,7 @@ int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.total_rows = a.total_rows;
   p.status = a.status;
   p.wait_ns = wait_limit_ns();
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mc;
   if (a.op == MXFP8_OP_WGRAD) {
     // A = dY^T [N][T], B = X^T [K][T], C[e] = [N][K]
     p.M = a.N;
@@ -1219,9 +1239,10 @@ int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     p.num_tiles = tiles;
     if (!make_map(&ma, a.A, 2, a.total_rows, p.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
     if (!make_map(&mb, a.B, 2, a.total_rows, p.N, 1, BK, bn)) return MXFP8_ERR_CUDA;
+    if (!make_out_map(&mc, a.C, p.M, p.N, p.E, p.out_fp32 != 0, 3)) return MXFP8_ERR_CUDA;
     const int64_t grid = tiles < num_sms() ? tiles : num_sms();
-    return wide ? launch<256, kGroupWgrad, false>(ma, mb, p, grid, stream)
-                : launch<128, kGroupWgrad, false>(ma, mb, p, grid, stream);
+    return wide ? launch<256, kGroupWgrad, false>(ma, mb, mc, p, grid, stream)
+                : launch<128, kGroupWgrad, false>(ma, mb, mc, p, grid, stream);
   }
   // fprop / dgrad: A [T][K] segmented by rows, B [E][N][K], C [T][N]
   p.M = a.total_rows;
@@ -1237,9 +1258,10 @@ int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.num_tiles = tiles;
   if (!make_map(&ma, a.A, 2, a.K, a.total_rows, 1, BK, BM)) return MXFP8_ERR_CUDA;
   if (!make_map(&mb, a.B, 3, a.K, a.N, a.num_experts, BK, bn)) return MXFP8_ERR_CUDA;
+  if (!make_out_map(&mc, a.C, a.total_rows, p.N, 1, p.out_fp32 != 0, 3)) return MXFP8_ERR_CUDA;
   const int64_t grid = tiles < num_sms() ? tiles : num_sms();
-  return wide ? launch<256, kGroupRows, false>(ma, mb, p, grid, stream)
-              : launch<128, kGroupRows, false>(ma, mb, p, grid, stream);
+  return wide ? launch<256, kGroupRows, false>(ma, mb, mc, p, grid, stream)
+              : launch<128, kGroupRows, false>(ma, mb, mc, p, grid, stream);
 }
 
 }  // namespace mxfp8
