@@ -386,7 +386,7 @@ def run_ours(args, rank, ws):
     gemm_tflops = g_units / (g_ms * 1e-3) / 1e12
     quant_gbs = q_units / (q_ms * 1e-3) / 1e9
     fp8_peak = pk["bf16_sus"] * FP8_OVER_BF16
-    traffic = recorded_traffic("mxfp8_gemm_kernel")
+    traffic = recorded_traffic("mxfp8_gemm")
     e2e = run_e2e(args, m, step, dev, stream, ws)
     graph_ms, eager_ms, host_ms = run_graph(m, step, stream, max(10, args.steps // 4))
     line = {
@@ -408,7 +408,7 @@ def run_ours(args, rank, ws):
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
                      "traffic": traffic,
-                     "kernel": "mxfp8_gemm_kernel (12 launches per step)",
+                     "kernel": "mxfp8_gemm_2sm_kernel (12 launches per step; 256x256 or 256x192 tiles)",
                      "peak_note": f"{pk['src']} bf16 sustained {pk['bf16_sus']} x "
                                   f"{FP8_OVER_BF16} (nominal FP8:BF16 ratio)",
                      "flops_per_launch": g_units / g_launches},
