@@ -184,32 +184,41 @@ class DenseStep:
 
     def run(self, stream, events=None):
         """Enqueues one step. With `events` (a list), appends (kind, units, start, end)."""
-        m = self.m
         for L in self.layers:
-            if self.dual:
-                # one read of each BF16 tensor gives both of its quantized copies
-                for src_key, rk, ck in (("x", "xr", "xc"), ("w", "wr", "wc"), ("dy", "dyr", "dyc")):
-                    src = L[src_key]
-                    ev = self._ev(events, stream, "quantize", src.numel() * DUAL_BYTES_PER_ELEM,
-                                  f"{L['name']}.{src_key} dual {src.shape[0]}x{src.shape[1]}")
-                    m.quantize_dual(src, m.SWIZZLED, row_out=L[rk][0], row_scales=L[rk][1],
-                                    col_out=L[ck][0], col_scales=L[ck][1], stream=stream)
-                    self._end(events, stream, ev)
-            else:
-                for key in ("xr", "xc", "wr", "wc", "dyr", "dyc"):
-                    q, s, src, axis = L[key]
-                    ev = self._ev(events, stream, "quantize", src.numel() * QBYTES_PER_ELEM,
-                                  f"{L['name']}.{key} {src.shape[0]}x{src.shape[1]}")
-                    m.quantize(src, axis, m.SWIZZLED, out=q, scales=s, stream=stream)
-                    self._end(events, stream, ev)
-            t, n, k = L["t"], L["n"], L["k"]
-            for op, a, b, out, mnk in ((m.FPROP, "xr", "wr", L["y"], (t, n, k)),
-                                       (m.DGRAD, "dyr", "wc", L["dx"], (t, k, n)),
-                                       (m.WGRAD, "dyc", "xc", L["dw"], (n, k, t))):
-                ev = self._ev(events, stream, "gemm", 2.0 * mnk[0] * mnk[1] * mnk[2],
-                              f"{L['name']}.{('fprop', 'dgrad', 'wgrad')[op]} {mnk[0]}x{mnk[1]}x{mnk[2]}")
-                m.gemm(L[a][0], L[a][1], L[b][0], L[b][1], op, m.OUT_BF16, out=out, stream=stream)
+            self.run_quantize(L, stream, events)
+            self.run_gemms(L, stream, events)
+
+    def run_quantize(self, L, stream, events=None):
+        """The layer's quantize launches (they read x, w and dy)."""
+        m = self.m
+        if self.dual:
+            # one read of each BF16 tensor gives both of its quantized copies
+            for src_key, rk, ck in (("x", "xr", "xc"), ("w", "wr", "wc"), ("dy", "dyr", "dyc")):
+                src = L[src_key]
+                ev = self._ev(events, stream, "quantize", src.numel() * DUAL_BYTES_PER_ELEM,
+                              f"{L['name']}.{src_key} dual {src.shape[0]}x{src.shape[1]}")
+                m.quantize_dual(src, m.SWIZZLED, row_out=L[rk][0], row_scales=L[rk][1],
+                                col_out=L[ck][0], col_scales=L[ck][1], stream=stream)
                 self._end(events, stream, ev)
+        else:
+            for key in ("xr", "xc", "wr", "wc", "dyr", "dyc"):
+                q, s, src, axis = L[key]
+                ev = self._ev(events, stream, "quantize", src.numel() * QBYTES_PER_ELEM,
+                              f"{L['name']}.{key} {src.shape[0]}x{src.shape[1]}")
+                m.quantize(src, axis, m.SWIZZLED, out=q, scales=s, stream=stream)
+                self._end(events, stream, ev)
+
+    def run_gemms(self, L, stream, events=None):
+        """The layer's three GEMMs (they write y, dx and dw)."""
+        m = self.m
+        t, n, k = L["t"], L["n"], L["k"]
+        for op, a, b, out, mnk in ((m.FPROP, "xr", "wr", L["y"], (t, n, k)),
+                                   (m.DGRAD, "dyr", "wc", L["dx"], (t, k, n)),
+                                   (m.WGRAD, "dyc", "xc", L["dw"], (n, k, t))):
+            ev = self._ev(events, stream, "gemm", 2.0 * mnk[0] * mnk[1] * mnk[2],
+                          f"{L['name']}.{('fprop', 'dgrad', 'wgrad')[op]} {mnk[0]}x{mnk[1]}x{mnk[2]}")
+            m.gemm(L[a][0], L[a][1], L[b][0], L[b][1], op, m.OUT_BF16, out=out, stream=stream)
+            self._end(events, stream, ev)
 
     @staticmethod
     def _ev(events, stream, kind, units, label=""):
@@ -426,39 +435,69 @@ def run_ours(args, rank, ws):
 
 def run_e2e(args, m, step, dev, stream, ws):
     """Same step through the public API, with the BF16 inputs copied in from pinned host
-    memory and the BF16 results copied back inside the timed region."""
+    memory and the BF16 results copied back inside the timed region. Copies run on their
+    own streams, layer by layer, so that host-to-device copies, compute and device-to-host
+    copies of different layers (and of consecutive steps) overlap, as a training loop with
+    asynchronous input and output transfers would run them. Events keep every dependency:
+    a layer's inputs are overwritten only after the previous step's quantize read them,
+    and its outputs only after the previous step's copy-out read them."""
     host_in, host_out = [], []
     for L in step.layers:
-        for key in ("x", "w", "dy"):
-            host_in.append((torch.empty_like(L[key], device="cpu").pin_memory(), L[key]))
-        for key in ("y", "dx", "dw"):
-            host_out.append((L[key], torch.empty_like(L[key], device="cpu").pin_memory()))
-    for h, d in host_in:
-        h.copy_(d)
-    h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
-    d2h = sum(h.numel() * h.element_size() for _, h in host_out)
+        host_in.append([(torch.empty_like(L[key], device="cpu").pin_memory(), L[key])
+                        for key in ("x", "w", "dy")])
+        host_out.append([(L[key], torch.empty_like(L[key], device="cpu").pin_memory())
+                         for key in ("y", "dx", "dw")])
+    for layer in host_in:
+        for h, d in layer:
+            h.copy_(d)
+    h2d = sum(h.numel() * h.element_size() for layer in host_in for h, _ in layer)
+    d2h = sum(h.numel() * h.element_size() for layer in host_out for _, h in layer)
     steps = max(3, args.steps // 4)
+    n = len(step.layers)
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()
+    in_ready, q_done = [ev() for _ in range(n)], [ev() for _ in range(n)]
+    g_done, out_done = [ev() for _ in range(n)], [ev() for _ in range(n)]
 
     def one():
-        for h, d in host_in:
-            d.copy_(h, non_blocking=True)
-        step.run(stream)
-        for d, h in host_out:
-            h.copy_(d, non_blocking=True)
+        for i in range(n):
+            s_in.wait_event(q_done[i])  # the previous step has read this layer's inputs
+            with torch.cuda.stream(s_in):
+                for h, d in host_in[i]:
+                    d.copy_(h, non_blocking=True)
+            in_ready[i].record(s_in)
+        for i, L in enumerate(step.layers):
+            stream.wait_event(in_ready[i])
+            step.run_quantize(L, stream)
+            q_done[i].record(stream)
+            stream.wait_event(out_done[i])  # the previous step's outputs have left
+            step.run_gemms(L, stream)
+            g_done[i].record(stream)
+            s_out.wait_event(g_done[i])
+            with torch.cuda.stream(s_out):
+                for d, h in host_out[i]:
+                    h.copy_(d, non_blocking=True)
+            out_done[i].record(s_out)
 
     for _ in range(2):
         one()
+    torch.cuda.synchronize()
     barrier(ws)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(stream)
+    s_in.wait_stream(stream)
+    s_out.wait_stream(stream)
     for _ in range(steps):
         one()
+    stream.wait_stream(s_in)
+    stream.wait_stream(s_out)
     e.record(stream)
+    torch.cuda.synchronize()
     barrier(ws)
     ms = max_over_ranks(s.elapsed_time(e), ws) / steps
     return {"value": ws * step.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "steps": steps}
+            "steps": steps, "overlap": "per-layer copy-in, compute and copy-out on three streams"}
 
 
 def run_graph(m, step, stream, steps):

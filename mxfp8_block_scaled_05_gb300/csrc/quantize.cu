@@ -112,7 +112,8 @@ __device__ __forceinline__ uint32_t scale_byte(uint32_t amax_bits, int rule) {
   return e > 0 ? static_cast<uint32_t>(e) : 0u;
 }
 
-// 2^-e for scale byte s = e + 127, as an FP32 (always a normal number for s <= 246).
+// 2^-e for scale byte s = e + 127, as an FP32 (a normal number for s <= 253; the 0xFF of a
+// NaN/Inf block gives -Inf, whose products are discarded).
 __device__ __forceinline__ float inv_scale(uint32_t s) {
   return __uint_as_float((254u - s) << 23);
 }
@@ -121,15 +122,18 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Two BF16 pairs (4 elements, memory order lo(w0), hi(w0), lo(w1), hi(w1)) -> 4 bytes.
-__device__ __forceinline__ uint32_t e4m3x4(uint32_t w0, uint32_t w1, float mul, bool nan_block) {
-  if (nan_block) {
-    const uint32_t s0 = (w0 >> 8) & 0x80u, s1 = (w0 >> 24) & 0x80u;
-    const uint32_t s2 = (w1 >> 8) & 0x80u, s3 = (w1 >> 24) & 0x80u;
-    return (0x7Fu | s0) | ((0x7Fu | s1) << 8) | ((0x7Fu | s2) << 16) | ((0x7Fu | s3) << 24);
-  }
+__device__ __forceinline__ uint32_t e4m3x4(uint32_t w0, uint32_t w1, float mul) {
   const uint32_t p0 = cvt_e4m3x2(bf16hi(w0) * mul, bf16lo(w0) * mul);
   const uint32_t p1 = cvt_e4m3x2(bf16hi(w1) * mul, bf16lo(w1) * mul);
   return p0 | (p1 << 16);
+}
+
+// The same 4 elements of a NaN/Inf block: 0x7F with each element's own sign. Blocks like
+// this take a separate branch after the normal conversion, which stays free of selects.
+__device__ __forceinline__ uint32_t nan4(uint32_t w0, uint32_t w1) {
+  const uint32_t s0 = (w0 >> 8) & 0x80u, s1 = (w0 >> 24) & 0x80u;
+  const uint32_t s2 = (w1 >> 8) & 0x80u, s3 = (w1 >> 24) & 0x80u;
+  return (0x7Fu | s0) | ((0x7Fu | s1) << 8) | ((0x7Fu | s2) << 16) | ((0x7Fu | s3) << 24);
 }
 
 // One CTA = one 128 x 128 BF16 tile (128 token rows x 128 columns). kRow: write the
@@ -236,11 +240,16 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
       const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
       const bool valid = col_ok && r < rows_valid;
       const uint32_t s = scale_byte(m, rule);
-      const float mul = inv_scale(s == 0xFFu ? 127u : s);
+      const float mul = inv_scale(s);  // (a NaN/Inf block's codes are replaced below)
       if (valid) {
         uint2 o;
-        o.x = e4m3x4(xv.x, xv.y, mul, s == 0xFFu);
-        o.y = e4m3x4(xv.z, xv.w, mul, s == 0xFFu);
+        if (__builtin_expect(s != 0xFFu, 1)) {
+          o.x = e4m3x4(xv.x, xv.y, mul);
+          o.y = e4m3x4(xv.z, xv.w, mul);
+        } else {
+          o.x = nan4(xv.x, xv.y);
+          o.y = nan4(xv.z, xv.w);
+        }
         *reinterpret_cast<uint2*>(ro.codes + (row0 + r) * cols + col0 + 8 * v) = o;
       }
       if ((v & 3) == 0) {
@@ -270,18 +279,27 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
     const uint32_t s0 = scale_byte(m01 & 0xFFFFu, rule), s1 = scale_byte(m01 >> 16, rule);
     uint4 stage_o0[2], stage_o1[2];
     if (valid) {
-      const float mul0 = inv_scale(s0 == 0xFFu ? 127u : s0);
-      const float mul1 = inv_scale(s1 == 0xFFu ? 127u : s1);
+      const float mul0 = inv_scale(s0), mul1 = inv_scale(s1);
       uint32_t o0[8], o1[8];
+      if (__builtin_expect(s0 != 0xFFu && s1 != 0xFFu, 1)) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint32_t a0 = colw[(4 * q) * kRowWords], a1 = colw[(4 * q + 1) * kRowWords];
-        const uint32_t a2 = colw[(4 * q + 2) * kRowWords], a3 = colw[(4 * q + 3) * kRowWords];
-        // column c: low halves; column c+1: high halves
-        o0[q] = e4m3x4(__byte_perm(a0, a1, 0x5410), __byte_perm(a2, a3, 0x5410), mul0,
-                       s0 == 0xFFu);
-        o1[q] = e4m3x4(__byte_perm(a0, a1, 0x7632), __byte_perm(a2, a3, 0x7632), mul1,
-                       s1 == 0xFFu);
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t a0 = colw[(4 * q) * kRowWords], a1 = colw[(4 * q + 1) * kRowWords];
+          const uint32_t a2 = colw[(4 * q + 2) * kRowWords], a3 = colw[(4 * q + 3) * kRowWords];
+          // column c: low halves; column c+1: high halves
+          o0[q] = e4m3x4(__byte_perm(a0, a1, 0x5410), __byte_perm(a2, a3, 0x5410), mul0);
+          o1[q] = e4m3x4(__byte_perm(a0, a1, 0x7632), __byte_perm(a2, a3, 0x7632), mul1);
+        }
+      } else {  // a NaN/Inf block in either column (rare)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t a0 = colw[(4 * q) * kRowWords], a1 = colw[(4 * q + 1) * kRowWords];
+          const uint32_t a2 = colw[(4 * q + 2) * kRowWords], a3 = colw[(4 * q + 3) * kRowWords];
+          const uint32_t c0a = __byte_perm(a0, a1, 0x5410), c0b = __byte_perm(a2, a3, 0x5410);
+          const uint32_t c1a = __byte_perm(a0, a1, 0x7632), c1b = __byte_perm(a2, a3, 0x7632);
+          o0[q] = s0 == 0xFFu ? nan4(c0a, c0b) : e4m3x4(c0a, c0b, mul0);
+          o1[q] = s1 == 0xFFu ? nan4(c1a, c1b) : e4m3x4(c1a, c1b, mul1);
+        }
       }
       stage_o0[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
       stage_o0[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
