@@ -4,7 +4,9 @@ and "Where the time goes": per linear layer, the operands X, W and dY are quanti
 row-wise and column-wise, then the fprop, dgrad and wgrad block-scaled GEMMs run).
 
 Per step and layer (qkv 4096->6144, o 4096->4096, gate_up 4096->24576, down 12288->4096):
-6 quantize launches + 3 GEMM launches; 36 launches per step. Inputs are synthetic
+two dual quantize launches (X and W together, as the forward pass has them; dY alone, as
+the backward pass has it), each giving both copies from one read, and 3 GEMM launches;
+20 launches per step (--quant separate: 6 single-axis quantizes per layer). Inputs are synthetic
 (seeded, BF16) and live in HBM before the timed region; the step's working set (453 MB
 of BF16 inputs) is larger than L2, so no flush is needed between steps.
 
@@ -180,7 +182,7 @@ class DenseStep:
             self.layers.append(L)
         self.flops = sum(layer_flops(L["t"], L["n"], L["k"]) for L in self.layers)
         self.qelems = sum(layer_quant_elems(L["t"], L["n"], L["k"]) for L in self.layers)
-        self.launches = (6 if dual else 9) * len(self.layers)
+        self.launches = (5 if dual else 9) * len(self.layers)
 
     def run(self, stream, events=None):
         """Enqueues one step. With `events` (a list), appends (kind, units, start, end)."""
@@ -192,14 +194,24 @@ class DenseStep:
         """The layer's quantize launches (they read x, w and dy)."""
         m = self.m
         if self.dual:
-            # one read of each BF16 tensor gives both of its quantized copies
-            for src_key, rk, ck in (("x", "xr", "xc"), ("w", "wr", "wc"), ("dy", "dyr", "dyc")):
-                src = L[src_key]
-                ev = self._ev(events, stream, "quantize", src.numel() * DUAL_BYTES_PER_ELEM,
-                              f"{L['name']}.{src_key} dual {src.shape[0]}x{src.shape[1]}")
-                m.quantize_dual(src, m.SWIZZLED, row_out=L[rk][0], row_scales=L[rk][1],
-                                col_out=L[ck][0], col_scales=L[ck][1], stream=stream)
-                self._end(events, stream, ev)
+            # One read of each BF16 tensor gives both of its quantized copies. The forward
+            # operands (x and w) go in one launch; dy, which a training step only has in
+            # the backward pass, in another.
+            x, w = L["x"], L["w"]
+            ev = self._ev(events, stream, "quantize",
+                          (x.numel() + w.numel()) * DUAL_BYTES_PER_ELEM,
+                          f"{L['name']}.x+w dual {x.shape[0]}x{x.shape[1]} + {w.shape[0]}x{w.shape[1]}")
+            m.quantize_dual_multi([x, w], m.SWIZZLED,
+                                  outs=[(L["xr"][0], L["xr"][1], L["xc"][0], L["xc"][1]),
+                                        (L["wr"][0], L["wr"][1], L["wc"][0], L["wc"][1])],
+                                  stream=stream)
+            self._end(events, stream, ev)
+            dy = L["dy"]
+            ev = self._ev(events, stream, "quantize", dy.numel() * DUAL_BYTES_PER_ELEM,
+                          f"{L['name']}.dy dual {dy.shape[0]}x{dy.shape[1]}")
+            m.quantize_dual(dy, m.SWIZZLED, row_out=L["dyr"][0], row_scales=L["dyr"][1],
+                            col_out=L["dyc"][0], col_scales=L["dyc"][1], stream=stream)
+            self._end(events, stream, ev)
         else:
             for key in ("xr", "xc", "wr", "wc", "dyr", "dyc"):
                 q, s, src, axis = L[key]
@@ -408,7 +420,8 @@ def run_ours(args, rank, ws):
         "gpu_launches": step.launches * args.steps,
         "quantize": {"GB/s": quant_gbs, "frac_of_hbm": quant_gbs / pk["hbm"],
                      "ms_per_step": q_ms / args.steps,
-                     "mode": "dual (one read, both copies)" if step.dual else "separate",
+                     "mode": ("dual (one read, both copies; X and W of a layer in one launch)"
+                              if step.dual else "separate"),
                      "bytes_per_elem": DUAL_BYTES_PER_ELEM if step.dual else QBYTES_PER_ELEM,
                      "bytes_per_step": q_units / args.steps,
                      "peak_GB/s": pk["hbm"], "peak_src": pk["src"]},

@@ -146,6 +146,37 @@ int mxfp8_quantize_dual(const void* src_dev, int64_t rows, int64_t cols, void* r
                         int scale_layout, void* stream);
 
 /*
+ * One job of mxfp8_quantize_dual_multi: the arguments of one mxfp8_quantize_dual call.
+ * All pointers are device pointers owned by the caller.
+ */
+typedef struct mxfp8_dual_job {
+  const void* src;     /* BF16 [rows][cols] */
+  int64_t rows, cols;  /* rows % 32 == 0, cols % 32 == 0 */
+  void* row_out;       /* E4M3 [rows][cols] */
+  void* row_scales;    /* mxfp8_scale_bytes(rows, cols, MXFP8_AXIS_ROW, layout) bytes */
+  void* col_out;       /* E4M3 [cols][rows] */
+  void* col_scales;    /* mxfp8_scale_bytes(rows, cols, MXFP8_AXIS_COL, layout) bytes */
+} mxfp8_dual_job;
+
+#define MXFP8_MAX_DUAL_JOBS 8
+
+/*
+ * Several mxfp8_quantize_dual calls in one launch. The tensors' 128 x 128 tiles form one
+ * grid, so a small tensor's partly filled last wave of CTAs is shared with the others
+ * instead of running alone. Typical use: a linear layer's activations and weight,
+ * quantized together before the forward GEMM. "The pipeline" (learner paragraph) gives
+ * the quantized operands; the batching is this library's.
+ *   jobs        host array of num_jobs descriptors (1 <= num_jobs <= MXFP8_MAX_DUAL_JOBS),
+ *               read during the call only; every job is checked as mxfp8_quantize_dual
+ *               checks its arguments, and nothing is launched if one fails. Jobs with
+ *               rows == 0 or cols == 0 are skipped.
+ * Bytes are identical to one mxfp8_quantize_dual call per job. Outputs of different jobs
+ * must not overlap.
+ */
+int mxfp8_quantize_dual_multi(const mxfp8_dual_job* jobs, int num_jobs, int scale_layout,
+                              void* stream);
+
+/*
  * `batch` independent matrices [batch][rows][cols] quantized as by mxfp8_quantize, each
  * with its own scale block of mxfp8_scale_bytes(rows, cols, axis, layout) bytes; the
  * scale blocks are concatenated in batch order. Used for per-expert MoE weights.

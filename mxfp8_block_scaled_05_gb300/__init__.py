@@ -36,6 +36,7 @@ SIGNATURES = {
     "mxfp8_quantize": (_I, [_P, _I64, _I64, _I, _P, _P, _I, _P]),
     "mxfp8_quantize_rule": (_I, [_P, _I64, _I64, _I, _P, _P, _I, _I, _P]),
     "mxfp8_quantize_dual": (_I, [_P, _I64, _I64, _P, _P, _P, _P, _I, _P]),
+    "mxfp8_quantize_dual_multi": (_I, [_P, _I, _I, _P]),
     "mxfp8_quantize_batched": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _I, _P]),
     "mxfp8_quantize_grouped_dual": (_I, [_P, _I64, _I64, _P, _I, _P, _P, _P, _P, _P]),
     "mxfp8_quantize_grouped": (_I, [_P, _I64, _I64, _I, _P, _I, _P, _P, _P]),
@@ -160,6 +161,42 @@ def quantize_dual(src: torch.Tensor, layout: int = SWIZZLED, row_out=None, row_s
                                      _ptr(col_out), _ptr(col_scales), layout, _stream(stream)),
            "mxfp8_quantize_dual")
     return row_out, row_scales, col_out, col_scales
+
+
+class DualJob(ctypes.Structure):
+    """mxfp8_dual_job (include/mxfp8.h)."""
+    _fields_ = [("src", _P), ("rows", _I64), ("cols", _I64), ("row_out", _P),
+                ("row_scales", _P), ("col_out", _P), ("col_scales", _P)]
+
+
+MAX_DUAL_JOBS = 8
+
+
+def quantize_dual_multi(srcs, layout: int = SWIZZLED, outs=None, stream=None):
+    """quantize_dual for several BF16 tensors in one launch. `outs`, if given, holds one
+    (row_codes, row_scales, col_codes, col_scales) tuple per source. Returns the list of
+    such tuples."""
+    if not 1 <= len(srcs) <= MAX_DUAL_JOBS:
+        raise ValueError(f"1 to {MAX_DUAL_JOBS} tensors per call")
+    result = []
+    jobs = (DualJob * len(srcs))()
+    for i, src in enumerate(srcs):
+        _require(src, torch.bfloat16, "src")
+        rows, cols = src.shape
+        dev = src.device
+        if outs is not None:
+            ro, rs, co, cs = outs[i]
+        else:
+            ro = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+            co = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+            rs = _alloc_scales(rows, cols, ROW, layout, dev)
+            cs = _alloc_scales(rows, cols, COL, layout, dev)
+        jobs[i] = DualJob(src.data_ptr(), rows, cols, ro.data_ptr(), rs.data_ptr(),
+                          co.data_ptr(), cs.data_ptr())
+        result.append((ro, rs, co, cs))
+    _check(lib().mxfp8_quantize_dual_multi(ctypes.cast(jobs, _P), len(srcs), layout,
+                                           _stream(stream)), "mxfp8_quantize_dual_multi")
+    return result
 
 
 def quantize_grouped_dual(src: torch.Tensor, offsets: torch.Tensor, row_out=None,

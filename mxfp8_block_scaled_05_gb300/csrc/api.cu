@@ -207,6 +207,51 @@ int mxfp8_quantize_dual(const void* src_dev, int64_t rows, int64_t cols, void* r
                          col_out_dev, col_scales_dev, scale_layout, nullptr, 0, stream);
 }
 
+int mxfp8_quantize_dual_multi(const mxfp8_dual_job* jobs, int num_jobs, int scale_layout,
+                              void* stream) {
+  if (!jobs || num_jobs < 1 || num_jobs > MXFP8_MAX_DUAL_JOBS) return MXFP8_ERR_INVALID_ARG;
+  if (scale_layout != MXFP8_SCALES_LINEAR && scale_layout != MXFP8_SCALES_SWIZZLED)
+    return MXFP8_ERR_INVALID_ARG;
+  static_assert(MXFP8_MAX_DUAL_JOBS <= kMaxQuantizeJobs, "job table too small");
+  QuantizeJobs q{};
+  q.n = num_jobs;
+  q.layout = scale_layout;
+  int64_t tiles = 0;
+  for (int i = 0; i < num_jobs; ++i) {
+    const mxfp8_dual_job& j = jobs[i];
+    // the same checks as mxfp8_quantize_dual
+    if (j.rows < 0 || j.cols < 0) return MXFP8_ERR_INVALID_ARG;
+    if (j.rows % 32 || j.cols % 32) return MXFP8_ERR_ALIGNMENT;
+    if (j.rows == 0 || j.cols == 0) continue;
+    if (!j.src || !j.row_out || !j.row_scales || !j.col_out || !j.col_scales)
+      return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(j.src) || !aligned16(j.row_out) || !aligned16(j.col_out))
+      return MXFP8_ERR_ALIGNMENT;
+    if (scale_layout == MXFP8_SCALES_SWIZZLED &&
+        (!aligned16(j.row_scales) || !aligned16(j.col_scales)))
+      return MXFP8_ERR_ALIGNMENT;
+    if (cdiv(j.rows, 128) > kMaxTokenTiles || cdiv(j.cols, 128) > 0x7FFFFFFF)
+      return MXFP8_ERR_INVALID_ARG;
+    tiles += cdiv(j.rows, 128) * cdiv(j.cols, 128);
+    q.src[i] = j.src;
+    q.rows[i] = j.rows;
+    q.cols[i] = j.cols;
+    q.out[i] = j.row_out;
+    q.scales[i] = j.row_scales;
+    q.out_col[i] = j.col_out;
+    q.scales_col[i] = j.col_scales;
+  }
+  if (tiles > 0x7FFFFFFF) return MXFP8_ERR_INVALID_ARG;
+  if (tiles == 0) return MXFP8_OK;
+  DeviceState* d = nullptr;
+  const int st = device_state(&d);
+  if (st != MXFP8_OK) return st;
+  q.status = d->status;
+  return launch_quantize_jobs(q, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MXFP8_OK
+             : MXFP8_ERR_CUDA;
+}
+
 int mxfp8_quantize_batched(const void* src_dev, int64_t batch, int64_t rows, int64_t cols,
                            int axis, void* out_dev, void* scales_dev, int scale_layout,
                            void* stream) {

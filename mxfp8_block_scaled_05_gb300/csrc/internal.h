@@ -28,6 +28,22 @@ struct QuantizeArgs {
 
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream);
 
+// Several dual (row-wise + column-wise) quantizations in one launch.
+constexpr int kMaxQuantizeJobs = 8;
+struct QuantizeJobs {
+  int n;
+  int layout;
+  const void* src[kMaxQuantizeJobs];
+  int64_t rows[kMaxQuantizeJobs], cols[kMaxQuantizeJobs];
+  void* out[kMaxQuantizeJobs];
+  void* scales[kMaxQuantizeJobs];
+  void* out_col[kMaxQuantizeJobs];
+  void* scales_col[kMaxQuantizeJobs];
+  int* status;
+};
+
+cudaError_t launch_quantize_jobs(const QuantizeJobs& j, cudaStream_t stream);
+
 struct GemmArgs {
   const void* A;
   const void* sA;

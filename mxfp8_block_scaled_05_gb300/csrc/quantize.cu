@@ -145,11 +145,23 @@ struct QOut {
   int64_t scale_item_bytes;  // bytes of one batch item's scale block
 };
 
-template <bool kRow, bool kCol, bool kSwizzled, bool kGrouped>
+// Jobs of a multi-tensor launch: job j owns the grid's tiles [tile_base[j], tile_base[j+1]).
+struct QJobs {
+  int n;
+  const uint16_t* src[kMaxQuantizeJobs];
+  int64_t rows[kMaxQuantizeJobs], cols[kMaxQuantizeJobs];
+  uint8_t* out[kMaxQuantizeJobs];
+  uint8_t* scales[kMaxQuantizeJobs];
+  uint8_t* out_col[kMaxQuantizeJobs];
+  uint8_t* scales_col[kMaxQuantizeJobs];
+  int64_t tile_base[kMaxQuantizeJobs + 1];
+};
+
+template <bool kRow, bool kCol, bool kSwizzled, bool kGrouped, bool kMulti>
 __global__ void __launch_bounds__(kThreads, kCol ? 6 : 1)
 quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t cols, QOut ro,
                      QOut co, const int32_t* __restrict__ offsets, int E, int rule,
-                     int* status) {
+                     int* status, const QJobs jobs) {
   __shared__ __align__(16) uint16_t tile[kCol ? kTile : 1][kCol ? kTile : 8];
   __shared__ __align__(16) uint8_t stile_r[512];
   __shared__ __align__(16) uint8_t stile_c[512];
@@ -158,18 +170,33 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
   if (kGrouped) load_segments(*seg, offsets, E, rows, status);
 
   // ---- which tile, and where its two 512-byte scale tiles go
+  int64_t bx = blockIdx.x, by = blockIdx.y, item = blockIdx.z;
+  if constexpr (kMulti) {  // a 1-D grid over every job's tiles, job by job
+    const int64_t g = blockIdx.x;
+    int j = 0;
+    while (j + 1 < jobs.n && g >= jobs.tile_base[j + 1]) ++j;
+    src = jobs.src[j];
+    rows = jobs.rows[j];
+    cols = jobs.cols[j];
+    ro = QOut{jobs.out[j], jobs.scales[j], 0};
+    co = QOut{jobs.out_col[j], jobs.scales_col[j], 0};
+    const int64_t local = g - jobs.tile_base[j], n_ct = (cols + kTile - 1) / kTile;
+    by = local / n_ct;
+    bx = local % n_ct;
+    item = 0;
+  }
   const int64_t n_col_tiles = (cols + kTile - 1) / kTile;  // = scale tiles per row-wise tile row
   int64_t row0, tile_row;       // first token row; global token-tile index
   int rows_valid;
   int64_t col_scale_tile;       // column-wise scale tile index
   if (!kGrouped) {
-    tile_row = blockIdx.y;
+    tile_row = by;
     row0 = tile_row * kTile;
     const int64_t left = rows - row0;
     rows_valid = static_cast<int>(left < kTile ? left : kTile);
-    col_scale_tile = static_cast<int64_t>(blockIdx.x) * ((rows + kTile - 1) / kTile) + tile_row;
+    col_scale_tile = bx * ((rows + kTile - 1) / kTile) + tile_row;
   } else {
-    const int t = blockIdx.y;
+    const int t = static_cast<int>(by);
     if (!seg->ok || t >= seg->tile_base[E]) return;
     const int e = find_expert(*seg, E, t);
     const int64_t i = t - seg->tile_base[e];
@@ -179,11 +206,10 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
     rows_valid = static_cast<int>(left < kTile ? left : kTile);
     const int64_t cnt = seg->off[e + 1] - seg->off[e];
     col_scale_tile = n_col_tiles * seg->tile_base[e] +
-                     static_cast<int64_t>(blockIdx.x) * ((cnt + kTile - 1) / kTile) + i;
+                     bx * ((cnt + kTile - 1) / kTile) + i;
   }
-  const int64_t row_scale_tile = tile_row * n_col_tiles + blockIdx.x;
+  const int64_t row_scale_tile = tile_row * n_col_tiles + bx;
 
-  const int64_t item = blockIdx.z;
   src += item * rows * cols;
   if (kRow) {
     ro.codes += item * rows * cols;
@@ -197,7 +223,7 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
   const int t = threadIdx.x;
   const int v = t & 15;             // 16-byte vector (8 elements) within the tile row
   const int rsub = t >> 4;          // rows rsub + 16 j
-  const int64_t col0 = static_cast<int64_t>(blockIdx.x) * kTile;
+  const int64_t col0 = bx * kTile;
   const int64_t cols_left = cols - col0;
   const int cols_valid = static_cast<int>(cols_left < kTile ? cols_left : kTile);
   const bool col_ok = 8 * v < cols_valid;   // cols % 8 == 0 (% 32 == 0 with kRow)
@@ -357,7 +383,7 @@ cudaError_t launch_tiles(const QuantizeArgs& a, cudaStream_t stream) {
   if (row_tiles > 65535 || col_tiles > 0x7FFFFFFF || a.batch > 65535)
     return cudaErrorInvalidValue;
   const size_t dyn = kGr ? sizeof(Segments) : 0;
-  auto k = quantize_tile_kernel<kRow, kCol, kSw, kGr>;
+  auto k = quantize_tile_kernel<kRow, kCol, kSw, kGr, false>;
   if (dyn) {
     const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(dyn));
@@ -370,7 +396,7 @@ cudaError_t launch_tiles(const QuantizeArgs& a, cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>(col_tiles), static_cast<unsigned>(row_tiles),
             static_cast<unsigned>(a.batch));
   k<<<grid, kThreads, dyn, stream>>>(static_cast<const uint16_t*>(a.src), a.rows, a.cols, ro, co,
-                                      a.offsets, a.num_experts, a.rule, a.status);
+                                      a.offsets, a.num_experts, a.rule, a.status, QJobs{});
   return cudaGetLastError();
 }
 
@@ -384,6 +410,38 @@ cudaError_t launch_axes(const QuantizeArgs& a, cudaStream_t stream) {
 }  // namespace
 
 int64_t scale_bytes_host(int64_t rows, int64_t cols, int axis, int layout);
+
+cudaError_t launch_quantize_jobs(const QuantizeJobs& in, cudaStream_t stream) {
+  QJobs j{};
+  j.n = 0;
+  int64_t tiles = 0;
+  for (int i = 0; i < in.n; ++i) {
+    if (in.rows[i] == 0 || in.cols[i] == 0) continue;
+    const int n = j.n++;
+    j.src[n] = static_cast<const uint16_t*>(in.src[i]);
+    j.rows[n] = in.rows[i];
+    j.cols[n] = in.cols[i];
+    j.out[n] = static_cast<uint8_t*>(in.out[i]);
+    j.scales[n] = static_cast<uint8_t*>(in.scales[i]);
+    j.out_col[n] = static_cast<uint8_t*>(in.out_col[i]);
+    j.scales_col[n] = static_cast<uint8_t*>(in.scales_col[i]);
+    j.tile_base[n] = tiles;
+    tiles += ((in.rows[i] + kTile - 1) / kTile) * ((in.cols[i] + kTile - 1) / kTile);
+  }
+  j.tile_base[j.n] = tiles;
+  if (tiles == 0) return cudaSuccess;
+  if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const QOut none{nullptr, nullptr, 0};
+  if (in.layout == MXFP8_SCALES_SWIZZLED)
+    quantize_tile_kernel<true, true, true, false, true><<<static_cast<unsigned>(tiles), kThreads, 0,
+                                                          stream>>>(
+        nullptr, 0, 0, none, none, nullptr, 0, MXFP8_RULE_FLOOR, in.status, j);
+  else
+    quantize_tile_kernel<true, true, false, false, true><<<static_cast<unsigned>(tiles), kThreads, 0,
+                                                           stream>>>(
+        nullptr, 0, 0, none, none, nullptr, 0, MXFP8_RULE_FLOOR, in.status, j);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream) {
   if (a.rows == 0 || a.cols == 0 || a.batch == 0) return cudaSuccess;

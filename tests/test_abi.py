@@ -99,6 +99,29 @@ def test_argument_errors_need_no_device(lib):
     assert qg(p, 48, 64, m.ROW, p, 4, p, p, None) == m.ERR_ALIGNMENT
 
 
+def test_multi_job_argument_errors_need_no_device(lib):
+    qm = lib.mxfp8_quantize_dual_multi
+    P = 0x10000
+
+    def jobs(*specs):
+        arr = (m.DualJob * len(specs))()
+        for i, (rows, cols, ptr) in enumerate(specs):
+            arr[i] = m.DualJob(ptr, rows, cols, P, P, P, P)
+        return ctypes.cast(arr, ctypes.c_void_p)
+
+    one = jobs((64, 64, P))
+    assert qm(None, 1, m.SWIZZLED, None) == m.ERR_INVALID_ARG
+    assert qm(one, 0, m.SWIZZLED, None) == m.ERR_INVALID_ARG
+    assert qm(jobs(*[(64, 64, P)] * 9), 9, m.SWIZZLED, None) == m.ERR_INVALID_ARG
+    assert qm(one, 1, 5, None) == m.ERR_INVALID_ARG
+    assert qm(jobs((64, 64, P), (48, 64, P)), 2, m.SWIZZLED, None) == m.ERR_ALIGNMENT  # rows % 32
+    assert qm(jobs((64, 64, P), (64, 40, P)), 2, m.SWIZZLED, None) == m.ERR_ALIGNMENT  # cols % 32
+    assert qm(jobs((64, 64, P + 1)), 1, m.SWIZZLED, None) == m.ERR_ALIGNMENT
+    assert qm(jobs((64, 64, 0)), 1, m.SWIZZLED, None) == m.ERR_INVALID_ARG
+    assert qm(jobs((-32, 64, P)), 1, m.SWIZZLED, None) == m.ERR_INVALID_ARG
+    assert qm(jobs((0, 64, 0), (64, 0, 0)), 2, m.SWIZZLED, None) == m.OK  # all empty: no-op
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU failure path")
 def test_valid_call_without_a_gpu_fails_cleanly(lib):
     p = ctypes.c_void_p(0x10000)

@@ -236,6 +236,32 @@ def test_dual_equals_both_axes(m, shape, layout):
     np.testing.assert_array_equal(u8(cs).reshape(-1), _expect_scales(ocs, layout))
 
 
+@pytest.mark.parametrize("layout", [O.LINEAR, O.SWIZZLED])
+def test_multi_job_launch_equals_separate_calls(m, layout):
+    """Several tensors in one launch: the oracle's bytes for a small job, and byte equality
+    with one quantize_dual per job for ragged shapes, a large one and an empty one."""
+    g = np.random.default_rng(23 + layout)
+    shapes = [(160, 96), (4096, 4096), (288, 4128), (0, 64), (6144, 4096), (32, 32)]
+    xs = [_rand_bf16(g, sh).to(DEV) if sh[0] else torch.empty(sh, dtype=torch.bfloat16, device=DEV)
+          for sh in shapes]
+    got = m.quantize_dual_multi(xs, layout)
+    assert m.device_status() == m.OK
+    for x, (rq, rs, cq, cs) in zip(xs, got):
+        if x.numel() == 0:
+            continue
+        want = m.quantize_dual(x, layout)
+        for a, b in zip((rq, rs, cq, cs), want):
+            assert torch.equal(a, b)
+    x0 = xs[0].cpu()
+    orq, ors = O.quantize(bf16_bits(x0), O.ROW)
+    ocq, ocs = O.quantize(bf16_bits(x0), O.COL)
+    rq, rs, cq, cs = got[0]
+    np.testing.assert_array_equal(u8(rq), orq)
+    np.testing.assert_array_equal(u8(rs).reshape(-1), _expect_scales(ors, layout))
+    np.testing.assert_array_equal(u8(cq), ocq)
+    np.testing.assert_array_equal(u8(cs).reshape(-1), _expect_scales(ocs, layout))
+
+
 def test_grouped_dual_equals_grouped(m):
     counts = [64, 0, 160, 32, 0, 256, 96, 0]
     off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
