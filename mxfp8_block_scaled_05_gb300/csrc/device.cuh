@@ -293,6 +293,19 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                ::"r"(cluster_addr) : "memory");
 }
 
+// Relaxed arrives, for hand-backs that order no memory: the epilogue returns TMEM once
+// tcgen05.wait::ld has completed its reads, so nothing it wrote needs to be made visible
+// first (a release arrive would also wait on the warp's outstanding global stores).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];"
+               ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
 // Tiled loads into this CTA's shared memory whose transaction bytes complete on an
 // mbarrier that may live in the peer CTA (`bar` is a shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_2sm(void* smem_dst, const CUtensorMap* map,

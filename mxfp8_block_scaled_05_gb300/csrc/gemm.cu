@@ -502,7 +502,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(acc_empty);
+        if (lane == 0) mbar_arrive_relaxed(acc_empty);
         ++acc_it;
       } else {
 #pragma unroll
@@ -844,7 +844,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8 * buf);
+      if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty0 + 8 * buf);
       ++acc_it;
       // Stores leave through shared memory: each 64-byte column group of the warp's 32 rows
       // is written into the warp's staging box (16-byte chunks XOR-swizzled as the tensor
