@@ -590,10 +590,22 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 // either on a 128-row scale tile or 64 rows into one. Both scale tiles are always copied
 // to the slot's 4-aligned columns; in the second case the MMA's B-scale address is two
 // columns further on, where the scales of the tile's B rows 0-31 are.
-template <int BN>
+constexpr int kMaxDuoExperts = 256;  // grouped GEMMs on the 2SM kernel (segment table size)
+
+// Expert segments of a grouped 2SM GEMM, rebuilt by every CTA from the offsets.
+struct DuoSeg {
+  int32_t off[kMaxDuoExperts + 1];
+  int32_t tile_base[kMaxDuoExperts + 1];  // prefix sums of ceil(count / 128)
+  int32_t pair_base[kMaxDuoExperts + 1];  // prefix sums of ceil(ceil(count / 128) / 2)
+  int16_t order[kMaxDuoExperts];          // experts by decreasing count (ties: lower index)
+  int ok;
+};
+
+template <int BN, int kMode = kDense>
 struct Duo {
+  static constexpr bool kGrouped = kMode != kDense;
   static constexpr int kAcc = BN == 256 ? 1 : 2;       // accumulator buffers
-  static constexpr int kStages = BN == 256 ? 6 : 7;
+  static constexpr int kStages = BN == 256 ? 6 : (kGrouped ? 6 : 7);
   static constexpr int kABytes = BM * BK;              // own 128 A rows
   static constexpr int kBBytes = (BN / 2) * BK;        // own half of the B tile
   static constexpr int kSfaBytes = 512;
@@ -609,7 +621,9 @@ struct Duo {
   // epilogue staging: one 32-row x 64-byte box (2 KB) per epilogue warp, 1024-aligned
   static constexpr int kStageBoxBytes = 32 * 64;
   static constexpr int kOffOut = (kOffMisc + 64 + 1023) / 1024 * 1024;
-  static constexpr int kSmemBytes = kOffOut + kEpiWarps * kStageBoxBytes + 1024;
+  static constexpr int kOffSeg = kOffOut + kEpiWarps * kStageBoxBytes;
+  static constexpr int kSmemBytes =
+      kOffSeg + (kGrouped ? static_cast<int>(sizeof(DuoSeg)) : 0) + 1024;
   static constexpr int kSfaCol = kAcc * BN;            // TMEM: accumulators, then scales
   static constexpr int kSfbSlot = 8;                   // columns per B scale slot
   static constexpr int kSfbCol = kSfaCol + 4 * kStages;
@@ -621,13 +635,19 @@ struct Duo {
 };
 
 struct DuoTile {
-  int64_t m0;        // this CTA's first output row
-  int64_t n0;        // the pair tile's first output column
-  int64_t mt;        // this CTA's 128-row tile index (its A rows and their scales)
-  int64_t sfb_tile;  // first 128-row scale tile of B the pair tile touches
-  int sfb_shift;     // 0, or 2 when the tile starts 64 rows into that scale tile
-  int rows_valid, cols_valid;
-  bool live;
+  int64_t m0 = 0;        // this CTA's first output row (within its problem)
+  int64_t n0 = 0;        // the pair tile's first output column
+  int64_t mt = 0;        // this CTA's 128-row tile index (its A rows and their scales)
+  int64_t sfb_tile = 0;  // first 128-row scale tile of B the pair tile touches
+  int sfb_shift = 0;     // 0, or 2 when the tile starts 64 rows into that scale tile
+  int rows_valid = 0, cols_valid = 0;
+  bool live = false;
+  int nk = 0;                  // K stages of this tile (0: an empty expert's zero tile)
+  int last_blocks = 0;         // 32-blocks of K in the last stage
+  int64_t k_origin = 0;        // TMA K coordinate of the first stage (grouped wgrad)
+  int64_t sfa_idx = 0;         // grouped: flat scale tile index of this CTA's A rows, stage 0
+  int64_t sfb_idx0 = 0, sfb_idx1 = 0;  // grouped: the two B scale tiles at stage 0
+  int b_z = 0, c_z = 0;        // expert index for the B (grouped rows) and C (wgrad) maps
 };
 
 template <int BN>
@@ -653,14 +673,106 @@ __device__ __forceinline__ DuoTile duo_tile(const Params& p, int64_t pid, uint32
   return t;
 }
 
-template <int BN>
+// Grouped pair tiles.
+//  kGroupRows: expert e's token rows are cut into 128-row tiles; a pair takes two adjacent
+//  tiles of one expert (the second may lie past the segment: computed, never stored) and
+//  one BN-column tile of N, against expert e's weight (B map z = e).
+//  kGroupWgrad: problem e is dW[e] = dY_e^T X_e, [M = N_out] x [N = K_out], reduced over
+//  expert e's tokens; experts are visited heaviest first.
+// Scale tiles are addressed by flat index in the grouped layouts (512 bytes each).
+template <int BN, int kMode>
+__device__ DuoTile duo_tile_grouped(const Params& p, const DuoSeg* seg, int64_t pid,
+                                    uint32_t crank) {
+  DuoTile t;
+  t.live = false;
+  if (!seg->ok) return t;
+  const int E = p.E;
+  const int64_t n_kt = (p.K + BK - 1) / BK;
+  const int64_t n_rt_b = (p.N + 127) / 128;
+  if (kMode == kGroupRows) {
+    const int64_t total = static_cast<int64_t>(seg->pair_base[E]) * p.num_n_tiles;
+    if (pid >= total) return t;
+    const int64_t rp = pid / p.num_n_tiles, nt = pid % p.num_n_tiles;
+    int lo = 0, hi = E - 1;  // expert owning pair row rp
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (seg->pair_base[mid] <= rp) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int64_t j = 2 * (rp - seg->pair_base[e]) + crank;  // row tile within the expert
+    t.m0 = seg->off[e] + j * BM;
+    const int64_t left = seg->off[e + 1] - t.m0;
+    t.rows_valid = static_cast<int>(left <= 0 ? 0 : (left < BM ? left : BM));
+    t.n0 = nt * BN;
+    t.cols_valid = static_cast<int>((p.N - t.n0) < BN ? (p.N - t.n0) : BN);
+    t.nk = static_cast<int>(n_kt);
+    t.last_blocks = static_cast<int>(((p.K - (n_kt - 1) * BK) + 31) / 32);
+    t.k_origin = 0;
+    // indices of tiles that do not exist (an odd last row tile, the second B scale tile
+    // past N) fall back to a tile that does: their rows and columns are never stored
+    const int64_t rt = seg->tile_base[e + 1] - seg->tile_base[e];
+    t.sfa_idx = (seg->tile_base[e] + (j < rt ? j : rt - 1)) * n_kt;
+    const int64_t h = t.n0 / 128;
+    t.sfb_idx0 = (e * n_rt_b + h) * n_kt;
+    t.sfb_idx1 = h + 1 < n_rt_b ? t.sfb_idx0 + n_kt : t.sfb_idx0;
+    t.b_z = e;
+    t.c_z = 0;
+  } else {
+    const int64_t n_pm = ((p.M + 127) / 128 + 1) / 2;
+    const int64_t per = n_pm * p.num_n_tiles;
+    if (pid >= per * E) return t;
+    const int e = seg->order[pid / per];
+    const int64_t r = pid % per;
+    const int64_t pm = r / p.num_n_tiles, nt = r % p.num_n_tiles;
+    const int64_t cnt = seg->off[e + 1] - seg->off[e];
+    const int64_t nk = (cnt + BK - 1) / BK;
+    const int64_t mt = 2 * pm + crank;
+    t.m0 = mt * BM;
+    const int64_t left = p.M - t.m0;
+    t.rows_valid = static_cast<int>(left <= 0 ? 0 : (left < BM ? left : BM));
+    t.n0 = nt * BN;
+    t.cols_valid = static_cast<int>((p.N - t.n0) < BN ? (p.N - t.n0) : BN);
+    t.nk = static_cast<int>(nk);
+    t.last_blocks = nk ? static_cast<int>((cnt - (nk - 1) * BK) / 32) : 0;
+    t.k_origin = seg->off[e];
+    const int64_t tb = seg->tile_base[e];
+    const int64_t n_rt_a = (p.M + 127) / 128;
+    t.sfa_idx = n_rt_a * tb + (mt < n_rt_a ? mt : n_rt_a - 1) * nk;
+    const int64_t h = t.n0 / 128;
+    t.sfb_idx0 = n_rt_b * tb + h * nk;
+    t.sfb_idx1 = h + 1 < n_rt_b ? t.sfb_idx0 + nk : t.sfb_idx0;
+    t.b_z = 0;
+    t.c_z = e;
+  }
+  t.mt = 0;
+  t.sfb_tile = 0;
+  t.sfb_shift = static_cast<int>((t.n0 % 128) / 32);
+  t.live = true;
+  return t;
+}
+
+template <int BN, int kMode>
+__device__ __forceinline__ DuoTile duo_tile_of(const Params& p, const DuoSeg* seg, int64_t pid,
+                                               uint32_t crank) {
+  if constexpr (kMode == kDense) {
+    DuoTile t = duo_tile<BN>(p, pid, crank);
+    t.nk = static_cast<int>((p.K + BK - 1) / BK);
+    t.last_blocks = static_cast<int>(((p.K - (t.nk - 1) * BK) + 31) / 32);
+    t.c_z = 0;
+    return t;
+  } else {
+    return duo_tile_grouped<BN, kMode>(p, seg, pid, crank);
+  }
+}
+
+template <int BN, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
                       const __grid_constant__ CUtensorMap map_b,
                       const __grid_constant__ CUtensorMap map_sfa,
                       const __grid_constant__ CUtensorMap map_sfb,
                       const __grid_constant__ CUtensorMap map_c, const Params p) {
-  using D = Duo<BN>;
+  using D = Duo<BN, kMode>;
   constexpr int kStages = D::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -680,8 +792,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
   const bool leader = crank == 0;
   const int64_t first_id = blockIdx.x >> 1;
   const int64_t id_step = gridDim.x >> 1;
-  const int64_t n_kt = (p.K + BK - 1) / BK;
-  const int last_blocks = static_cast<int>(((p.K - (n_kt - 1) * BK) + 31) / 32);
+  DuoSeg* seg = D::kGrouped ? reinterpret_cast<DuoSeg*>(smem + D::kOffSeg) : nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -701,6 +812,46 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     tma_prefetch_desc(&map_sfb);
     tma_prefetch_desc(&map_c);
   }
+  if constexpr (D::kGrouped) {
+    // segment table: offsets checked (0-based, non-decreasing, 32-aligned, ending at
+    // total_rows), prefix sums, and the heaviest-first expert order
+    const int E = p.E;
+    if (threadIdx.x == 0) seg->ok = 1;
+    __syncthreads();
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) seg->off[i] = p.offsets[i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < E; i += blockDim.x) {
+      const int32_t lo = seg->off[i], hi = seg->off[i + 1];
+      if (hi < lo || (lo & 31) || (hi & 31)) seg->ok = 0;
+    }
+    if (threadIdx.x == 0 &&
+        (seg->off[0] != 0 || static_cast<int64_t>(seg->off[E]) != p.total_rows))
+      seg->ok = 0;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int32_t tiles = 0, pairs = 0;
+      for (int e = 0; e < E; ++e) {
+        seg->tile_base[e] = tiles;
+        seg->pair_base[e] = pairs;
+        const int32_t cnt = seg->off[e + 1] - seg->off[e];
+        const int32_t rt = cnt > 0 ? (cnt + 127) / 128 : 0;
+        tiles += rt;
+        pairs += (rt + 1) / 2;
+      }
+      seg->tile_base[E] = tiles;
+      seg->pair_base[E] = pairs;
+      if (!seg->ok && blockIdx.x == 0) latch_error(p.status, MXFP8_ERR_BAD_OFFSETS);
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      const int32_t ce = seg->off[e + 1] - seg->off[e];
+      int rank = 0;
+      for (int f = 0; f < E; ++f) {
+        const int32_t cf = seg->off[f + 1] - seg->off[f];
+        rank += (cf > ce) || (cf == ce && f < e);
+      }
+      seg->order[rank] = static_cast<int16_t>(e);
+    }
+  }
   if (warp == 1) tmem_alloc_2sm(tmem_slot, D::kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -716,23 +867,36 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     uint32_t it = 0;
     bool ok = true;
     for (int64_t id = first_id; ok; id += id_step) {
-      const DuoTile t = duo_tile<BN>(p, id, crank);
+      const DuoTile t = duo_tile_of<BN, kMode>(p, seg, id, crank);
       if (!t.live) break;
-      for (int64_t kb = 0; kb < n_kt; ++kb, ++it) {
+      for (int64_t kb = 0; kb < t.nk; ++kb, ++it) {
         const uint32_t s = it % kStages, ph = (it / kStages) & 1;
         if (!warp_wait(&empty[s], ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
         const uint32_t bar = full0 + 8 * s;
-        const int32_t kx = static_cast<int32_t>(kb * BK);
+        const int32_t kx = static_cast<int32_t>(t.k_origin + kb * BK);
         if (issuer) {
           if (leader) mbar_arrive_expect_tx(&full[s], 2 * D::kStageBytes);
           tma_load_2d_2sm(smem + D::kOffA + s * D::kABytes, &map_a, kx,
                           static_cast<int32_t>(t.m0), bar);
-          tma_load_2d_2sm(smem + D::kOffB + s * D::kBBytes, &map_b, kx,
-                          static_cast<int32_t>(t.n0 + crank * (BN / 2)), bar);
-          tma_load_3d_2sm(smem + D::kOffSfa + s * D::kSfaBytes, &map_sfa, 0,
-                          static_cast<int32_t>(kb), static_cast<int32_t>(t.mt), bar);
-          tma_load_3d_2sm(smem + D::kOffSfb + s * D::kSfbBytes, &map_sfb, 0,
-                          static_cast<int32_t>(kb), static_cast<int32_t>(t.sfb_tile), bar);
+          if constexpr (kMode == kGroupRows)
+            tma_load_3d_2sm(smem + D::kOffB + s * D::kBBytes, &map_b, kx,
+                            static_cast<int32_t>(t.n0 + crank * (BN / 2)), t.b_z, bar);
+          else
+            tma_load_2d_2sm(smem + D::kOffB + s * D::kBBytes, &map_b, kx,
+                            static_cast<int32_t>(t.n0 + crank * (BN / 2)), bar);
+          if constexpr (kMode == kDense) {
+            tma_load_3d_2sm(smem + D::kOffSfa + s * D::kSfaBytes, &map_sfa, 0,
+                            static_cast<int32_t>(kb), static_cast<int32_t>(t.mt), bar);
+            tma_load_3d_2sm(smem + D::kOffSfb + s * D::kSfbBytes, &map_sfb, 0,
+                            static_cast<int32_t>(kb), static_cast<int32_t>(t.sfb_tile), bar);
+          } else {  // scale tiles by flat index, one 512-byte tile per load
+            tma_load_2d_2sm(smem + D::kOffSfa + s * D::kSfaBytes, &map_sfa, 0,
+                            static_cast<int32_t>(t.sfa_idx + kb), bar);
+            tma_load_2d_2sm(smem + D::kOffSfb + s * D::kSfbBytes, &map_sfb, 0,
+                            static_cast<int32_t>(t.sfb_idx0 + kb), bar);
+            tma_load_2d_2sm(smem + D::kOffSfb + s * D::kSfbBytes + 512, &map_sfb, 0,
+                            static_cast<int32_t>(t.sfb_idx1 + kb), bar);
+          }
         }
         __syncwarp();
       }
@@ -762,8 +926,9 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     constexpr uint32_t kId0 = mxf8_idesc(2 * BM, BN, 0, 0), kId1 = mxf8_idesc(2 * BM, BN, 1, 1);
     constexpr uint32_t kId2 = mxf8_idesc(2 * BM, BN, 2, 2), kId3 = mxf8_idesc(2 * BM, BN, 3, 3);
     for (int64_t id = first_id; ok; id += id_step) {
-      const DuoTile t = duo_tile<BN>(p, id, crank);
+      const DuoTile t = duo_tile_of<BN, kMode>(p, seg, id, crank);
       if (!t.live) break;
+      if (t.nk == 0) continue;  // an empty expert's dW tile: the epilogue writes zeros
       const uint32_t buf = acc_it % D::kAcc, aph = (acc_it / D::kAcc) & 1;
       if (!warp_wait(&acc_empty[buf], aph ^ 1, abort_flag, p.wait_ns)) {
         ok = false;
@@ -772,7 +937,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
       tc_fence_after();
       const uint32_t d_t = tmem + buf * BN;
       const uint32_t shift = static_cast<uint32_t>(t.sfb_shift);
-      for (int64_t kb = 0; kb < n_kt; ++kb, ++it) {
+      for (int64_t kb = 0; kb < t.nk; ++kb, ++it) {
         const uint32_t s = it % kStages, ph = (it / kStages) & 1;
         if (!warp_wait(&full[s], ph, abort_flag, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
@@ -787,13 +952,13 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
           tmem_cp_32x128b_x4_2sm(sfa_t, sfa_desc0 + s * (D::kSfaBytes / 16));
           tmem_cp_32x128b_x4_2sm(sfb_slot, sbd);
           tmem_cp_32x128b_x4_2sm(sfb_slot + 4, sbd + 512 / 16);
-          if (kb != n_kt - 1 || last_blocks == 4) {
+          if (kb != t.nk - 1 || t.last_blocks == 4) {
             mma_mxf8_2sm(d_t, ad, bd, kId0, sfa_t, sfb_t, acc0);
             mma_mxf8_2sm(d_t, ad + 2, bd + 2, kId1, sfa_t, sfb_t, 1u);
             mma_mxf8_2sm(d_t, ad + 4, bd + 4, kId2, sfa_t, sfb_t, 1u);
             mma_mxf8_2sm(d_t, ad + 6, bd + 6, kId3, sfa_t, sfb_t, 1u);
           } else {
-            for (int k = 0; k < last_blocks; ++k)
+            for (int k = 0; k < t.last_blocks; ++k)
               mma_mxf8_2sm(d_t, ad + 2 * k, bd + 2 * k, mxf8_idesc(2 * BM, BN, k, k), sfa_t,
                            sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
           }
@@ -826,26 +991,33 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     uint32_t acc_it = 0;
     bool ok = true;
     for (int64_t id = first_id; ok; id += id_step) {
-      const DuoTile t = duo_tile<BN>(p, id, crank);
+      const DuoTile t = duo_tile_of<BN, kMode>(p, seg, id, crank);
       if (!t.live) break;
-      const uint32_t buf = acc_it % D::kAcc, aph = (acc_it / D::kAcc) & 1;
-      int got = 0;
-      if (lane == 0) got = mbar_wait_bounded(&acc_full[buf], aph, abort_flag, p.wait_ns);
-      got = __shfl_sync(0xFFFFFFFFu, got, 0);
-      if (!got) { ok = false; break; }
-      tc_fence_after();
       // The whole slice goes to registers and TMEM is handed back before any store.
       uint32_t v[kChunks][32];
-      __syncwarp();
-      const uint32_t base =
-          tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + half * kChunks * 32;
+      if (t.nk > 0) {
+        const uint32_t buf = acc_it % D::kAcc, aph = (acc_it / D::kAcc) & 1;
+        int got = 0;
+        if (lane == 0) got = mbar_wait_bounded(&acc_full[buf], aph, abort_flag, p.wait_ns);
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        if (!got) { ok = false; break; }
+        tc_fence_after();
+        __syncwarp();
+        const uint32_t base =
+            tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * BN + half * kChunks * 32;
 #pragma unroll
-      for (int c = 0; c < kChunks; ++c) tmem_ld_32x32b_x32(base + 32 * c, v[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty0 + 8 * buf);
-      ++acc_it;
+        for (int c = 0; c < kChunks; ++c) tmem_ld_32x32b_x32(base + 32 * c, v[c]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty0 + 8 * buf);
+        ++acc_it;
+      } else {  // an empty expert: its dW tile is zero
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[c][i] = 0;
+      }
       // Stores leave through shared memory: each 64-byte column group of the warp's 32 rows
       // is written into the warp's staging box (16-byte chunks XOR-swizzled as the tensor
       // map's 64-byte swizzle expects, so the 32 lanes hit distinct banks) and sent with one
@@ -883,8 +1055,12 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&map_c, box, static_cast<int32_t>(t.n0 + col),
-                           static_cast<int32_t>(t.m0 + 32 * q));
+              if constexpr (kMode == kDense)
+                tma_store_2d(&map_c, box, static_cast<int32_t>(t.n0 + col),
+                             static_cast<int32_t>(t.m0 + 32 * q));
+              else
+                tma_store_3d(&map_c, box, static_cast<int32_t>(t.n0 + col),
+                             static_cast<int32_t>(t.m0 + 32 * q), t.c_z);
               bulk_commit_group();
             }
           }
@@ -1087,18 +1263,18 @@ cudaLaunchConfig_t cluster2_config(int64_t grid, int smem, cudaStream_t stream,
 }
 
 // How many clusters of the 2SM kernel fit on the device at once (cached per device).
-template <int BN>
+template <int BN, int kMode = kDense>
 int64_t max_duo_clusters() {
   static int64_t cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
-  auto k = mxfp8_gemm_2sm_kernel<BN>;
+  auto k = mxfp8_gemm_2sm_kernel<BN, kMode>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Duo<BN>::kSmemBytes) != cudaSuccess)
+                           Duo<BN, kMode>::kSmemBytes) != cudaSuccess)
     return 0;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster2_config(2 * 256, Duo<BN>::kSmemBytes, nullptr, attr);
+  cudaLaunchConfig_t cfg = cluster2_config(2 * 256, Duo<BN, kMode>::kSmemBytes, nullptr, attr);
   int clusters = 0;
   if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess || clusters <= 0)
     clusters = num_sms() / 2;
@@ -1157,11 +1333,73 @@ int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
   if (fit <= 0) return MXFP8_ERR_CUDA;
   const int64_t clusters = pair_tiles < fit ? pair_tiles : fit;
   if (clusters <= 0) return MXFP8_OK;
-  auto k = mxfp8_gemm_2sm_kernel<BN>;
+  auto k = mxfp8_gemm_2sm_kernel<BN, kDense>;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster2_config(2 * clusters, D::kSmemBytes, stream, attr);
   return cudaLaunchKernelEx(&cfg, k, ma, mb, msa, msb, mc, p) == cudaSuccess ? MXFP8_OK
                                                                               : MXFP8_ERR_CUDA;
+}
+
+// The scale tiles of an operand as a flat array of 512-byte tiles (16-bit elements), for
+// grouped layouts whose K-tile count differs from expert to expert.
+bool make_sf_flat_map(CUtensorMap* map, const void* base, int64_t tiles) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {256, static_cast<cuuint64_t>(tiles)};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {256, 1};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Grouped GEMM on CTA pairs (kGroupRows: fprop/dgrad, kGroupWgrad). `p` has M, N, K, E,
+// offsets and total_rows set as the one-SM grouped launcher sets them.
+template <int BN, int kMode>
+int launch_duo_grouped(const GemmArgs& a, Params p, cudaStream_t stream) {
+  using D = Duo<BN, kMode>;
+  const int64_t T = p.total_rows, E = p.E;
+  const int64_t seg_tiles = (T + 127) / 128 + E;  // bound on sum of ceil(count / 128)
+  const bool fp32 = p.out_fp32 != 0;
+  CUtensorMap ma, mb, msa, msb, mc;
+  int64_t pair_tiles = 0;
+  p.num_n_tiles = static_cast<int>((p.N + BN - 1) / BN);
+  if (kMode == kGroupWgrad) {
+    // A = dY^T [M][T], B = X^T [N][T], both blocked along the tokens; C[e] = [M][N]
+    if (!make_map(&ma, a.A, 2, T, p.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
+    if (!make_map(&mb, a.B, 2, T, p.N, 1, BK, BN / 2)) return MXFP8_ERR_CUDA;
+    if (!make_sf_flat_map(&msa, a.sA, ((p.M + 127) / 128) * seg_tiles)) return MXFP8_ERR_CUDA;
+    if (!make_sf_flat_map(&msb, a.sB, ((p.N + 127) / 128) * seg_tiles)) return MXFP8_ERR_CUDA;
+    if (!make_out_map(&mc, a.C, p.M, p.N, E, fp32, 3)) return MXFP8_ERR_CUDA;
+    pair_tiles = (((p.M + 127) / 128 + 1) / 2) * p.num_n_tiles * E;
+  } else {
+    // A = X [T][K] segmented by rows, B = W [E][N][K], C = [T][N]
+    const int64_t n_kt = (p.K + BK - 1) / BK;
+    if (!make_map(&ma, a.A, 2, p.K, T, 1, BK, BM)) return MXFP8_ERR_CUDA;
+    if (!make_map(&mb, a.B, 3, p.K, p.N, E, BK, BN / 2)) return MXFP8_ERR_CUDA;
+    if (!make_sf_flat_map(&msa, a.sA, seg_tiles * n_kt)) return MXFP8_ERR_CUDA;
+    if (!make_sf_flat_map(&msb, a.sB, E * ((p.N + 127) / 128) * n_kt)) return MXFP8_ERR_CUDA;
+    if (!make_out_map(&mc, a.C, T, p.N, 1, fp32, 3)) return MXFP8_ERR_CUDA;
+    pair_tiles = ((T + 127) / 128 / 2 + E) * p.num_n_tiles;  // bound on pair tiles
+  }
+  const int64_t fit = max_duo_clusters<BN, kMode>();
+  if (fit <= 0) return MXFP8_ERR_CUDA;
+  const int64_t clusters = pair_tiles < fit ? pair_tiles : fit;
+  if (clusters <= 0) return MXFP8_OK;
+  auto k = mxfp8_gemm_2sm_kernel<BN, kMode>;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster2_config(2 * clusters, D::kSmemBytes, stream, attr);
+  return cudaLaunchKernelEx(&cfg, k, ma, mb, msa, msb, mc, p) == cudaSuccess ? MXFP8_OK
+                                                                              : MXFP8_ERR_CUDA;
+}
+
+// Tile width for the grouped 2SM GEMMs: 256 (measured faster than 192 for both modes on
+// the Qwen3-30B-A3B expert layer, wgrad included); MXFP8_GEMM_BN forces a width.
+int duo_grouped_width(int) {
+  const char* e = getenv("MXFP8_GEMM_BN");
+  const int w = e ? atoi(e) : 0;
+  return (w == 256 || w == 192) ? w : 256;
 }
 
 bool pairs_enabled() {
@@ -1237,6 +1475,10 @@ int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     p.num_n_tiles = static_cast<int>((p.N + bn - 1) / bn);
     const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles * p.E;
     p.num_tiles = tiles;
+    if (wide && p.num_m_tiles >= 2 && p.E <= kMaxDuoExperts && duo_enabled())
+      return duo_grouped_width(kGroupWgrad) == 256
+                 ? launch_duo_grouped<256, kGroupWgrad>(a, p, stream)
+                 : launch_duo_grouped<192, kGroupWgrad>(a, p, stream);
     if (!make_map(&ma, a.A, 2, a.total_rows, p.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
     if (!make_map(&mb, a.B, 2, a.total_rows, p.N, 1, BK, bn)) return MXFP8_ERR_CUDA;
     if (!make_out_map(&mc, a.C, p.M, p.N, p.E, p.out_fp32 != 0, 3)) return MXFP8_ERR_CUDA;
@@ -1256,6 +1498,10 @@ int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.num_n_tiles = static_cast<int>((p.N + bn - 1) / bn);
   const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
   p.num_tiles = tiles;
+  if (wide && p.E <= kMaxDuoExperts && duo_enabled())
+    return duo_grouped_width(kGroupRows) == 256
+               ? launch_duo_grouped<256, kGroupRows>(a, p, stream)
+               : launch_duo_grouped<192, kGroupRows>(a, p, stream);
   if (!make_map(&ma, a.A, 2, a.K, a.total_rows, 1, BK, BM)) return MXFP8_ERR_CUDA;
   if (!make_map(&mb, a.B, 3, a.K, a.N, a.num_experts, BK, bn)) return MXFP8_ERR_CUDA;
   if (!make_out_map(&mc, a.C, a.total_rows, p.N, 1, p.out_fp32 != 0, 3)) return MXFP8_ERR_CUDA;

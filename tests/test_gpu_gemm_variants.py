@@ -2,7 +2,7 @@
 
 The library picks a kernel per problem: the 2SM kernel (tcgen05.mma.cta_group::2) with
 256 x 256 or 256 x 192 tiles, or the one-SM kernel, run as CTA pairs sharing B or as
-single CTAs. The choice is read from the environment once per process, so each forced
+single CTAs; grouped (MoE) GEMMs run on the 2SM kernel too, or on the one-SM kernel. The choice is read from the environment once per process, so each forced
 variant runs the parity tests of test_gpu_gemm.py in a child process. The shapes there
 cover ragged M, N and K, a CTA pair whose second M tile lies past M, and 192-wide tiles
 starting 64 rows into a B scale tile.
@@ -22,7 +22,8 @@ VARIANTS = {
     "1sm_pairs": {"MXFP8_GEMM_2SM": "0", "MXFP8_GEMM_PAIRS": "1"},
     "1sm_single": {"MXFP8_GEMM_2SM": "0", "MXFP8_GEMM_PAIRS": "0"},
 }
-SELECT = ("shapes_random_operands or extreme_scales or small_layer or layer_set_full_size")
+SELECT = ("shapes_random_operands or extreme_scales or small_layer or layer_set_full_size "
+          "or grouped_fprop_dgrad_wgrad_small or experts_full_size")
 
 
 @pytest.mark.parametrize("name", sorted(VARIANTS))
