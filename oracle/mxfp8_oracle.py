@@ -192,6 +192,69 @@ def dequantize(codes, scales) -> np.ndarray:
     return (v * e8m0_decode(scales)[..., None]).reshape(rows, cols)
 
 
+# ---------------------------------------------- FP8 block-wise weights (a different grid)
+
+BW_BLOCK = 128                 # 128 x 128 weight blocks (reading; the pages give no size)
+BW_SCALE_FP32, BW_SCALE_POW2 = 0, 1
+
+
+def quantize_blockwise_2d(x_bits, scale_type=BW_SCALE_FP32):
+    """FP8 block-wise quantization of a BF16 weight: E4M3 elements, one scale per 128 x 128
+    block ("End-to-End MXFP8 RL on Blackwell", section "A different grid, and drift": the
+    FP8-blockwise learner must use power-of-two block scales on Blackwell while its
+    sampler uses FP32 scales, so the two round the same BF16 weight differently; section
+    "The pipeline", paragraph "The format": TE emulates that recipe with MXFP8 GEMMs,
+    hence the power-of-two scales).
+
+    Readings: blocks are 128 x 128 (ragged at the matrix edge); amax = max |v| over the
+    block; the quantization factor s is
+      BW_SCALE_FP32: 448 / amax as an IEEE single-precision division, or the largest
+                     finite single-precision value when that quotient overflows
+                     (amax below about 448 * 2^-128);
+      BW_SCALE_POW2: 2^-e with e = ceil(log2(amax / 448)), clamped at -127 (the round-up
+                     rule of block_scale_exponent);
+    s = 1 for an all-zero block; element = E4M3(v * s) with the product rounded to single
+    precision (exact for POW2), then round-to-nearest-even, saturating; the stored
+    dequantization factor is 1 / s rounded to single precision (exactly 2^e for POW2).
+    A block with a NaN or an infinity stores NaN and every element becomes 0x7F with its
+    own sign. Returns (codes uint8 [R, C], scale_inv float32 [ceil(R/128), ceil(C/128)])."""
+    x = bf16_to_f64(x_bits)
+    rows, cols = x.shape
+    br, bc = ceil_div(rows, BW_BLOCK), ceil_div(cols, BW_BLOCK)
+    codes = np.empty((rows, cols), dtype=np.uint8)
+    scale_inv = np.empty((br, bc), dtype=np.float32)
+    for i in range(br):
+        for j in range(bc):
+            blk = x[i * BW_BLOCK:(i + 1) * BW_BLOCK, j * BW_BLOCK:(j + 1) * BW_BLOCK]
+            out = codes[i * BW_BLOCK:(i + 1) * BW_BLOCK, j * BW_BLOCK:(j + 1) * BW_BLOCK]
+            if not np.all(np.isfinite(blk)):
+                out[...] = (E4M3_NAN | (np.signbit(blk).astype(np.int64) << 7)).astype(np.uint8)
+                scale_inv[i, j] = np.float32(np.nan)
+                continue
+            amax = float(np.max(np.abs(blk)))
+            if amax == 0.0:
+                s = np.float32(1.0)
+            elif scale_type == BW_SCALE_FP32:
+                with np.errstate(over="ignore"):
+                    s = np.float32(E4M3_MAX) / np.float32(amax)
+                if not np.isfinite(s):
+                    s = np.finfo(np.float32).max
+            else:
+                e = int(block_scale_exponent(amax, RULE_CEIL))
+                s = np.float32(np.ldexp(1.0, -e))
+            prod = (blk.astype(np.float32) * s).astype(np.float64)  # single-precision product
+            out[...] = e4m3_round_code(prod)
+            scale_inv[i, j] = np.float32(1.0) / s
+    return codes, scale_inv
+
+
+def dequantize_blockwise_2d(codes, scale_inv) -> np.ndarray:
+    """float64 value of block-wise codes: E4M3 value times the block's scale_inv."""
+    v = e4m3_decode(codes)
+    f = np.repeat(np.repeat(np.asarray(scale_inv, dtype=np.float64), BW_BLOCK, 0), BW_BLOCK, 1)
+    return v * f[:v.shape[0], :v.shape[1]]
+
+
 # -------------------------------------------------------------- swizzled scale layout
 
 def ceil_div(a, b):
