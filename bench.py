@@ -602,9 +602,27 @@ def run_workload(args):
         ms = timed(sync_pass, 5)
         elems = sum(n * k for _, _, n, k in shapes)
         gbs = elems * QBYTES_PER_ELEM / (ms * 1e-3) / 1e9
-        print(json.dumps({"workload": "weight-sync quantize pass, Qwen3-8B shapes (144 weights, "
-                          f"{elems / 1e9:.3f} G elems)", "ms": ms, "GB/s": gbs,
-                          "frac_of_hbm": gbs / pk["hbm"], "launches": len(shapes)}), flush=True)
+        line = {"workload": "weight-sync quantize pass, Qwen3-8B shapes (144 weights, "
+                            f"{elems / 1e9:.3f} G elems)", "ms": ms, "GB/s": gbs,
+                "frac_of_hbm": gbs / pk["hbm"], "launches": len(shapes)}
+        # the same pass with the FP8 block-wise recipe (128 x 128 blocks): 2 B read + 1 B
+        # written per element, plus one float per block
+        bw_bytes = elems * (3.0 + 4.0 / (128 * 128))
+        for key, st in (("blockwise_pow2", m.BW_POW2), ("blockwise_fp32", m.BW_FP32)):
+            bw_out = {name: (torch.empty_like(w, dtype=torch.uint8),
+                             torch.empty(((w.shape[0] + 127) // 128, (w.shape[1] + 127) // 128),
+                                         dtype=torch.float32, device=dev))
+                      for name, (w, _, _) in bufs.items()}
+
+            def bw_pass(st=st, bw_out=bw_out):
+                for _, name, n, k in shapes:
+                    q, si = bw_out[name]
+                    m.quantize_blockwise(bufs[name][0], st, out=q, scale_inv=si, stream=stream)
+
+            bms = timed(bw_pass, 5)
+            line[key] = {"ms": bms, "GB/s": bw_bytes / (bms * 1e-3) / 1e9,
+                         "frac_of_hbm": bw_bytes / (bms * 1e-3) / 1e9 / pk["hbm"]}
+        print(json.dumps(line), flush=True)
     elif args.workload == "moe":
         d = W.moe_expert_layer(dev)
         offs = d["offsets"].to(dev)
@@ -629,7 +647,19 @@ def run_workload(args):
             if name.startswith("quantize"):
                 res[name] = {"ms": ms, "GB/s": x.numel() * QBYTES_PER_ELEM / (ms * 1e-3) / 1e9}
             else:
-                res[name] = {"ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12}
+                # algorithmic bytes: E4M3 operands (+1/32 scales) and the BF16 output; the
+                # roofline is min(tensor peak, arithmetic intensity x HBM bandwidth)
+                t_rows = int(d["offsets"][-1])
+                if name == "wgrad":
+                    nbytes = (n + k) * t_rows * (1 + 1 / 32) + E * n * k * 2
+                else:
+                    nin, nout = (k, n) if name == "fprop" else (n, k)
+                    nbytes = (t_rows * nin + E * n * k) * (1 + 1 / 32) + t_rows * nout * 2
+                ai = flops / nbytes
+                roof = min(pk["bf16_sus"] * FP8_OVER_BF16, ai * pk["hbm"] * 1e-3)
+                tf = flops / (ms * 1e-3) / 1e12
+                res[name] = {"ms": ms, "TFLOP/s": tf, "flop_per_byte": ai,
+                             "roof_TFLOP/s": roof, "frac_of_roof": tf / roof}
         print(json.dumps({"workload": "Qwen3-30B-A3B gate_up experts (128 x 1536 x 2048), "
                           f"{real} routed rows, {int(d['offsets'][-1])} padded", **res}), flush=True)
     elif args.workload == "sweep":

@@ -176,6 +176,42 @@ typedef struct mxfp8_dual_job {
 int mxfp8_quantize_dual_multi(const mxfp8_dual_job* jobs, int num_jobs, int scale_layout,
                               void* stream);
 
+/* Scale choice of the FP8 block-wise recipe (mxfp8_quantize_blockwise). */
+typedef enum {
+  MXFP8_BW_SCALE_FP32 = 0, /* quantization factor 448 / amax in single precision */
+  MXFP8_BW_SCALE_POW2 = 1  /* power-of-two factor 2^-ceil(log2(amax / 448)) */
+} mxfp8_blockwise_scale;
+
+/*
+ * Number of float scales mxfp8_quantize_blockwise writes for a [rows][cols] weight:
+ * ceil(rows/128) * ceil(cols/128). Returns 0 for invalid arguments.
+ */
+size_t mxfp8_blockwise_scale_count(int64_t rows, int64_t cols);
+
+/*
+ * FP8 block-wise weight quantization, the recipe the pages contrast with MXFP8 ("A
+ * different grid, and drift": on Blackwell the block-wise learner must use power-of-two
+ * block scales while its sampler uses FP32 scales, so the two sides round the same BF16
+ * weight differently; "The pipeline", "The format": TE emulates that recipe with MXFP8
+ * GEMMs). One scale per 128 x 128 block (the pages give no block size; 128 x 128 is the
+ * block-wise weight recipe's usual one):
+ *   amax = max |v| over the block;
+ *   s = 448 / amax in IEEE single precision (largest finite float if that overflows),
+ *       or 2^-e with e = ceil(log2(amax / 448)) >= -127 for MXFP8_BW_SCALE_POW2;
+ *       s = 1 for an all-zero block;
+ *   code = E4M3(v * s), the product rounded to single precision, then to nearest even,
+ *          saturating at 448;
+ *   scale_inv = 1 / s in single precision (exactly 2^e for POW2);
+ *   a block holding a NaN or an infinity: scale_inv NaN, codes 0x7F with each sign.
+ *   src_dev        BF16 [rows][cols], cols % 8 == 0, 16-byte aligned
+ *   out_dev        E4M3 [rows][cols], 16-byte aligned
+ *   scale_inv_dev  float [ceil(rows/128)][ceil(cols/128)], 4-byte aligned
+ * Errors: MXFP8_ERR_INVALID_ARG (bad scale_type, negative or too large sizes, null
+ * pointers), MXFP8_ERR_ALIGNMENT (cols % 8, misaligned pointers).
+ */
+int mxfp8_quantize_blockwise(const void* src_dev, int64_t rows, int64_t cols, void* out_dev,
+                             float* scale_inv_dev, int scale_type, void* stream);
+
 /*
  * `batch` independent matrices [batch][rows][cols] quantized as by mxfp8_quantize, each
  * with its own scale block of mxfp8_scale_bytes(rows, cols, axis, layout) bytes; the

@@ -37,6 +37,8 @@ SIGNATURES = {
     "mxfp8_quantize_rule": (_I, [_P, _I64, _I64, _I, _P, _P, _I, _I, _P]),
     "mxfp8_quantize_dual": (_I, [_P, _I64, _I64, _P, _P, _P, _P, _I, _P]),
     "mxfp8_quantize_dual_multi": (_I, [_P, _I, _I, _P]),
+    "mxfp8_blockwise_scale_count": (_SZ, [_I64, _I64]),
+    "mxfp8_quantize_blockwise": (_I, [_P, _I64, _I64, _P, _P, _I, _P]),
     "mxfp8_quantize_batched": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _I, _P]),
     "mxfp8_quantize_grouped_dual": (_I, [_P, _I64, _I64, _P, _I, _P, _P, _P, _P, _P]),
     "mxfp8_quantize_grouped": (_I, [_P, _I64, _I64, _I, _P, _I, _P, _P, _P]),
@@ -161,6 +163,26 @@ def quantize_dual(src: torch.Tensor, layout: int = SWIZZLED, row_out=None, row_s
                                      _ptr(col_out), _ptr(col_scales), layout, _stream(stream)),
            "mxfp8_quantize_dual")
     return row_out, row_scales, col_out, col_scales
+
+
+BW_FP32, BW_POW2 = 0, 1  # mxfp8_blockwise_scale
+
+
+def quantize_blockwise(src: torch.Tensor, scale_type: int = BW_FP32, out=None, scale_inv=None,
+                       stream=None):
+    """FP8 block-wise weight quantization (128 x 128 blocks). Returns (E4M3 codes as uint8
+    [rows, cols], float32 scale_inv [ceil(rows/128), ceil(cols/128)])."""
+    _require(src, torch.bfloat16, "src")
+    rows, cols = src.shape
+    dev = src.device
+    out = torch.empty((rows, cols), dtype=torch.uint8, device=dev) if out is None else out
+    if scale_inv is None:
+        scale_inv = torch.empty(((rows + 127) // 128, (cols + 127) // 128), dtype=torch.float32,
+                                device=dev)
+    _check(lib().mxfp8_quantize_blockwise(_ptr(src), rows, cols, _ptr(out), _ptr(scale_inv),
+                                          scale_type, _stream(stream)),
+           "mxfp8_quantize_blockwise")
+    return out, scale_inv
 
 
 class DualJob(ctypes.Structure):

@@ -252,6 +252,33 @@ int mxfp8_quantize_dual_multi(const mxfp8_dual_job* jobs, int num_jobs, int scal
              : MXFP8_ERR_CUDA;
 }
 
+size_t mxfp8_blockwise_scale_count(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0 || cols % 8) return 0;
+  return static_cast<size_t>(cdiv(rows, 128) * cdiv(cols, 128));
+}
+
+int mxfp8_quantize_blockwise(const void* src_dev, int64_t rows, int64_t cols, void* out_dev,
+                             float* scale_inv_dev, int scale_type, void* stream) {
+  if (scale_type != MXFP8_BW_SCALE_FP32 && scale_type != MXFP8_BW_SCALE_POW2)
+    return MXFP8_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0) return MXFP8_ERR_INVALID_ARG;
+  if (cols % 8) return MXFP8_ERR_ALIGNMENT;
+  if (rows == 0 || cols == 0) return MXFP8_OK;
+  if (!src_dev || !out_dev || !scale_inv_dev) return MXFP8_ERR_INVALID_ARG;
+  if (!aligned16(src_dev) || !aligned16(out_dev) ||
+      (reinterpret_cast<uintptr_t>(scale_inv_dev) & 3u))
+    return MXFP8_ERR_ALIGNMENT;
+  if (cdiv(rows, 128) > 65535 || cdiv(cols, 128) > 0x7FFFFFFF) return MXFP8_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  const int st = device_state(&d);
+  if (st != MXFP8_OK) return st;
+  return launch_blockwise(src_dev, rows, cols, out_dev, scale_inv_dev,
+                          scale_type == MXFP8_BW_SCALE_POW2,
+                          static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MXFP8_OK
+             : MXFP8_ERR_CUDA;
+}
+
 int mxfp8_quantize_batched(const void* src_dev, int64_t batch, int64_t rows, int64_t cols,
                            int axis, void* out_dev, void* scales_dev, int scale_layout,
                            void* stream) {

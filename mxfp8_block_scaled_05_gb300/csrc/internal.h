@@ -44,6 +44,10 @@ struct QuantizeJobs {
 
 cudaError_t launch_quantize_jobs(const QuantizeJobs& j, cudaStream_t stream);
 
+// FP8 block-wise (128 x 128) weight quantization; scale_inv [ceil(rows/128)][ceil(cols/128)].
+cudaError_t launch_blockwise(const void* src, int64_t rows, int64_t cols, void* out,
+                             float* scale_inv, bool pow2, cudaStream_t stream);
+
 struct GemmArgs {
   const void* A;
   const void* sA;

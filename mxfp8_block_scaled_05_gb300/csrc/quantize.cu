@@ -375,6 +375,89 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
   }
 }
 
+// FP8 block-wise weight quantization: one FP32 (or power-of-two) scale per 128 x 128
+// block ("End-to-End MXFP8 RL on Blackwell", section "A different grid, and drift"). One
+// CTA per block: the block maximum comes from packed 16-bit maxima, warp shuffles and a
+// shared-memory step; the factor s is 448 / amax (IEEE division, clamped to the largest
+// float on overflow) or the power-of-two 2^-ceil(log2(amax / 448)); elements are
+// E4M3(v * s) with the product rounded to single precision; 1 / s is stored.
+template <bool kPow2>
+__global__ void __launch_bounds__(kThreads)
+blockwise_quantize_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t cols,
+                          uint8_t* __restrict__ out, float* __restrict__ scale_inv) {
+  __shared__ uint32_t warp_max[kThreads / 32];
+  __shared__ float s_factor;
+  const int t = threadIdx.x, v = t & 15, rsub = t >> 4;
+  const int64_t row0 = static_cast<int64_t>(blockIdx.y) * kTile;
+  const int64_t col0 = static_cast<int64_t>(blockIdx.x) * kTile;
+  const int rows_valid = static_cast<int>((rows - row0) < kTile ? (rows - row0) : kTile);
+  const int cols_valid = static_cast<int>((cols - col0) < kTile ? (cols - col0) : kTile);
+  const bool col_ok = 8 * v < cols_valid;  // cols % 8 == 0
+  uint4 x[8];
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int r = rsub + 16 * j;
+    x[j] = (col_ok && r < rows_valid) ? ld_nc_v4(src + (row0 + r) * cols + col0 + 8 * v)
+                                      : make_uint4(0, 0, 0, 0);
+    m2 = max_u16x2(m2, max_u16x2(max_u16x2(x[j].x & kAbs2, x[j].y & kAbs2),
+                                 max_u16x2(x[j].z & kAbs2, x[j].w & kAbs2)));
+  }
+  uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((t & 31) == 0) warp_max[t >> 5] = m;
+  __syncthreads();
+  if (t == 0) {
+    uint32_t a = 0;
+    for (int w = 0; w < kThreads / 32; ++w) a = max(a, warp_max[w]);
+    float f, inv;
+    if (a >= 0x7F80u) {                 // NaN or Inf in the block
+      f = 0.f;
+      inv = __uint_as_float(0x7FC00000u);
+    } else if (a == 0) {                // all zero
+      f = 1.f;
+      inv = 1.f;
+    } else if (kPow2) {
+      // e = ceil(log2(amax / 448)) >= -127; the BF16 exponent gives floor(log2 amax)
+      int e = static_cast<int>(a >> 7) - 127 - 8 + ((a & 0x7Fu) > 0x60u ? 1 : 0);
+      if ((a >> 7) == 0) e = -127;      // BF16 subnormal
+      e = e < -127 ? -127 : e;
+      f = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+      inv = e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23)
+                      : __uint_as_float(0x00400000u);  // 2^-127
+    } else {
+      f = __fdiv_rn(448.f, __uint_as_float(a << 16));
+      if (isinf(f)) f = 3.40282347e38f;  // the largest finite float
+      inv = __fdiv_rn(1.f, f);
+    }
+    s_factor = f;
+    scale_inv[static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x] = inv;
+  }
+  __syncthreads();
+  const float f = s_factor;
+  const bool nan_block = f == 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int r = rsub + 16 * j;
+    if (!col_ok || r >= rows_valid) continue;
+    uint2 o;
+    if (!nan_block) {
+      const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+      uint32_t b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        b[i] = cvt_e4m3x2(__fmul_rn(bf16hi(w[i]), f), __fmul_rn(bf16lo(w[i]), f));
+      o.x = b[0] | (b[1] << 16);
+      o.y = b[2] | (b[3] << 16);
+    } else {
+      o.x = nan4(x[j].x, x[j].y);
+      o.y = nan4(x[j].z, x[j].w);
+    }
+    *reinterpret_cast<uint2*>(out + (row0 + r) * cols + col0 + 8 * v) = o;
+  }
+}
+
 template <bool kRow, bool kCol, bool kSw, bool kGr>
 cudaError_t launch_tiles(const QuantizeArgs& a, cudaStream_t stream) {
   const int64_t col_tiles = (a.cols + kTile - 1) / kTile;
@@ -440,6 +523,21 @@ cudaError_t launch_quantize_jobs(const QuantizeJobs& in, cudaStream_t stream) {
     quantize_tile_kernel<true, true, false, false, true><<<static_cast<unsigned>(tiles), kThreads, 0,
                                                            stream>>>(
         nullptr, 0, 0, none, none, nullptr, 0, MXFP8_RULE_FLOOR, in.status, j);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_blockwise(const void* src, int64_t rows, int64_t cols, void* out,
+                             float* scale_inv, bool pow2, cudaStream_t stream) {
+  const int64_t gx = (cols + kTile - 1) / kTile, gy = (rows + kTile - 1) / kTile;
+  if (gx == 0 || gy == 0) return cudaSuccess;
+  if (gy > 65535 || gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+  if (pow2)
+    blockwise_quantize_kernel<true><<<grid, kThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(src), rows, cols, static_cast<uint8_t*>(out), scale_inv);
+  else
+    blockwise_quantize_kernel<false><<<grid, kThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(src), rows, cols, static_cast<uint8_t*>(out), scale_inv);
   return cudaGetLastError();
 }
 

@@ -99,6 +99,22 @@ def test_argument_errors_need_no_device(lib):
     assert qg(p, 48, 64, m.ROW, p, 4, p, p, None) == m.ERR_ALIGNMENT
 
 
+def test_blockwise_sizes_and_argument_errors_need_no_device(lib):
+    P = ctypes.c_void_p(0x10000)
+    assert lib.mxfp8_blockwise_scale_count(256, 384) == 2 * 3
+    assert lib.mxfp8_blockwise_scale_count(200, 136) == 2 * 2
+    assert lib.mxfp8_blockwise_scale_count(64, 12) == 0            # cols % 8
+    assert lib.mxfp8_blockwise_scale_count(-1, 64) == 0
+    qb = lib.mxfp8_quantize_blockwise
+    assert qb(P, 64, 64, P, P, 2, None) == m.ERR_INVALID_ARG         # scale type
+    assert qb(P, 64, 60, P, P, m.BW_FP32, None) == m.ERR_ALIGNMENT  # cols % 8
+    assert qb(None, 64, 64, P, P, m.BW_POW2, None) == m.ERR_INVALID_ARG
+    assert qb(P, 64, 64, P, ctypes.c_void_p(0x10002), m.BW_FP32, None) == m.ERR_ALIGNMENT
+    assert qb(ctypes.c_void_p(0x10008), 64, 64, P, P, m.BW_FP32, None) == m.ERR_ALIGNMENT
+    assert qb(P, -1, 64, P, P, m.BW_FP32, None) == m.ERR_INVALID_ARG
+    assert qb(None, 0, 64, None, None, m.BW_FP32, None) == m.OK     # empty: no-op
+
+
 def test_multi_job_argument_errors_need_no_device(lib):
     qm = lib.mxfp8_quantize_dual_multi
     P = 0x10000
