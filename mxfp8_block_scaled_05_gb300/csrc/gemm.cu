@@ -92,6 +92,8 @@ struct Params {
   int band;              // dense: M tiles (CTA pairs: pairs of M tiles) per raster band
   int* status;
   uint64_t wait_ns;
+  // dense 2SM kernel: pair tiles from this index on each run as two half-width tiles
+  int64_t split_from = INT64_MAX;
 };
 
 // Everything a role needs to know about one output tile.
@@ -648,12 +650,23 @@ struct DuoTile {
   int64_t sfa_idx = 0;         // grouped: flat scale tile index of this CTA's A rows, stage 0
   int64_t sfb_idx0 = 0, sfb_idx1 = 0;  // grouped: the two B scale tiles at stage 0
   int b_z = 0, c_z = 0;        // expert index for the B (grouped rows) and C (wgrad) maps
+  int width = 0;               // output columns of the tile: BN, or BN / 2 for a half tile
 };
 
+// Dense pair tiles. Work item `pid` below p.split_from is pair tile pid; from there on, two
+// items share one pair tile, each taking half of its columns (256 x BN/2). The host puts the
+// split at the last, partial wave of clusters when its halves fit in one wave, so that wave
+// takes about half as long.
 template <int BN>
-__device__ __forceinline__ DuoTile duo_tile(const Params& p, int64_t pid, uint32_t crank) {
+__device__ __forceinline__ DuoTile duo_tile(const Params& p, int64_t item, uint32_t crank) {
   DuoTile t;
   const int64_t n_pm = (p.num_m_tiles + 1) / 2;
+  int64_t pid = item;
+  int half = -1;  // -1: the whole tile; 0 / 1: its left / right half
+  if (item >= p.split_from) {
+    pid = p.split_from + (item - p.split_from) / 2;
+    half = static_cast<int>((item - p.split_from) & 1);
+  }
   t.live = pid < n_pm * p.num_n_tiles;
   if (!t.live) return t;
   const int64_t GP = p.band;  // bands of p.band pair rows sweep across N, pair rows fastest
@@ -664,12 +677,14 @@ __device__ __forceinline__ DuoTile duo_tile(const Params& p, int64_t pid, uint32
   const int64_t nt = (pid % band) / gp;
   t.mt = 2 * pm + crank;
   t.m0 = t.mt * BM;
-  t.n0 = nt * BN;
+  t.width = half < 0 ? BN : BN / 2;
+  t.n0 = nt * BN + (half > 0 ? BN / 2 : 0);
   t.sfb_tile = t.n0 / 128;
   t.sfb_shift = static_cast<int>((t.n0 % 128) / 32);
   const int64_t left = p.M - t.m0;
   t.rows_valid = static_cast<int>(left <= 0 ? 0 : (left < BM ? left : BM));
-  t.cols_valid = static_cast<int>((p.N - t.n0) < BN ? (p.N - t.n0) : BN);
+  const int64_t cols = p.N - t.n0;
+  t.cols_valid = static_cast<int>(cols <= 0 ? 0 : (cols < t.width ? cols : t.width));
   return t;
 }
 
@@ -747,6 +762,7 @@ __device__ DuoTile duo_tile_grouped(const Params& p, const DuoSeg* seg, int64_t 
   t.mt = 0;
   t.sfb_tile = 0;
   t.sfb_shift = static_cast<int>((t.n0 % 128) / 32);
+  t.width = BN;
   t.live = true;
   return t;
 }
@@ -883,7 +899,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
                             static_cast<int32_t>(t.n0 + crank * (BN / 2)), t.b_z, bar);
           else
             tma_load_2d_2sm(smem + D::kOffB + s * D::kBBytes, &map_b, kx,
-                            static_cast<int32_t>(t.n0 + crank * (BN / 2)), bar);
+                            static_cast<int32_t>(t.n0 + crank * (t.width / 2)), bar);
           if constexpr (kMode == kDense) {
             tma_load_3d_2sm(smem + D::kOffSfa + s * D::kSfaBytes, &map_sfa, 0,
                             static_cast<int32_t>(kb), static_cast<int32_t>(t.mt), bar);
@@ -925,6 +941,8 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     const uint64_t sfb_desc0 = smem_desc(smem_u32(smem + D::kOffSfb), 0, 128, 0);
     constexpr uint32_t kId0 = mxf8_idesc(2 * BM, BN, 0, 0), kId1 = mxf8_idesc(2 * BM, BN, 1, 1);
     constexpr uint32_t kId2 = mxf8_idesc(2 * BM, BN, 2, 2), kId3 = mxf8_idesc(2 * BM, BN, 3, 3);
+    // half tiles: N = BN / 2, the same B scale bytes (their columns start at a 128-row tile)
+    constexpr uint32_t kHalfN = mxf8_idesc(2 * BM, BN / 2, 0, 0) ^ kId0;
     for (int64_t id = first_id; ok; id += id_step) {
       const DuoTile t = duo_tile_of<BN, kMode>(p, seg, id, crank);
       if (!t.live) break;
@@ -937,6 +955,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
       tc_fence_after();
       const uint32_t d_t = tmem + buf * BN;
       const uint32_t shift = static_cast<uint32_t>(t.sfb_shift);
+      const uint32_t nx = t.width == BN ? 0u : kHalfN;  // flips the N field to BN / 2
       for (int64_t kb = 0; kb < t.nk; ++kb, ++it) {
         const uint32_t s = it % kStages, ph = (it / kStages) & 1;
         if (!warp_wait(&full[s], ph, abort_flag, p.wait_ns)) { ok = false; break; }
@@ -953,14 +972,14 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
           tmem_cp_32x128b_x4_2sm(sfb_slot, sbd);
           tmem_cp_32x128b_x4_2sm(sfb_slot + 4, sbd + 512 / 16);
           if (kb != t.nk - 1 || t.last_blocks == 4) {
-            mma_mxf8_2sm(d_t, ad, bd, kId0, sfa_t, sfb_t, acc0);
-            mma_mxf8_2sm(d_t, ad + 2, bd + 2, kId1, sfa_t, sfb_t, 1u);
-            mma_mxf8_2sm(d_t, ad + 4, bd + 4, kId2, sfa_t, sfb_t, 1u);
-            mma_mxf8_2sm(d_t, ad + 6, bd + 6, kId3, sfa_t, sfb_t, 1u);
+            mma_mxf8_2sm(d_t, ad, bd, kId0 ^ nx, sfa_t, sfb_t, acc0);
+            mma_mxf8_2sm(d_t, ad + 2, bd + 2, kId1 ^ nx, sfa_t, sfb_t, 1u);
+            mma_mxf8_2sm(d_t, ad + 4, bd + 4, kId2 ^ nx, sfa_t, sfb_t, 1u);
+            mma_mxf8_2sm(d_t, ad + 6, bd + 6, kId3 ^ nx, sfa_t, sfb_t, 1u);
           } else {
             for (int k = 0; k < t.last_blocks; ++k)
-              mma_mxf8_2sm(d_t, ad + 2 * k, bd + 2 * k, mxf8_idesc(2 * BM, BN, k, k), sfa_t,
-                           sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
+              mma_mxf8_2sm(d_t, ad + 2 * k, bd + 2 * k, mxf8_idesc(2 * BM, BN, k, k) ^ nx,
+                           sfa_t, sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit_2sm_mc(&empty[s], 0x3);
         }
@@ -1292,12 +1311,22 @@ bool duo_enabled() {
   return on;
 }
 
+// Half-width tiles for the last wave of the 256-wide 2SM kernel; MXFP8_GEMM_HALF_TAIL=0
+// turns them off.
+bool half_tail_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("MXFP8_GEMM_HALF_TAIL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
 // Tile width of the 2SM kernel for one problem. A 256-wide tile does 4/3 the work of a
 // 192-wide one in about the same stage time, but tile counts that leave the last wave of
 // clusters nearly empty waste up to a sixth of the launch; 192 is taken when its fuller
 // last wave outweighs the narrower tile: 0.75 x wave efficiency(192) > 0.85 x wave
-// efficiency(256) (the factor was fitted on the Qwen3-8B layer shapes). MXFP8_GEMM_BN=256
-// or 192 forces a width.
+// efficiency(256) (the factor was fitted on the Qwen3-8B layer shapes), where a last wave
+// of 256-wide half tiles counts as half a wave. MXFP8_GEMM_BN=256 or 192 forces a width.
 int duo_width(int64_t M, int64_t N) {
   static const int forced = [] {
     const char* e = getenv("MXFP8_GEMM_BN");
@@ -1305,11 +1334,14 @@ int duo_width(int64_t M, int64_t N) {
     return (w == 256 || w == 192) ? w : 0;
   }();
   if (forced) return forced;
-  const double clusters = static_cast<double>(num_sms() / 2);
+  const int64_t clusters = num_sms() / 2;
   auto eff = [&](int bn) {
-    const double tiles = static_cast<double>(((M + 255) / 256) * ((N + bn - 1) / bn));
-    const double waves = tiles / clusters;
-    return waves / std::ceil(waves);
+    const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
+    const int64_t full = tiles / clusters, tail = tiles % clusters;
+    double waves = static_cast<double>(full + (tail > 0 ? 1 : 0));
+    if (bn == 256 && half_tail_enabled() && tail > 0 && 2 * tail <= clusters)
+      waves -= 0.5;  // the last wave runs half-width tiles
+    return static_cast<double>(tiles) / static_cast<double>(clusters) / waves;
   };
   return 0.75 * eff(192) > 0.85 * eff(256) ? 192 : 256;
 }
@@ -1331,7 +1363,15 @@ int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
   const int64_t pair_tiles = static_cast<int64_t>((p.num_m_tiles + 1) / 2) * p.num_n_tiles;
   const int64_t fit = max_duo_clusters<BN>();
   if (fit <= 0) return MXFP8_ERR_CUDA;
-  const int64_t clusters = pair_tiles < fit ? pair_tiles : fit;
+  // The tiles of the last, partial wave run as half-width tiles when their halves still fit
+  // in one wave of clusters (256-wide tiles only).
+  int64_t items = pair_tiles;
+  const int64_t tail = pair_tiles % fit;
+  if (BN == 256 && half_tail_enabled() && tail > 0 && 2 * tail <= fit) {
+    p.split_from = pair_tiles - tail;
+    items = pair_tiles + tail;
+  }
+  const int64_t clusters = items < fit ? items : fit;
   if (clusters <= 0) return MXFP8_OK;
   auto k = mxfp8_gemm_2sm_kernel<BN, kDense>;
   cudaLaunchAttribute attr[1];

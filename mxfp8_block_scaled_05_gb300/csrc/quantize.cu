@@ -35,6 +35,7 @@ namespace {
 
 constexpr int kTile = 128;        // rows and columns of a CTA tile
 constexpr int kThreads = 256;
+constexpr int kTilePitch = kTile + 8;  // BF16 row pitch of the shared tile: 272 bytes
 constexpr int kMaxExperts = 1024; // grouped calls: experts scanned in shared memory
 
 // Expert segmentation of the token rows for grouped calls. Every CTA re-derives the
@@ -84,7 +85,18 @@ __device__ int find_expert(const Segments& s, int E, int t) {
 
 constexpr uint32_t kAbs2 = 0x7FFF7FFFu;  // clears both BF16 sign bits of a word
 
-// Per-half unsigned 16-bit maximum of two words.
+// Per-half maximum of |a| and |b| for two BF16 pairs, NaN winning over every number; the
+// sign bits of the result are meaningless (cleared by kAbs2 once per block). Compared with
+// clearing both signs and taking an unsigned 16-bit maximum this is one instruction instead
+// of three. A BF16 subnormal amax gives scale byte 0 whether or not it is flushed here.
+__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Per-half unsigned 16-bit maximum of two words: on sign-cleared BF16 bits, the exact
+// maximum magnitude, subnormals included (the block-wise FP32 scale depends on it).
 __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -118,14 +130,48 @@ __device__ __forceinline__ float inv_scale(uint32_t s) {
   return __uint_as_float((254u - s) << 23);
 }
 
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// Two elements given as FP32 bit patterns (lo first in memory order) -> 2 bytes: scaled
+// by one packed multiply (mul.rn.f32x2: IEEE single-precision products rounded to nearest,
+// exact for a power-of-two scale), then one RNE-saturating E4M3 conversion.
+__device__ __forceinline__ uint32_t e4m3x2_f32bits(uint32_t lo, uint32_t hi, uint64_t mul2) {
+  uint64_t x, y;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(lo), "r"(hi));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(x), "l"(mul2));
+  uint16_t c;
+  asm("{ .reg .f32 lo, hi; mov.b64 {lo, hi}, %1; cvt.rn.satfinite.e4m3x2.f32 %0, hi, lo; }"
+      : "=h"(c) : "l"(y));
+  return c;
+}
+
+__device__ __forceinline__ uint64_t splat2(float mul) {
+  uint64_t mul2;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(mul2) : "r"(__float_as_uint(mul)));
+  return mul2;
+}
 
 // Two BF16 pairs (4 elements, memory order lo(w0), hi(w0), lo(w1), hi(w1)) -> 4 bytes.
+// A BF16 value's FP32 bit pattern is its 16 bits shifted to the top half.
 __device__ __forceinline__ uint32_t e4m3x4(uint32_t w0, uint32_t w1, float mul) {
-  const uint32_t p0 = cvt_e4m3x2(bf16hi(w0) * mul, bf16lo(w0) * mul);
-  const uint32_t p1 = cvt_e4m3x2(bf16hi(w1) * mul, bf16lo(w1) * mul);
-  return p0 | (p1 << 16);
+  const uint64_t mul2 = splat2(mul);
+  return e4m3x2_f32bits(w0 << 16, w0 & 0xFFFF0000u, mul2) |
+         (e4m3x2_f32bits(w1 << 16, w1 & 0xFFFF0000u, mul2) << 16);
+}
+
+// One column of four consecutive rows of a two-column word pair -> 4 bytes: the low
+// halves (column c) or the high halves (column c + 1) of a0..a3, widened in place.
+template <bool kHigh>
+__device__ __forceinline__ uint32_t e4m3x4_col(uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, float mul) {
+  const uint64_t mul2 = splat2(mul);
+  auto f = [](uint32_t w) { return kHigh ? (w & 0xFFFF0000u) : (w << 16); };
+  return e4m3x2_f32bits(f(a0), f(a1), mul2) | (e4m3x2_f32bits(f(a2), f(a3), mul2) << 16);
+}
+
+// 32 bytes global store in one instruction (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&o)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               ::"l"(p), "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]),
+                 "r"(o[6]), "r"(o[7]) : "memory");
 }
 
 // The same 4 elements of a NaN/Inf block: 0x7F with each element's own sign. Blocks like
@@ -138,7 +184,10 @@ __device__ __forceinline__ uint32_t nan4(uint32_t w0, uint32_t w1) {
 
 // One CTA = one 128 x 128 BF16 tile (128 token rows x 128 columns). kRow: write the
 // row-wise copy (blocks along the columns); kCol: write the column-wise copy (blocks
-// along the rows, emitted transposed). With both, the input is read once.
+// along the rows, emitted transposed). With both, the input is read once, into a shared
+// tile whose rows are padded to 272 bytes: the row-wise pass (one thread per 32-block,
+// eight consecutive rows per eight lanes) and the column-wise pass (one word per row and
+// lane) then read it without bank conflicts.
 struct QOut {
   uint8_t* codes;
   uint8_t* scales;
@@ -162,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, kCol ? 6 : 1)
 quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t cols, QOut ro,
                      QOut co, const int32_t* __restrict__ offsets, int E, int rule,
                      int* status, const QJobs jobs) {
-  __shared__ __align__(16) uint16_t tile[kCol ? kTile : 1][kCol ? kTile : 8];
+  __shared__ __align__(16) uint16_t tile[kCol ? kTile : 1][kCol ? kTilePitch : 8];
   __shared__ __align__(16) uint8_t stile_r[512];
   __shared__ __align__(16) uint8_t stile_c[512];
   extern __shared__ __align__(16) uint8_t dyn[];  // Segments for grouped calls
@@ -250,19 +299,68 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
     }
   }
 
-  // ---- row-wise copy: the 4 lanes of a 32-block share amax
-  if (kRow) {
+  // ---- row-wise copy from the shared tile: one thread per 32-block (8 consecutive rows
+  // per 8 lanes, conflict-free with the padded pitch), 32 code bytes per thread
+  if (kRow && kCol) {
+    const int64_t s_cols = cols / 32;
+    const int w = t >> 5, l = t & 31;
+    const int b = l >> 3;
+    const bool block_ok = 32 * b < cols_valid;
+    const bool wide = (reinterpret_cast<uintptr_t>(ro.codes) & 31) == 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = 8 * w + (l & 7) + 64 * i;
+      const uint4* rp = reinterpret_cast<const uint4*>(&tile[r][32 * b]);
+      const uint4 x0 = rp[0], x1 = rp[1], x2 = rp[2], x3 = rp[3];
+      uint32_t m2 = max_abs_bf16x2(
+          max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(x0.x, x0.y), max_abs_bf16x2(x0.z, x0.w)),
+                         max_abs_bf16x2(max_abs_bf16x2(x1.x, x1.y), max_abs_bf16x2(x1.z, x1.w))),
+          max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(x2.x, x2.y), max_abs_bf16x2(x2.z, x2.w)),
+                         max_abs_bf16x2(max_abs_bf16x2(x3.x, x3.y), max_abs_bf16x2(x3.z, x3.w))));
+      m2 &= kAbs2;
+      const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+      const bool valid = block_ok && r < rows_valid;
+      const uint32_t s = scale_byte(m, rule);
+      if (valid) {
+        uint32_t o[8];
+        if (__builtin_expect(s != 0xFFu, 1)) {
+          const float mul = inv_scale(s);
+          o[0] = e4m3x4(x0.x, x0.y, mul); o[1] = e4m3x4(x0.z, x0.w, mul);
+          o[2] = e4m3x4(x1.x, x1.y, mul); o[3] = e4m3x4(x1.z, x1.w, mul);
+          o[4] = e4m3x4(x2.x, x2.y, mul); o[5] = e4m3x4(x2.z, x2.w, mul);
+          o[6] = e4m3x4(x3.x, x3.y, mul); o[7] = e4m3x4(x3.z, x3.w, mul);
+        } else {
+          o[0] = nan4(x0.x, x0.y); o[1] = nan4(x0.z, x0.w);
+          o[2] = nan4(x1.x, x1.y); o[3] = nan4(x1.z, x1.w);
+          o[4] = nan4(x2.x, x2.y); o[5] = nan4(x2.z, x2.w);
+          o[6] = nan4(x3.x, x3.y); o[7] = nan4(x3.z, x3.w);
+        }
+        uint8_t* dst = ro.codes + (row0 + r) * cols + col0 + 32 * b;
+        if (wide) {
+          st_global_v8(dst, o);
+        } else {
+          reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+      }
+      if (kSwizzled)
+        stile_r[(r & 31) * 16 + (r >> 5) * 4 + b] = valid ? static_cast<uint8_t>(s) : 0;
+      else if (valid)
+        ro.scales[(row0 + r) * s_cols + col0 / 32 + b] = static_cast<uint8_t>(s);
+    }
+  }
+
+  // ---- row-wise copy from registers: the 4 lanes of a 32-block share amax
+  if (kRow && !kCol) {
     const int64_t s_cols = cols / 32;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int r = rsub + 16 * j;
-      uint4 xv;
-      if constexpr (kCol) xv = *reinterpret_cast<const uint4*>(&tile[r][8 * v]);
-      else xv = x[j];
-      uint32_t m2 = max_u16x2(max_u16x2(xv.x & kAbs2, xv.y & kAbs2),
-                              max_u16x2(xv.z & kAbs2, xv.w & kAbs2));
-      m2 = max_u16x2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 1));
-      m2 = max_u16x2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 2));
+      const uint4 xv = x[j];
+      uint32_t m2 = max_abs_bf16x2(max_abs_bf16x2(xv.x, xv.y), max_abs_bf16x2(xv.z, xv.w));
+      m2 = max_abs_bf16x2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 1));
+      m2 = max_abs_bf16x2(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, 2));
+      m2 &= kAbs2;
       const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
       const bool valid = col_ok && r < rows_valid;
       const uint32_t s = scale_byte(m, rule);
@@ -298,10 +396,11 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
     const int c = 2 * cp;
     const bool valid = c < cols_valid && 32 * j < rows_valid;
     const uint32_t* colw = reinterpret_cast<const uint32_t*>(&tile[32 * j][c]);
-    constexpr int kRowWords = kTile / 2;
+    constexpr int kRowWords = kTilePitch / 2;
     uint32_t m01 = 0;  // both columns' block maxima, one per half
 #pragma unroll
-    for (int i = 0; i < 32; ++i) m01 = max_u16x2(m01, colw[i * kRowWords] & kAbs2);
+    for (int i = 0; i < 32; ++i) m01 = max_abs_bf16x2(m01, colw[i * kRowWords]);
+    m01 &= kAbs2;
     const uint32_t s0 = scale_byte(m01 & 0xFFFFu, rule), s1 = scale_byte(m01 >> 16, rule);
     uint4 stage_o0[2], stage_o1[2];
     if (valid) {
@@ -313,8 +412,8 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
           const uint32_t a0 = colw[(4 * q) * kRowWords], a1 = colw[(4 * q + 1) * kRowWords];
           const uint32_t a2 = colw[(4 * q + 2) * kRowWords], a3 = colw[(4 * q + 3) * kRowWords];
           // column c: low halves; column c+1: high halves
-          o0[q] = e4m3x4(__byte_perm(a0, a1, 0x5410), __byte_perm(a2, a3, 0x5410), mul0);
-          o1[q] = e4m3x4(__byte_perm(a0, a1, 0x7632), __byte_perm(a2, a3, 0x7632), mul1);
+          o0[q] = e4m3x4_col<false>(a0, a1, a2, a3, mul0);
+          o1[q] = e4m3x4_col<true>(a0, a1, a2, a3, mul1);
         }
       } else {  // a NaN/Inf block in either column (rare)
 #pragma unroll
@@ -443,13 +542,8 @@ blockwise_quantize_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_
     if (!col_ok || r >= rows_valid) continue;
     uint2 o;
     if (!nan_block) {
-      const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
-      uint32_t b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        b[i] = cvt_e4m3x2(__fmul_rn(bf16hi(w[i]), f), __fmul_rn(bf16lo(w[i]), f));
-      o.x = b[0] | (b[1] << 16);
-      o.y = b[2] | (b[3] << 16);
+      o.x = e4m3x4(x[j].x, x[j].y, f);
+      o.y = e4m3x4(x[j].z, x[j].w, f);
     } else {
       o.x = nan4(x[j].x, x[j].y);
       o.y = nan4(x[j].z, x[j].w);

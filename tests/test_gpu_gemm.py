@@ -51,7 +51,8 @@ def test_tiny_config_fprop(m):
 @pytest.mark.parametrize("mnk", [(128, 128, 32), (128, 128, 128), (144, 272, 96), (256, 256, 256),
                                  (16, 16, 32), (400, 528, 1056), (2048, 4096, 256),
                                  (512, 384, 4096), (1040, 112, 160), (1040, 272, 160),
-                                 (384, 512, 256), (128, 512, 256), (4224, 2304, 128)])
+                                 (384, 512, 256), (128, 512, 256), (4224, 2304, 128),
+                                 (2304, 2560, 256)])
 def test_shapes_random_operands(m, mnk):
     """Random finite codes and scales spanning 2^-17..2^12: any mistake in the scale
     layout, a tile origin or a tail mask shows up as a gross error."""

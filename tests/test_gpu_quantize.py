@@ -236,6 +236,28 @@ def test_dual_equals_both_axes(m, shape, layout):
     np.testing.assert_array_equal(u8(cs).reshape(-1), _expect_scales(ocs, layout))
 
 
+@pytest.mark.parametrize("offset", [16, 48])
+def test_dual_row_codes_at_16_byte_offsets(m, offset):
+    """The row-wise codes leave in 32-byte stores when their buffer is 32-byte aligned and
+    in 16-byte stores otherwise: the same oracle bytes at a 16-byte but not 32-byte aligned
+    address, with the bytes around the output untouched."""
+    shape = (160, 4128)
+    x = _rand_bf16(np.random.default_rng(offset), shape)
+    n = shape[0] * shape[1]
+    buf = torch.full((n + 2 * offset,), 0xA5, dtype=torch.uint8, device=DEV)
+    row_out = buf[offset:offset + n].view(shape)
+    assert row_out.data_ptr() % 32 == 16
+    rq, rs, cq, cs = m.quantize_dual(x.to(DEV), O.SWIZZLED, row_out=row_out)
+    orq, ors = O.quantize(bf16_bits(x), O.ROW)
+    ocq, ocs = O.quantize(bf16_bits(x), O.COL)
+    np.testing.assert_array_equal(u8(rq), orq)
+    np.testing.assert_array_equal(u8(cq), ocq)
+    np.testing.assert_array_equal(u8(rs).reshape(-1), _expect_scales(ors, O.SWIZZLED))
+    np.testing.assert_array_equal(u8(cs).reshape(-1), _expect_scales(ocs, O.SWIZZLED))
+    rest = u8(buf)
+    assert np.all(rest[:offset] == 0xA5) and np.all(rest[offset + n:] == 0xA5)
+
+
 @pytest.mark.parametrize("layout", [O.LINEAR, O.SWIZZLED])
 def test_multi_job_launch_equals_separate_calls(m, layout):
     """Several tensors in one launch: the oracle's bytes for a small job, and byte equality
