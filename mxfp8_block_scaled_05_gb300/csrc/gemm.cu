@@ -603,15 +603,24 @@ struct DuoSeg {
   int ok;
 };
 
+// BN = 384 (dense, BF16 output): each K step issues two N = 192 MMAs that share the A
+// stage, into accumulator columns [0, 192) and [192, 384); each CTA stages two 96-row B
+// boxes (rows 96c.. and 192 + 96c.. of the pair tile). Fewer staged bytes and scale copies
+// per FLOP than a 256-wide tile, and fewer tiles to hand over per launch.
 template <int BN, int kMode = kDense>
 struct Duo {
   static constexpr bool kGrouped = kMode != kDense;
-  static constexpr int kAcc = BN == 256 ? 1 : 2;       // accumulator buffers
-  static constexpr int kStages = BN == 256 ? 6 : (kGrouped ? 6 : 7);
+  static constexpr bool kWide = BN == 384;
+  static_assert(!kWide || !kGrouped, "384-wide tiles are dense only");
+  static constexpr int kMmaN = kWide ? 192 : BN;       // N of one MMA instruction
+  static constexpr int kBoxRows = kWide ? 96 : BN / 2; // B rows per TMA box
+  static constexpr int kAcc = BN == 192 ? 2 : 1;       // accumulator buffers
+  static constexpr int kStages = BN == 256 ? 6 : (kWide ? 5 : (kGrouped ? 6 : 7));
   static constexpr int kABytes = BM * BK;              // own 128 A rows
   static constexpr int kBBytes = (BN / 2) * BK;        // own half of the B tile
   static constexpr int kSfaBytes = 512;
-  static constexpr int kSfbBytes = 1024;               // two 128-row scale tiles of B
+  static constexpr int kSfbTiles = kWide ? 3 : 2;      // 128-row scale tiles of B per stage
+  static constexpr int kSfbBytes = 512 * kSfbTiles;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
@@ -620,14 +629,16 @@ struct Duo {
   static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
   static constexpr int kNumBars = 2 * kStages + 2 * kAcc + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  // epilogue staging: one 32-row x 64-byte box (2 KB) per epilogue warp, 1024-aligned
-  static constexpr int kStageBoxBytes = 32 * 64;
+  // epilogue staging: one 32-row box per epilogue warp, 1024-aligned; 64-byte rows, or
+  // 32-byte rows for 384-wide tiles (which leave less shared memory)
+  static constexpr int kBoxRowBytes = kWide ? 32 : 64;
+  static constexpr int kStageBoxBytes = 32 * kBoxRowBytes;
   static constexpr int kOffOut = (kOffMisc + 64 + 1023) / 1024 * 1024;
   static constexpr int kOffSeg = kOffOut + kEpiWarps * kStageBoxBytes;
   static constexpr int kSmemBytes =
       kOffSeg + (kGrouped ? static_cast<int>(sizeof(DuoSeg)) : 0) + 1024;
   static constexpr int kSfaCol = kAcc * BN;            // TMEM: accumulators, then scales
-  static constexpr int kSfbSlot = 8;                   // columns per B scale slot
+  static constexpr int kSfbSlot = 4 * kSfbTiles;       // columns per B scale slot
   static constexpr int kSfbCol = kSfaCol + 4 * kStages;
   static constexpr int kTmemCols = 512;
   static constexpr int kAccEmptyCount = 2 * kEpiWarps;  // epilogue warps of both CTAs
@@ -897,9 +908,17 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
           if constexpr (kMode == kGroupRows)
             tma_load_3d_2sm(smem + D::kOffB + s * D::kBBytes, &map_b, kx,
                             static_cast<int32_t>(t.n0 + crank * (BN / 2)), t.b_z, bar);
-          else
+          else if constexpr (D::kWide) {
+            // rows 96c.. of each 192-column half of the pair tile (a half tile uses the
+            // first box only; the second is loaded all the same, as the byte count expects)
+            uint8_t* bs = smem + D::kOffB + s * D::kBBytes;
+            tma_load_2d_2sm(bs, &map_b, kx, static_cast<int32_t>(t.n0 + 96 * crank), bar);
+            tma_load_2d_2sm(bs + 96 * BK, &map_b, kx,
+                            static_cast<int32_t>(t.n0 + 192 + 96 * crank), bar);
+          } else {
             tma_load_2d_2sm(smem + D::kOffB + s * D::kBBytes, &map_b, kx,
                             static_cast<int32_t>(t.n0 + crank * (t.width / 2)), bar);
+          }
           if constexpr (kMode == kDense) {
             tma_load_3d_2sm(smem + D::kOffSfa + s * D::kSfaBytes, &map_sfa, 0,
                             static_cast<int32_t>(kb), static_cast<int32_t>(t.mt), bar);
@@ -939,10 +958,12 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     const uint64_t b_desc0 = smem_desc(smem_u32(smem + D::kOffB), 16, 1024, 2);
     const uint64_t sfa_desc0 = smem_desc(smem_u32(smem + D::kOffSfa), 0, 128, 0);
     const uint64_t sfb_desc0 = smem_desc(smem_u32(smem + D::kOffSfb), 0, 128, 0);
-    constexpr uint32_t kId0 = mxf8_idesc(2 * BM, BN, 0, 0), kId1 = mxf8_idesc(2 * BM, BN, 1, 1);
-    constexpr uint32_t kId2 = mxf8_idesc(2 * BM, BN, 2, 2), kId3 = mxf8_idesc(2 * BM, BN, 3, 3);
-    // half tiles: N = BN / 2, the same B scale bytes (their columns start at a 128-row tile)
-    constexpr uint32_t kHalfN = mxf8_idesc(2 * BM, BN / 2, 0, 0) ^ kId0;
+    constexpr int kN = D::kMmaN;
+    constexpr uint32_t kId0 = mxf8_idesc(2 * BM, kN, 0, 0), kId1 = mxf8_idesc(2 * BM, kN, 1, 1);
+    constexpr uint32_t kId2 = mxf8_idesc(2 * BM, kN, 2, 2), kId3 = mxf8_idesc(2 * BM, kN, 3, 3);
+    // half tiles of the 256-wide kernel: N = 128, the same B scale bytes (their columns
+    // start at a 128-row tile); a 384-wide kernel's half tile is its first MMA alone
+    constexpr uint32_t kHalfN = D::kWide ? 0u : (mxf8_idesc(2 * BM, BN / 2, 0, 0) ^ kId0);
     for (int64_t id = first_id; ok; id += id_step) {
       const DuoTile t = duo_tile_of<BN, kMode>(p, seg, id, crank);
       if (!t.live) break;
@@ -956,6 +977,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
       const uint32_t d_t = tmem + buf * BN;
       const uint32_t shift = static_cast<uint32_t>(t.sfb_shift);
       const uint32_t nx = t.width == BN ? 0u : kHalfN;  // flips the N field to BN / 2
+      const bool second = D::kWide && t.width == BN;     // the columns [192, 384) too
       for (int64_t kb = 0; kb < t.nk; ++kb, ++it) {
         const uint32_t s = it % kStages, ph = (it / kStages) & 1;
         if (!warp_wait(&full[s], ph, abort_flag, p.wait_ns)) { ok = false; break; }
@@ -971,15 +993,30 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
           tmem_cp_32x128b_x4_2sm(sfa_t, sfa_desc0 + s * (D::kSfaBytes / 16));
           tmem_cp_32x128b_x4_2sm(sfb_slot, sbd);
           tmem_cp_32x128b_x4_2sm(sfb_slot + 4, sbd + 512 / 16);
+          if constexpr (D::kWide) tmem_cp_32x128b_x4_2sm(sfb_slot + 8, sbd + 1024 / 16);
+          // 384-wide: the second MMA's B rows start 96 rows into the stage, its scales 192
+          // rows into the slot (column 6: 64 rows into the second scale tile)
+          const uint64_t bd2 = bd + (96 * BK) / 16;
+          const uint32_t d_t2 = d_t + 192, sfb_t2 = sfb_slot + 6;
           if (kb != t.nk - 1 || t.last_blocks == 4) {
             mma_mxf8_2sm(d_t, ad, bd, kId0 ^ nx, sfa_t, sfb_t, acc0);
             mma_mxf8_2sm(d_t, ad + 2, bd + 2, kId1 ^ nx, sfa_t, sfb_t, 1u);
             mma_mxf8_2sm(d_t, ad + 4, bd + 4, kId2 ^ nx, sfa_t, sfb_t, 1u);
             mma_mxf8_2sm(d_t, ad + 6, bd + 6, kId3 ^ nx, sfa_t, sfb_t, 1u);
+            if (second) {
+              mma_mxf8_2sm(d_t2, ad, bd2, kId0, sfa_t, sfb_t2, acc0);
+              mma_mxf8_2sm(d_t2, ad + 2, bd2 + 2, kId1, sfa_t, sfb_t2, 1u);
+              mma_mxf8_2sm(d_t2, ad + 4, bd2 + 4, kId2, sfa_t, sfb_t2, 1u);
+              mma_mxf8_2sm(d_t2, ad + 6, bd2 + 6, kId3, sfa_t, sfb_t2, 1u);
+            }
           } else {
             for (int k = 0; k < t.last_blocks; ++k)
-              mma_mxf8_2sm(d_t, ad + 2 * k, bd + 2 * k, mxf8_idesc(2 * BM, BN, k, k) ^ nx,
+              mma_mxf8_2sm(d_t, ad + 2 * k, bd + 2 * k, mxf8_idesc(2 * BM, kN, k, k) ^ nx,
                            sfa_t, sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
+            if (second)
+              for (int k = 0; k < t.last_blocks; ++k)
+                mma_mxf8_2sm(d_t2, ad + 2 * k, bd2 + 2 * k, mxf8_idesc(2 * BM, kN, k, k), sfa_t,
+                             sfb_t2, (kb > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit_2sm_mc(&empty[s], 0x3);
         }
@@ -1012,6 +1049,69 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     for (int64_t id = first_id; ok; id += id_step) {
       const DuoTile t = duo_tile_of<BN, kMode>(p, seg, id, crank);
       if (!t.live) break;
+      if constexpr (D::kWide) {
+        // 384-wide (BF16 out): 6 chunks of 32 columns per warp, converted to BF16 pairs as
+        // they leave TMEM in 3 rounds of 2 chunks, so that the accumulator is handed back
+        // before any store; then 32-byte boxes (16 columns) with the 32-byte swizzle.
+        uint32_t b[6][16];
+        if (t.nk > 0) {
+          const uint32_t aph = acc_it & 1;
+          int got = 0;
+          if (lane == 0) got = mbar_wait_bounded(&acc_full[0], aph, abort_flag, p.wait_ns);
+          got = __shfl_sync(0xFFFFFFFFu, got, 0);
+          if (!got) { ok = false; break; }
+          tc_fence_after();
+          __syncwarp();
+          const uint32_t base = tmem + (static_cast<uint32_t>(32 * q) << 16) + half * 192;
+#pragma unroll
+          for (int r = 0; r < 3; ++r) {
+            uint32_t v[2][32];
+            tmem_ld_32x32b_x32(base + 64 * r, v[0]);
+            tmem_ld_32x32b_x32(base + 64 * r + 32, v[1]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                b[2 * r + u][i] = cvt_bf16x2(__uint_as_float(v[u][2 * i + 1]),
+                                             __uint_as_float(v[u][2 * i]));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty0);
+          ++acc_it;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 6; ++c)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) b[c][i] = 0;
+        }
+        if (32 * q < t.rows_valid) {
+          const int sw = (lane >> 2) & 1;
+#pragma unroll
+          for (int c6 = 0; c6 < 6; ++c6) {
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              const int col = 32 * (half * 6 + c6) + 16 * g;  // first column of this box
+              if (col >= t.cols_valid) continue;
+              if (lane == 0) bulk_wait_read_all();  // the box is free again
+              __syncwarp();
+              *reinterpret_cast<uint4*>(box + lane * 32 + 16 * sw) =
+                  make_uint4(b[c6][8 * g], b[c6][8 * g + 1], b[c6][8 * g + 2], b[c6][8 * g + 3]);
+              *reinterpret_cast<uint4*>(box + lane * 32 + 16 * (sw ^ 1)) =
+                  make_uint4(b[c6][8 * g + 4], b[c6][8 * g + 5], b[c6][8 * g + 6], b[c6][8 * g + 7]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&map_c, box, static_cast<int32_t>(t.n0 + col),
+                             static_cast<int32_t>(t.m0 + 32 * q));
+                bulk_commit_group();
+              }
+            }
+          }
+        }
+        continue;
+      }
       // The whole slice goes to registers and TMEM is handed back before any store.
       uint32_t v[kChunks][32];
       if (t.nk > 0) {
@@ -1247,9 +1347,9 @@ bool make_sf_map(CUtensorMap* map, const void* base, int64_t row_tiles, int64_t 
 }
 
 // The output C [Z][rows][N] (BF16 or FP32; rank 2 when Z == 1 and rank == 2) for TMA
-// stores of 32-row x 64-byte boxes with the 64-byte swizzle.
+// stores of 32-row boxes of `row_bytes` (64 or 32) with the swizzle of the same width.
 bool make_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t N, int64_t Z, bool fp32,
-                  int rank) {
+                  int rank, uint32_t row_bytes = 64) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const uint32_t elem = fp32 ? 4 : 2;
@@ -1257,11 +1357,12 @@ bool make_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t N, int64_t
                         static_cast<cuuint64_t>(Z)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * elem,
                            static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(rows) * elem};
-  cuuint32_t box[3] = {64 / elem, 32, 1};
+  cuuint32_t box[3] = {row_bytes / elem, 32, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
             static_cast<cuuint32_t>(rank), base, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            row_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1311,8 +1412,17 @@ bool duo_enabled() {
   return on;
 }
 
-// Half-width tiles for the last wave of the 256-wide 2SM kernel; MXFP8_GEMM_HALF_TAIL=0
-// turns them off.
+// 384-wide tiles for dense BF16-output GEMMs; MXFP8_GEMM_WIDE=0 turns them off.
+bool wide_tiles_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("MXFP8_GEMM_WIDE");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
+// Half-width tiles for the last wave of the 256- and 384-wide 2SM kernel;
+// MXFP8_GEMM_HALF_TAIL=0 turns them off.
 bool half_tail_enabled() {
   static const bool on = [] {
     const char* e = getenv("MXFP8_GEMM_HALF_TAIL");
@@ -1321,29 +1431,39 @@ bool half_tail_enabled() {
   return on;
 }
 
-// Tile width of the 2SM kernel for one problem. A 256-wide tile does 4/3 the work of a
-// 192-wide one in about the same stage time, but tile counts that leave the last wave of
-// clusters nearly empty waste up to a sixth of the launch; 192 is taken when its fuller
-// last wave outweighs the narrower tile: 0.75 x wave efficiency(192) > 0.85 x wave
-// efficiency(256) (the factor was fitted on the Qwen3-8B layer shapes), where a last wave
-// of 256-wide half tiles counts as half a wave. MXFP8_GEMM_BN=256 or 192 forces a width.
-int duo_width(int64_t M, int64_t N) {
+// Tile width of the 2SM kernel for one problem: 192, 256 or 384 (BF16 output only), the
+// one with the least estimated time. A tile's time per K stage relative to a 256-wide tile,
+// as measured on GB300 (narrow tiles pay the per-stage scale copies and fills over fewer
+// FLOPs; the 384-wide tile, two MMAs sharing A, is slightly cheaper per FLOP): 192 -> 0.78,
+// 256 -> 1, 384 -> 1.46; a last wave of half tiles costs 0.93 (256) or 0.78 (384, two
+// 192-wide halves). MXFP8_GEMM_BN=192, 256 or 384 forces a width.
+int duo_width(int64_t M, int64_t N, bool fp32) {
   static const int forced = [] {
     const char* e = getenv("MXFP8_GEMM_BN");
     const int w = e ? atoi(e) : 0;
-    return (w == 256 || w == 192) ? w : 0;
+    return (w == 256 || w == 192 || w == 384) ? w : 0;
   }();
-  if (forced) return forced;
+  if (forced && !(forced == 384 && fp32)) return forced;
   const int64_t clusters = num_sms() / 2;
-  auto eff = [&](int bn) {
+  auto cost = [&](int bn) {
+    const double full = bn == 192 ? 0.78 : (bn == 256 ? 1.0 : 1.46);
+    const double halfc = bn == 256 ? 0.93 : 0.78;
     const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
-    const int64_t full = tiles / clusters, tail = tiles % clusters;
-    double waves = static_cast<double>(full + (tail > 0 ? 1 : 0));
-    if (bn == 256 && half_tail_enabled() && tail > 0 && 2 * tail <= clusters)
-      waves -= 0.5;  // the last wave runs half-width tiles
-    return static_cast<double>(tiles) / static_cast<double>(clusters) / waves;
+    const int64_t waves = tiles / clusters, tail = tiles % clusters;
+    double t = static_cast<double>(waves) * full;
+    if (tail > 0)
+      t += (bn != 192 && half_tail_enabled() && 2 * tail <= clusters) ? halfc : full;
+    return t;
   };
-  return 0.75 * eff(192) > 0.85 * eff(256) ? 192 : 256;
+  int best = 256;
+  double best_t = cost(256);
+  const int others[2] = {192, 384};
+  for (int bn : others) {
+    if (bn == 384 && (fp32 || !wide_tiles_enabled())) continue;
+    const double t = cost(bn);
+    if (t < best_t) best = bn, best_t = t;
+  }
+  return best;
 }
 
 // Dense GEMM on CTA pairs with 256 x BN tiles (tcgen05 cta_group::2).
@@ -1353,10 +1473,12 @@ int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
   const int64_t n_kt = (a.K + BK - 1) / BK;
   CUtensorMap ma, mb, msa, msb, mc;
   if (!make_map(&ma, a.A, 2, a.K, a.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
-  if (!make_map(&mb, a.B, 2, a.K, a.N, 1, BK, BN / 2)) return MXFP8_ERR_CUDA;
-  if (!make_out_map(&mc, a.C, a.M, a.N, 1, a.out_dtype == MXFP8_OUT_FP32, 2)) return MXFP8_ERR_CUDA;
+  if (D::kWide && a.out_dtype == MXFP8_OUT_FP32) return MXFP8_ERR_INVALID_ARG;
+  if (!make_map(&mb, a.B, 2, a.K, a.N, 1, BK, D::kBoxRows)) return MXFP8_ERR_CUDA;
+  if (!make_out_map(&mc, a.C, a.M, a.N, 1, a.out_dtype == MXFP8_OUT_FP32, 2, D::kBoxRowBytes))
+    return MXFP8_ERR_CUDA;
   if (!make_sf_map(&msa, a.sA, (a.M + 127) / 128, n_kt, 1)) return MXFP8_ERR_CUDA;
-  if (!make_sf_map(&msb, a.sB, (a.N + 127) / 128, n_kt, 2)) return MXFP8_ERR_CUDA;
+  if (!make_sf_map(&msb, a.sB, (a.N + 127) / 128, n_kt, D::kSfbTiles)) return MXFP8_ERR_CUDA;
   p.num_n_tiles = static_cast<int>((a.N + BN - 1) / BN);
   p.num_tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
   p.band = (band_tiles(a.M, a.N, a.K, p.num_m_tiles) + 1) / 2;
@@ -1364,10 +1486,10 @@ int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
   const int64_t fit = max_duo_clusters<BN>();
   if (fit <= 0) return MXFP8_ERR_CUDA;
   // The tiles of the last, partial wave run as half-width tiles when their halves still fit
-  // in one wave of clusters (256-wide tiles only).
+  // in one wave of clusters (256- and 384-wide tiles).
   int64_t items = pair_tiles;
   const int64_t tail = pair_tiles % fit;
-  if (BN == 256 && half_tail_enabled() && tail > 0 && 2 * tail <= fit) {
+  if (BN != 192 && half_tail_enabled() && tail > 0 && 2 * tail <= fit) {
     p.split_from = pair_tiles - tail;
     items = pair_tiles + tail;
   }
@@ -1408,7 +1530,7 @@ int launch_duo_grouped(const GemmArgs& a, Params p, cudaStream_t stream) {
   if (kMode == kGroupWgrad) {
     // A = dY^T [M][T], B = X^T [N][T], both blocked along the tokens; C[e] = [M][N]
     if (!make_map(&ma, a.A, 2, T, p.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
-    if (!make_map(&mb, a.B, 2, T, p.N, 1, BK, BN / 2)) return MXFP8_ERR_CUDA;
+    if (!make_map(&mb, a.B, 2, T, p.N, 1, BK, D::kBoxRows)) return MXFP8_ERR_CUDA;
     if (!make_sf_flat_map(&msa, a.sA, ((p.M + 127) / 128) * seg_tiles)) return MXFP8_ERR_CUDA;
     if (!make_sf_flat_map(&msb, a.sB, ((p.N + 127) / 128) * seg_tiles)) return MXFP8_ERR_CUDA;
     if (!make_out_map(&mc, a.C, p.M, p.N, E, fp32, 3)) return MXFP8_ERR_CUDA;
@@ -1417,7 +1539,7 @@ int launch_duo_grouped(const GemmArgs& a, Params p, cudaStream_t stream) {
     // A = X [T][K] segmented by rows, B = W [E][N][K], C = [T][N]
     const int64_t n_kt = (p.K + BK - 1) / BK;
     if (!make_map(&ma, a.A, 2, p.K, T, 1, BK, BM)) return MXFP8_ERR_CUDA;
-    if (!make_map(&mb, a.B, 3, p.K, p.N, E, BK, BN / 2)) return MXFP8_ERR_CUDA;
+    if (!make_map(&mb, a.B, 3, p.K, p.N, E, BK, D::kBoxRows)) return MXFP8_ERR_CUDA;
     if (!make_sf_flat_map(&msa, a.sA, seg_tiles * n_kt)) return MXFP8_ERR_CUDA;
     if (!make_sf_flat_map(&msb, a.sB, E * ((p.N + 127) / 128) * n_kt)) return MXFP8_ERR_CUDA;
     if (!make_out_map(&mc, a.C, T, p.N, 1, fp32, 3)) return MXFP8_ERR_CUDA;
@@ -1470,8 +1592,11 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.num_tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
   p.band = band_tiles(a.M, a.N, a.K, p.num_m_tiles);
   if (wide && p.num_m_tiles >= 2 && duo_enabled())
-    return duo_width(a.M, a.N) == 256 ? launch_duo<256>(a, p, stream)
-                                      : launch_duo<192>(a, p, stream);
+    switch (duo_width(a.M, a.N, p.out_fp32 != 0)) {
+      case 384: return launch_duo<384>(a, p, stream);
+      case 192: return launch_duo<192>(a, p, stream);
+      default: return launch_duo<256>(a, p, stream);
+    }
   CUtensorMap ma, mb, mc;
   if (!make_map(&ma, a.A, 2, a.K, a.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
   if (!make_out_map(&mc, a.C, a.M, a.N, 1, p.out_fp32 != 0, 3)) return MXFP8_ERR_CUDA;
