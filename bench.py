@@ -430,7 +430,7 @@ def run_ours(args, rank, ws):
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
                      "traffic": traffic,
-                     "kernel": "mxfp8_gemm_2sm_kernel (12 launches per step; 256x256 or 256x192 tiles)",
+                     "kernel": "mxfp8_gemm_2sm_kernel (12 launches per step; 256x384, 256x256 or 256x192 tiles)",
                      "peak_note": f"{pk['src']} bf16 sustained {pk['bf16_sus']} x "
                                   f"{FP8_OVER_BF16} (nominal FP8:BF16 ratio)",
                      "flops_per_launch": g_units / g_launches},
