@@ -410,6 +410,11 @@ def run_ours(args, rank, ws):
     traffic = recorded_traffic("mxfp8_gemm")
     e2e = run_e2e(args, m, step, dev, stream, ws)
     graph_ms, eager_ms, host_ms = run_graph(m, step, stream, max(10, args.steps // 4))
+    cal = calibrate(dev)
+    # the end-to-end step cannot beat moving its bytes over the host link in both directions
+    link_ms = (e2e["h2d_bytes_per_step"] + e2e["d2h_bytes_per_step"]) / (cal["h2d+d2h_GB/s"] * 1e6)
+    e2e["host_link_bound_ms_per_step"] = link_ms
+    e2e["frac_of_host_link_bound"] = link_ms / e2e["ms_per_step"]
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
@@ -424,7 +429,8 @@ def run_ours(args, rank, ws):
                               if step.dual else "separate"),
                      "bytes_per_elem": DUAL_BYTES_PER_ELEM if step.dual else QBYTES_PER_ELEM,
                      "bytes_per_step": q_units / args.steps,
-                     "peak_GB/s": pk["hbm"], "peak_src": pk["src"]},
+                     "peak_GB/s": pk["hbm"], "peak_src": pk["src"],
+                     "frac_of_copy_this_run": quant_gbs / cal["d2d_GB/s"]},
         "gemm": {"TFLOP/s": gemm_tflops, "frac_of_mxfp8": gemm_tflops / fp8_peak,
                  "ms_per_step": g_ms / args.steps, "flops_per_step": step.flops},
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
@@ -437,6 +443,7 @@ def run_ours(args, rank, ws):
         "clocks": clk.summary(),
         "e2e": e2e,
         "per_launch": breakdown,
+        "calibration": cal,
         "cuda_graph": {"ms_per_step": graph_ms, "eager_ms_per_step": eager_ms,
                        "host_enqueue_ms_per_step": host_ms,
                        "value": ws * step.flops / (graph_ms * 1e-3) / 1e12, "unit": "TFLOP/s"},
@@ -444,6 +451,53 @@ def run_ours(args, rank, ws):
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline_obj()
         print(json.dumps(line), flush=True)
+
+
+def calibrate(dev, nbytes=512 << 20, reps=10):
+    """Copy bandwidths on this GPU in the same run: device to device (read + write bytes, the
+    HBM bound of the quantizer) and pinned host memory to and from the device, each way and
+    both at once (the bound of the end-to-end step). torch copies, CUDA events, buffers larger
+    than L2."""
+    a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    b = torch.empty_like(a)
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def timed_ms(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def both():
+        cur = torch.cuda.current_stream()
+        s1.wait_stream(cur)
+        s2.wait_stream(cur)
+        with torch.cuda.stream(s1):
+            b.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(a, non_blocking=True)
+        cur.wait_stream(s1)
+        cur.wait_stream(s2)
+
+    d2d = timed_ms(lambda: b.copy_(a))
+    h2d = timed_ms(lambda: b.copy_(h_in, non_blocking=True))
+    d2h = timed_ms(lambda: h_out.copy_(a, non_blocking=True))
+    bidir = timed_ms(both)
+    out = {"d2d_GB/s": 2 * nbytes / (d2d * 1e-3) / 1e9,
+           "h2d_GB/s": nbytes / (h2d * 1e-3) / 1e9,
+           "d2h_GB/s": nbytes / (d2h * 1e-3) / 1e9,
+           "h2d+d2h_GB/s": 2 * nbytes / (bidir * 1e-3) / 1e9,
+           "bytes": nbytes, "reps": reps}
+    del a, b, h_in, h_out
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, m, step, dev, stream, ws):
