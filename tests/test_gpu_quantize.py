@@ -222,10 +222,14 @@ def test_weight_sync_pass_byte_equality(m):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("shape", [(32, 32), (160, 96), (4096, 40 * 32), (288, 4128)])
+@pytest.mark.parametrize("shape", [(32, 32), (160, 96), (4096, 40 * 32), (288, 4128), (4096, 4096),
+                                   (4128, 3872)])
 @pytest.mark.parametrize("layout", [O.LINEAR, O.SWIZZLED])
 def test_dual_equals_both_axes(m, shape, layout):
-    """One read, both copies: identical to the oracle's row-wise and column-wise bytes."""
+    """One read, both copies: identical to the oracle's row-wise and column-wise bytes. The
+    two large shapes have more 128 x 128 tiles than resident CTAs, so their last wave runs
+    as 32-row strips (4128 rows: the last tile row has one strip of data and three of
+    padding, whose scale entries must still be zero)."""
     x = _rand_bf16(np.random.default_rng(shape[0] + shape[1]), shape)
     rq, rs, cq, cs = m.quantize_dual(x.to(DEV), layout)
     orq, ors = O.quantize(bf16_bits(x), O.ROW)
