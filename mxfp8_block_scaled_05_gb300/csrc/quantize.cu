@@ -229,7 +229,10 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
     cols = jobs.cols[j];
     ro = QOut{jobs.out[j], jobs.scales[j], 0};
     co = QOut{jobs.out_col[j], jobs.scales_col[j], 0};
-    const int64_t local = g - jobs.tile_base[j], n_ct = (cols + kTile - 1) / kTile;
+    // tile counts are below 2^31 (checked on the host): 32-bit division, far cheaper than
+    // the 64-bit one every thread would otherwise run
+    const uint32_t local = static_cast<uint32_t>(g - jobs.tile_base[j]);
+    const uint32_t n_ct = static_cast<uint32_t>((cols + kTile - 1) / kTile);
     by = local / n_ct;
     bx = local % n_ct;
     item = 0;
