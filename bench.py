@@ -11,10 +11,10 @@ the backward pass has it), each giving both copies from one read, and 3 GEMM lau
 of BF16 inputs) is larger than L2, so no flush is needed between steps.
 
 Output: one JSON line (rank 0). `value` is the step's MXFP8 GEMM FLOPs divided by the
-step time (quantization included), in TFLOP/s, with the step's 20 launches captured once
-in a CUDA graph and replayed K times (`eager` gives the same step issued launch by launch).
-The `quantize` and `gemm` objects split the time, from CUDA events around every launch of
-eager steps; `roofline` is for the dominant kernel (the GEMM).
+step time (quantization included), in TFLOP/s, with the step's 20 launches issued on one
+stream (`cuda_graph` gives the same step replayed from a CUDA graph). The `quantize` and
+`gemm` objects split the time, from CUDA events around every launch of further steps;
+`roofline` is for the dominant kernel (the GEMM).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --workload moe|sync|sweep     # the other configurations
@@ -373,18 +373,14 @@ def run_ours(args, rank, ws):
     if m.device_status() != m.OK:
         raise RuntimeError("device status set during warm-up")
 
-    # The step runs as one CUDA graph (its 20 launches captured once, replayed per step), as
-    # a training loop runs a captured micro-batch: no host dispatch between launches.
-    graph = capture_step(step, stream)
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
+    # The K timed steps: the 20 launches of each step issued on one stream, nothing else
+    # enqueued between them (the host stays ahead of the GPU).
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
         barrier(ws)
         start.record(stream)
         for _ in range(args.steps):
-            graph.replay()
+            step.run(stream)
         end.record(stream)
         barrier(ws)
     ms = start.elapsed_time(end)
@@ -393,8 +389,8 @@ def run_ours(args, rank, ws):
     if status != m.OK:
         raise RuntimeError(f"device status {status} after the timed region")
 
-    # The split between quantize and GEMM time, per launch: eager steps with CUDA events
-    # around every launch (the kernels are the ones the graph replays).
+    # The split between quantize and GEMM time, per launch: further steps with CUDA events
+    # around every launch.
     split_steps = max(10, args.steps // 4)
     events = []
     for _ in range(split_steps):
@@ -423,7 +419,7 @@ def run_ours(args, rank, ws):
     fp8_peak = pk["bf16_sus"] * FP8_OVER_BF16
     traffic = recorded_traffic("mxfp8_gemm")
     e2e = run_e2e(args, m, step, dev, stream, ws)
-    eager_ms, host_ms = run_eager(step, stream, split_steps)
+    graph_ms = run_graph(step, stream, split_steps)
     cal = calibrate(dev)
     # the end-to-end step cannot beat moving its bytes over the host link in both directions
     link_ms = (e2e["h2d_bytes_per_step"] + e2e["d2h_bytes_per_step"]) / (cal["h2d+d2h_GB/s"] * 1e6)
@@ -458,10 +454,10 @@ def run_ours(args, rank, ws):
         "e2e": e2e,
         "per_launch": breakdown,
         "calibration": cal,
-        "execution": "CUDA graph of one step (20 launches), captured once and replayed",
-        "eager": {"ms_per_step": eager_ms, "host_enqueue_ms_per_step": host_ms,
-                  "value": ws * step.flops / (eager_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                  "note": "the same launches issued one by one from the host"},
+        "execution": "20 launches per step issued on one stream",
+        "cuda_graph": {"ms_per_step": graph_ms,
+                       "value": ws * step.flops / (graph_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "note": "the same step captured once in a CUDA graph and replayed"},
     }
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline_obj()
@@ -596,19 +592,19 @@ def capture_step(step, stream):
     return graph
 
 
-def run_eager(step, stream, steps):
-    """The step issued launch by launch from the host; returns (ms per step, host ms to
-    enqueue one step)."""
+def run_graph(step, stream, steps):
+    """The step captured once in a CUDA graph and replayed `steps` times; ms per step."""
+    graph = capture_step(step, stream)
+    for _ in range(3):
+        graph.replay()
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0 = time.perf_counter()
     s.record(stream)
     for _ in range(steps):
-        step.run(stream)
-    host_ms = (time.perf_counter() - t0) * 1e3 / steps
+        graph.replay()
     e.record(stream)
     torch.cuda.synchronize()
-    return s.elapsed_time(e) / steps, host_ms
+    return s.elapsed_time(e) / steps
 
 def cpu_baseline_obj():
     budget, t0 = 15.0, time.perf_counter()
