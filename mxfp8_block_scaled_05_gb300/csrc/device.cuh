@@ -42,10 +42,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -287,12 +283,6 @@ __device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
   return r;
 }
 
-// Arrive on an mbarrier given by its shared::cluster address (possibly the peer CTA's).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
-               ::"r"(cluster_addr) : "memory");
-}
-
 // Relaxed arrives, for hand-backs that order no memory: the epilogue returns TMEM once
 // tcgen05.wait::ld has completed its reads, so nothing it wrote needs to be made visible
 // first (a release arrive would also wait on the warp's outstanding global stores).
@@ -407,14 +397,6 @@ __device__ __forceinline__ void mma_commit_2sm_mc(uint64_t* bar, uint16_t mask) 
 }
 
 // ------------------------------------------------------------------------- numerics
-
-// Two floats -> packed E4M3 pair, round to nearest even, saturating; `hi` lands in the
-// upper byte.
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 
 __device__ __forceinline__ uint32_t cvt_bf16x2(float hi, float lo) {
   uint32_t r;
