@@ -460,7 +460,8 @@ def run_ours(args, rank, ws):
                        "note": "the same step captured once in a CUDA graph and replayed"},
     }
     if rank == 0:
-        line["cpu_baseline"] = cpu_baseline_obj()
+        if ws == 1:  # the oracle baseline is timed at N = 1 only
+            line["cpu_baseline"] = cpu_baseline_obj()
         print(json.dumps(line), flush=True)
 
 
