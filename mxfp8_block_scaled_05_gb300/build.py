@@ -7,6 +7,7 @@ machine without a GPU; CUDA is only needed when a compute call runs).
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -53,20 +54,34 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
+def _fresh() -> bool:
+    return os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps()
+
+
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compiles and links libmxfp8.so if any source is newer than it; returns its path."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps():
+    """Compiles and links libmxfp8.so if any source is newer than it; returns its path.
+    Processes that build at once (the ranks of a multi-GPU launch) take turns under a file
+    lock, and a process that finds the library fresh once it holds the lock does not
+    rebuild it."""
+    if not force and _fresh():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    tmp = LIB + ".tmp"
-    cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and _fresh():
+                return LIB
+            with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+                objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
+            tmp = f"{LIB}.{os.getpid()}.tmp"
+            cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+            os.replace(tmp, LIB)
+            return LIB
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
 
 
 if __name__ == "__main__":
