@@ -7,15 +7,23 @@
 // and weight-gradient GEMMs per linear layer); expert GEMMs of Qwen3-30B-A3B: section
 // "A held-out workload, and end to end", Table 4.
 //
-// Kernel design (one persistent CTA per SM, warp-specialised):
-//   warp 0      TMA producer: per 128-wide K stage, one tiled load of the A tile
-//               (128 x 128 B) and of the B tile (BN x 128 B), both with the 128-byte
-//               swizzle, plus one 512-byte bulk copy per 128-row scale tile.
-//   warp 1      allocates TMEM; one thread copies the stage's scale tiles into TMEM
+// Kernel design: persistent CTAs, warp-specialised, 320 threads.
+//   warp 0      TMA producer: per 128-wide K stage, tiled loads of the A and B tiles with
+//               the 128-byte swizzle and of the stage's scale tiles; the whole warp runs
+//               the loop and one elected lane issues.
+//   warp 1      allocates TMEM; its elected lane copies the stage's scale tiles into TMEM
 //               (tcgen05.cp 32x128b.warpx4: a 512-byte swizzled tile lands as 4 TMEM
-//               columns, byte k of each column = K block k) and issues four
-//               128 x BN x 32 block-scaled MMAs into the FP32 accumulator in TMEM.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator, FP32 -> BF16/FP32, stores.
+//               columns, byte k of each column = K block k) and issues the stage's
+//               block-scaled MMAs (K = 32 each) into the FP32 accumulator in TMEM.
+//   warps 2-9   epilogue, two warps per TMEM lane quarter: tcgen05.ld of the accumulator,
+//               FP32 -> BF16 (or FP32), stores through shared memory with TMA.
+// Two kernels share this layout:
+//   mxfp8_gemm_2sm_kernel  clusters of two CTAs on two SMs compute 256 x BN tiles with
+//                          tcgen05.mma.cta_group::2: BN = 256, 192 (two accumulators) or
+//                          384 (two N = 192 MMAs sharing the A stage); the dense GEMMs
+//                          with N > 128 and the grouped GEMMs for up to 256 experts.
+//   mxfp8_gemm_kernel      one CTA per SM, 128 x 256 or 128 x 128 tiles (CTA pairs may
+//                          share B by TMA multicast); everything else.
 // Shared-memory stages are recycled through full/empty mbarriers; the accumulator
 // through acc_full/acc_empty, so the producer already streams the next tile's operands
 // while the epilogue drains the current one. Each stage has its own TMEM scale slot,

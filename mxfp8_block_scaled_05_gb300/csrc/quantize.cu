@@ -15,13 +15,18 @@
 // 128 x 4 blocks, i.e. one 512-byte swizzled scale tile, which the CTA assembles in
 // shared memory and stores with 16-byte writes.
 //
-// Block maxima are taken on the BF16 bits of two elements at once (|x| = bits & 0x7FFF,
-// compared as unsigned 16-bit pairs), which orders finite values, Inf and NaN correctly.
+// Block maxima are taken two elements at once: max.NaN.xorsign.abs.bf16x2 in the MXFP8
+// kernels (magnitudes compared, NaN wins; the sign bits are cleared once per block), and
+// unsigned 16-bit maxima of the sign-cleared bits in the block-wise kernel, whose FP32
+// scale needs the exact maximum even when it is subnormal.
 //
 // The block exponent is taken from the integer bits of the block's largest |BF16|
 // (biased exponent E): scale byte = max(E - 8, 0) (floor(log2 amax) - 8, clamped at
-// -127). Elements are multiplied by 2^-e - an exact power-of-two scaling in FP32 - and
-// converted with cvt.rn.satfinite.e4m3x2 (round to nearest even, saturating).
+// -127). Elements are widened to FP32, multiplied by 2^-e two at a time (mul.rn.f32x2,
+// an exact power-of-two scaling) and converted with cvt.rn.satfinite.e4m3x2 (round to
+// nearest even, saturating). The dual kernel's row pass gives each thread one 32-element
+// block and stores its 32 code bytes at once; the column pass reads column pairs from the
+// shared tile, whose rows are padded so that both passes are free of bank conflicts.
 
 #include <cstdint>
 #include <cuda_runtime.h>
