@@ -119,20 +119,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// 2-D tiled load multicast to every CTA of the cluster in `mask`: the box lands at the
-// same shared-memory offset in each, and completes its bytes on the mbarrier at the
-// same offset in each.
-__device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap* map,
-                                               int32_t x, int32_t y, uint64_t* bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;"
-      ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
-        "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map,
                                             int32_t x, int32_t y, int32_t z, uint64_t* bar) {
   asm volatile(
@@ -227,14 +213,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
       ::"r"(smem_u32(bar)) : "memory");
-}
-
-// As mma_commit, but arrives on the mbarrier at the same offset in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;"
-      ::"r"(smem_u32(bar)), "h"(mask) : "memory");
 }
 
 // Every thread of every CTA in the cluster; orders shared-memory (and barrier) state.

@@ -22,8 +22,8 @@
 //                          tcgen05.mma.cta_group::2: BN = 256, 192 (two accumulators) or
 //                          384 (two N = 192 MMAs sharing the A stage); the dense GEMMs
 //                          with N > 128 and the grouped GEMMs for up to 256 experts.
-//   mxfp8_gemm_kernel      one CTA per SM, 128 x 256 or 128 x 128 tiles (CTA pairs may
-//                          share B by TMA multicast); everything else.
+//   mxfp8_gemm_kernel      one CTA per SM, 128 x 256 or 128 x 128 tiles; everything else.
+// No load is multicast across a cluster: every CTA loads its own operand tiles.
 // Shared-memory stages are recycled through full/empty mbarriers; the accumulator
 // through acc_full/acc_empty, so the producer already streams the next tile's operands
 // while the epilogue drains the current one. Each stage has its own TMEM scale slot,
@@ -97,7 +97,7 @@ struct Params {
   int64_t sb_item_bytes; // grouped rows: bytes of one expert's B scale block
   int64_t num_tiles;     // dense: all tiles; grouped: upper bound
   int num_m_tiles, num_n_tiles;
-  int band;              // dense: M tiles (CTA pairs: pairs of M tiles) per raster band
+  int band;              // dense: M tiles (2SM kernel: pairs of M tiles) per raster band
   int* status;
   uint64_t wait_ns;
   // dense 2SM kernel: pair tiles from this index on each run as two half-width tiles
@@ -118,7 +118,6 @@ struct Tile {
   const uint8_t* sfb_base;
   int64_t sfb_row_tiles_stride;  // tiles between consecutive 128-row B tiles
   int c_z;               // the problem's index in the output map (expert for wgrad)
-  bool a_valid;          // the A row tile exists (a CTA pair may overhang M by one tile)
   bool live;
 };
 
@@ -142,7 +141,6 @@ template <int BN, int kMode>
 __device__ Tile make_tile(const Params& p, const SegShared* seg, int64_t id) {
   Tile t;
   t.live = false;
-  t.a_valid = true;
   const int64_t n_kt_dense = (p.K + BK - 1) / BK;
   if (kMode == kDense) {
     if (id >= p.num_tiles) return t;
@@ -228,60 +226,15 @@ __device__ Tile make_tile(const Params& p, const SegShared* seg, int64_t id) {
   return t;
 }
 
-// Dense tiles of a CTA pair (cluster of 2): the pair shares one N tile and takes two
-// adjacent M tiles; CTA rank r of the cluster owns M tile 2 * pm + r.
-template <int BN>
-__device__ Tile make_tile_pair(const Params& p, int64_t pid, uint32_t crank) {
-  Tile t;
-  t.live = false;
-  const int64_t n_pm = (p.num_m_tiles + 1) / 2;
-  if (pid >= n_pm * p.num_n_tiles) return t;
-  const int64_t GP = p.band;  // bands of p.band pairs sweep across N
-  const int64_t band = GP * p.num_n_tiles;
-  const int64_t first = (pid / band) * GP;
-  const int64_t gp = (n_pm - first) < GP ? (n_pm - first) : GP;
-  const int64_t pm = first + (pid % band) % gp;
-  const int64_t nt = (pid % band) / gp;
-  const int64_t mt = 2 * pm + crank;
-  const int64_t n_kt = (p.K + BK - 1) / BK;
-  t.m0 = mt * BM;
-  t.n0 = nt * BN;
-  const int64_t left = p.M - t.m0;
-  t.rows_valid = static_cast<int>(left <= 0 ? 0 : (left < BM ? left : BM));
-  t.cols_valid = static_cast<int>((p.N - t.n0) < BN ? (p.N - t.n0) : BN);
-  t.a_row = t.m0;
-  t.k_origin = 0;
-  t.nk = static_cast<int>(n_kt);
-  t.last_blocks = static_cast<int>(((p.K - (n_kt - 1) * BK) + 31) / 32);
-  t.b_z = 0;
-  t.sfa_tile0 = mt * n_kt;
-  t.sfa_kstride = 1;
-  t.sfb_base = p.sB + nt * (BN / 128) * n_kt * 512;
-  t.sfb_row_tiles_stride = n_kt;
-  t.c_z = 0;
-  t.a_valid = mt < p.num_m_tiles;
-  t.live = true;
-  return t;
-}
-
-template <int BN, int kMode, bool kPair>
-__device__ __forceinline__ Tile tile_of(const Params& p, const SegShared* seg, int64_t id,
-                                        uint32_t crank) {
-  if (kPair) return make_tile_pair<BN>(p, id, crank);
-  return make_tile<BN, kMode>(p, seg, id);
-}
-
-template <int BN, int kMode, bool kPair>
+template <int BN, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                   const __grid_constant__ CUtensorMap map_b,
                   const __grid_constant__ CUtensorMap map_c, const Params p) {
   using C = Cfg<BN>;
-  static_assert(!kPair || kMode == kDense, "CTA pairs are used for the dense GEMM only");
-  // persistent tile loop: CTAs (or CTA pairs) stride over the tile list
-  const uint32_t crank = kPair ? cluster_ctarank() : 0;
-  const int64_t first_id = kPair ? (blockIdx.x >> 1) : blockIdx.x;
-  const int64_t id_step = kPair ? (gridDim.x >> 1) : gridDim.x;
+  // persistent tile loop: CTAs stride over the tile list
+  const int64_t first_id = blockIdx.x;
+  const int64_t id_step = gridDim.x;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -302,7 +255,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kPair ? 2 : 1);  // a pair's stage is freed by both MMA issuers
+      mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, kEpiWarps);
@@ -355,8 +308,6 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
-  // the peer's barriers must be initialised before any multicast copy or commit lands
-  if (kPair) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -367,11 +318,11 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     uint32_t it = 0;
     bool ok = true;
     for (int64_t id = first_id; ok; id += id_step) {
-      const Tile t = tile_of<BN, kMode, kPair>(p, seg, id, crank);
+      const Tile t = make_tile<BN, kMode>(p, seg, id);
       if (!t.live) break;
       int n_sfb = 0;
       for (int h = 0; h < C::kSfbTiles; ++h) n_sfb += (t.n0 + 128 * h < p.N);
-      const uint32_t bytes = C::kABytes + C::kBBytes + (t.a_valid ? 512 : 0) + 512 * n_sfb;
+      const uint32_t bytes = C::kABytes + C::kBBytes + 512 + 512 * n_sfb;
       for (int kb = 0; kb < t.nk; ++kb, ++it) {
         const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1;
         if (!warp_wait(&empty[s], ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
@@ -380,17 +331,13 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
           const int32_t kx = static_cast<int32_t>(t.k_origin + static_cast<int64_t>(kb) * BK);
           tma_load_2d(smem + C::kOffA + s * C::kABytes, &map_a, kx,
                       static_cast<int32_t>(t.a_row), &full[s]);
-          if (kPair)  // my half of the shared B tile, into both CTAs of the pair
-            tma_load_2d_mc(smem + C::kOffB + s * C::kBBytes + crank * (C::kBBytes / 2), &map_b, kx,
-                           static_cast<int32_t>(t.n0 + crank * (BN / 2)), &full[s], 0x3);
-          else if (kMode == kGroupRows)
+          if (kMode == kGroupRows)
             tma_load_3d(smem + C::kOffB + s * C::kBBytes, &map_b, kx, static_cast<int32_t>(t.n0),
                         t.b_z, &full[s]);
           else
             tma_load_2d(smem + C::kOffB + s * C::kBBytes, &map_b, kx, static_cast<int32_t>(t.n0),
                         &full[s]);
-          if (t.a_valid)
-            bulk_load(smem + C::kOffSfa + s * 512, p.sA + (t.sfa_tile0 + kb) * 512, 512, &full[s]);
+          bulk_load(smem + C::kOffSfa + s * 512, p.sA + (t.sfa_tile0 + kb) * 512, 512, &full[s]);
           for (int h = 0; h < n_sfb; ++h)
             bulk_load(smem + C::kOffSfb + s * C::kSfbBytes + h * 512,
                       t.sfb_base + (h * t.sfb_row_tiles_stride + kb) * 512, 512, &full[s]);
@@ -427,7 +374,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     constexpr uint32_t kId0 = mxf8_idesc(BM, BN, 0, 0), kId1 = mxf8_idesc(BM, BN, 1, 1);
     constexpr uint32_t kId2 = mxf8_idesc(BM, BN, 2, 2), kId3 = mxf8_idesc(BM, BN, 3, 3);
     for (int64_t id = first_id; ok; id += id_step) {
-      const Tile t = tile_of<BN, kMode, kPair>(p, seg, id, crank);
+      const Tile t = make_tile<BN, kMode>(p, seg, id);
       if (!t.live) break;
       if (t.nk == 0) continue;
       if (!warp_wait(acc_empty, (acc_it & 1) ^ 1, abort_flag, p.wait_ns)) {
@@ -459,10 +406,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
               mma_mxf8(tmem, ad + 2 * k, bd + 2 * k, mxf8_idesc(BM, BN, k, k), sfa_t, sfb_t,
                        (kb > 0 || k > 0) ? 1u : 0u);
           }
-          if (kPair)
-            mma_commit_mc(&empty[s], 0x3);  // frees the stage in both CTAs of the pair
-          else
-            mma_commit(&empty[s]);
+          mma_commit(&empty[s]);
         }
         __syncwarp();
       }
@@ -490,7 +434,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     uint32_t acc_it = 0;
     bool ok = true;
     for (int64_t id = first_id; ok; id += id_step) {
-      const Tile t = tile_of<BN, kMode, kPair>(p, seg, id, crank);
+      const Tile t = make_tile<BN, kMode>(p, seg, id);
       if (!t.live) break;
       if (t.nk > 0) {
         // one lane waits, the warp follows its verdict (keeps the warp converged)
@@ -574,8 +518,6 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 
   tc_fence_before();
   __syncthreads();
-  // no CTA of a pair may leave while its peer can still multicast into it or arrive on it
-  if (kPair) cluster_sync();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -1260,11 +1202,11 @@ uint64_t wait_limit_ns() {
   return ns;
 }
 
-template <int BN, int kMode, bool kPair>
+template <int BN, int kMode>
 int launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const Params& p,
            int64_t grid, cudaStream_t stream) {
   using C = Cfg<BN>;
-  auto k = mxfp8_gemm_kernel<BN, kMode, kPair>;
+  auto k = mxfp8_gemm_kernel<BN, kMode>;
   static bool attr_set[64] = {};  // per device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MXFP8_ERR_CUDA;
@@ -1275,51 +1217,8 @@ int launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, 
     attr_set[dev] = true;
   }
   if (grid <= 0) return MXFP8_OK;
-  if (!kPair) {
-    k<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(ma, mb, mc, p);
-    return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, ma, mb, mc, p) == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
-}
-
-// How many CTA pairs of the dense kernel fit on the device at once (cached per device).
-template <int BN>
-int64_t max_pairs() {
-  static int64_t cached[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
-  using C = Cfg<BN>;
-  auto k = mxfp8_gemm_kernel<BN, kDense, true>;
-  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * 256, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess || clusters <= 0)
-    clusters = num_sms() / 2;
-  if (dev >= 0 && dev < 64) cached[dev] = clusters;
-  return clusters;
+  k<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(ma, mb, mc, p);
+  return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
 }
 
 // Raster band width, in M tiles. Tiles of a band are visited M tile first, so that while
@@ -1411,7 +1310,7 @@ int64_t max_duo_clusters() {
 }
 
 // Dense GEMMs with N > 128 and at least two M tiles run on the 2SM kernel;
-// MXFP8_GEMM_2SM=0 selects the one-SM CTA pairs instead.
+// MXFP8_GEMM_2SM=0 selects the one-SM kernel instead.
 bool duo_enabled() {
   static const bool on = [] {
     const char* e = getenv("MXFP8_GEMM_2SM");
@@ -1572,14 +1471,6 @@ int duo_grouped_width(int) {
   return (w == 256 || w == 192) ? w : 256;
 }
 
-bool pairs_enabled() {
-  static const bool on = [] {
-    const char* e = getenv("MXFP8_GEMM_PAIRS");
-    return !(e && e[0] == '0');
-  }();
-  return on;
-}
-
 }  // namespace
 
 int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
@@ -1608,20 +1499,10 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   CUtensorMap ma, mb, mc;
   if (!make_map(&ma, a.A, 2, a.K, a.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
   if (!make_out_map(&mc, a.C, a.M, a.N, 1, p.out_fp32 != 0, 3)) return MXFP8_ERR_CUDA;
-  // A CTA pair shares each B tile: each CTA loads half of it and multicasts it to both.
-  const bool pair = wide && pairs_enabled() && p.num_m_tiles >= 2;
-  if (pair) {
-    if (!make_map(&mb, a.B, 2, a.K, a.N, 1, BK, bn / 2)) return MXFP8_ERR_CUDA;
-    const int64_t pair_tiles = static_cast<int64_t>((p.num_m_tiles + 1) / 2) * p.num_n_tiles;
-    p.band = (p.band + 1) / 2;
-    const int64_t mp = max_pairs<256>();
-    const int64_t pairs = pair_tiles < mp ? pair_tiles : mp;
-    return launch<256, kDense, true>(ma, mb, mc, p, 2 * pairs, stream);
-  }
   if (!make_map(&mb, a.B, 2, a.K, a.N, 1, BK, bn)) return MXFP8_ERR_CUDA;
   const int64_t grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-  return wide ? launch<256, kDense, false>(ma, mb, mc, p, grid, stream)
-              : launch<128, kDense, false>(ma, mb, mc, p, grid, stream);
+  return wide ? launch<256, kDense>(ma, mb, mc, p, grid, stream)
+              : launch<128, kDense>(ma, mb, mc, p, grid, stream);
 }
 
 int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
@@ -1656,8 +1537,8 @@ int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     if (!make_map(&mb, a.B, 2, a.total_rows, p.N, 1, BK, bn)) return MXFP8_ERR_CUDA;
     if (!make_out_map(&mc, a.C, p.M, p.N, p.E, p.out_fp32 != 0, 3)) return MXFP8_ERR_CUDA;
     const int64_t grid = tiles < num_sms() ? tiles : num_sms();
-    return wide ? launch<256, kGroupWgrad, false>(ma, mb, mc, p, grid, stream)
-                : launch<128, kGroupWgrad, false>(ma, mb, mc, p, grid, stream);
+    return wide ? launch<256, kGroupWgrad>(ma, mb, mc, p, grid, stream)
+                : launch<128, kGroupWgrad>(ma, mb, mc, p, grid, stream);
   }
   // fprop / dgrad: A [T][K] segmented by rows, B [E][N][K], C [T][N]
   p.M = a.total_rows;
@@ -1679,8 +1560,8 @@ int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   if (!make_map(&mb, a.B, 3, a.K, a.N, a.num_experts, BK, bn)) return MXFP8_ERR_CUDA;
   if (!make_out_map(&mc, a.C, a.total_rows, p.N, 1, p.out_fp32 != 0, 3)) return MXFP8_ERR_CUDA;
   const int64_t grid = tiles < num_sms() ? tiles : num_sms();
-  return wide ? launch<256, kGroupRows, false>(ma, mb, mc, p, grid, stream)
-              : launch<128, kGroupRows, false>(ma, mb, mc, p, grid, stream);
+  return wide ? launch<256, kGroupRows>(ma, mb, mc, p, grid, stream)
+              : launch<128, kGroupRows>(ma, mb, mc, p, grid, stream);
 }
 
 }  // namespace mxfp8
