@@ -296,7 +296,8 @@ int mxfp8_grouped_gemm(const void* A_dev, const void* sA_dev, const void* B_dev,
 
 /*
  * Workspace bytes mxfp8_selfcheck needs for `tokens` random input rows against an
- * [N][K] weight (0 for invalid sizes: tokens % 16, N % 16 and K % 32 must be 0).
+ * [N][K] weight (0 for invalid sizes: tokens % 16, N % 16 and K % 32 must be 0, and the
+ * size must fit in 64 bits).
  */
 size_t mxfp8_selfcheck_workspace_bytes(int64_t tokens, int64_t N, int64_t K);
 
@@ -312,7 +313,8 @@ size_t mxfp8_selfcheck_workspace_bytes(int64_t tokens, int64_t N, int64_t K);
  * ||Y - Y_ref||_F / ||Y_ref||_F to *rel_err_dev (device float). A healthy weight gives a
  * few percent (the activations' quantization error); a derived layout that is stale or
  * misplaced relative to the synchronized weight gives order 1; the pages' tolerance is
- * 0.25. Requires tokens % 16 == 0, N % 16 == 0, K % 32 == 0.
+ * 0.25. Requires tokens % 16 == 0, N % 16 == 0, K % 32 == 0 and tokens <= 2097120;
+ * sizes whose workspace would not fit in 64 bits are invalid (MXFP8_ERR_INVALID_ARG).
  *   workspace_dev  caller-owned, >= mxfp8_selfcheck_workspace_bytes(tokens, N, K)
  *                  bytes, 256-byte aligned; holds the quantized input, the FP32 output
  *                  and the two reduction sums. Overwritten.
@@ -334,8 +336,9 @@ int mxfp8_selfcheck(const void* w_codes_dev, const void* w_scales_dev,
  *   exits), so mxfp8_selfcheck_workspace_bytes(tokens, N, K) must not exceed
  *   8 MiB (8388608 bytes); larger sizes return MXFP8_ERR_INVALID_ARG.
  *   No device memory is allocated and no allocating library routine is called.
- *   The first call on a device looks up the array's device address on that device;
- *   make that first call before any stream capture.
+ *   The first call on a device looks up the array's device address on that device
+ *   (under a lock, so host threads may make their first calls at the same time); make
+ *   that first call before any stream capture.
  *   All calls share the one array: calls that overlap on the GPU (other streams, other
  *   host threads) race on it and must be serialised by the caller. Every call
  *   rewrites what it reads, and clears its two reduction sums itself.

@@ -64,6 +64,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 constexpr int64_t kMaxTokenTiles = 65535;  // grid.y limit of the quantizer launch
+// grid.y limit of the self-check's reference kernel (32 tokens per CTA row)
+constexpr int64_t kMaxSelfcheckTokens = int64_t(32) * 65535;
 
 }  // namespace
 
@@ -362,7 +364,8 @@ int mxfp8_grouped_gemm(const void* A_dev, const void* sA_dev, const void* B_dev,
 
 size_t mxfp8_selfcheck_workspace_bytes(int64_t tokens, int64_t N, int64_t K) {
   if (tokens <= 0 || N <= 0 || K <= 0 || K % 32 || N % 16 || tokens % 16) return 0;
-  return static_cast<size_t>(selfcheck_workspace_bytes(tokens, N, K));
+  const int64_t b = selfcheck_workspace_bytes(tokens, N, K);
+  return b < 0 ? 0 : static_cast<size_t>(b);
 }
 
 int mxfp8_selfcheck(const void* w_codes_dev, const void* w_scales_dev,
@@ -375,8 +378,9 @@ int mxfp8_selfcheck(const void* w_codes_dev, const void* w_scales_dev,
   if (tokens <= 0 || N <= 0 || K <= 0) return MXFP8_ERR_INVALID_ARG;
   if (K % 32 || N % 16 || tokens % 16) return MXFP8_ERR_ALIGNMENT;
   if (tokens > 0x7FFFFF00 || N > 0x7FFFFF00 || K > 0x7FFFFF00) return MXFP8_ERR_INVALID_ARG;
-  if (workspace_bytes < static_cast<size_t>(selfcheck_workspace_bytes(tokens, N, K)))
-    return MXFP8_ERR_INVALID_ARG;
+  if (tokens > kMaxSelfcheckTokens) return MXFP8_ERR_INVALID_ARG;
+  const int64_t need = selfcheck_workspace_bytes(tokens, N, K);
+  if (need < 0 || workspace_bytes < static_cast<size_t>(need)) return MXFP8_ERR_INVALID_ARG;
   if (!aligned16(w_codes_dev) || !aligned16(w_scales_dev) || !aligned16(x_bf16_dev) ||
       (reinterpret_cast<uintptr_t>(workspace_dev) & 255u) ||
       (reinterpret_cast<uintptr_t>(rel_err_dev) & 3u))
@@ -399,8 +403,9 @@ int mxfp8_selfcheck_noalloc(const void* w_codes_dev, const void* w_scales_dev,
   if (tokens <= 0 || N <= 0 || K <= 0) return MXFP8_ERR_INVALID_ARG;
   if (K % 32 || N % 16 || tokens % 16) return MXFP8_ERR_ALIGNMENT;
   if (tokens > 0x7FFFFF00 || N > 0x7FFFFF00 || K > 0x7FFFFF00) return MXFP8_ERR_INVALID_ARG;
-  if (selfcheck_workspace_bytes(tokens, N, K) > kSelfcheckNoallocMaxBytes)
-    return MXFP8_ERR_INVALID_ARG;
+  if (tokens > kMaxSelfcheckTokens) return MXFP8_ERR_INVALID_ARG;
+  const int64_t need = selfcheck_workspace_bytes(tokens, N, K);
+  if (need < 0 || need > kSelfcheckNoallocMaxBytes) return MXFP8_ERR_INVALID_ARG;
   if (!aligned16(w_codes_dev) || !aligned16(w_scales_dev) || !aligned16(x_bf16_dev) ||
       (reinterpret_cast<uintptr_t>(rel_err_dev) & 3u))
     return MXFP8_ERR_ALIGNMENT;

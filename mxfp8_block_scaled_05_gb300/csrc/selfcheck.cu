@@ -17,6 +17,8 @@
 // synchronized weight therefore shows up as an error of order 1.
 
 #include <cstdint>
+#include <mutex>
+
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -130,9 +132,23 @@ static __device__ __align__(256) uint8_t g_selfcheck_scratch[kSelfcheckNoallocMa
 }  // namespace
 
 int64_t selfcheck_workspace_bytes(int64_t T, int64_t N, int64_t K) {
-  auto up = [](int64_t b) { return (b + 255) / 256 * 256; };
-  const int64_t xs = ((T + 127) / 128) * ((K / 32 + 3) / 4) * 512;
-  return up(T * K) + up(xs) + up(T * N * 4) + 256;
+  // Each term is formed with overflow checks: T, N and K may each be near 2^31, so their
+  // products can leave int64. Any overflow makes the size invalid (-1), which every caller
+  // rejects, so no size can wrap around to a small value that passes a capacity check.
+  if (T <= 0 || N <= 0 || K <= 0) return -1;
+  int64_t tk, tn, tn4, xs_tiles, xs, sum;
+  if (__builtin_mul_overflow(T, K, &tk) || __builtin_mul_overflow(T, N, &tn) ||
+      __builtin_mul_overflow(tn, int64_t(4), &tn4) ||
+      __builtin_mul_overflow((T + 127) / 128, (K / 32 + 3) / 4, &xs_tiles) ||
+      __builtin_mul_overflow(xs_tiles, int64_t(512), &xs))
+    return -1;
+  constexpr int64_t kPad = 255;  // each part is rounded up to 256 bytes
+  if (tk > INT64_MAX / 4 || tn4 > INT64_MAX / 4 || xs > INT64_MAX / 4) return -1;
+  auto up = [](int64_t b) { return (b + kPad) / 256 * 256; };
+  if (__builtin_add_overflow(up(tk), up(xs), &sum) || __builtin_add_overflow(sum, up(tn4), &sum) ||
+      __builtin_add_overflow(sum, int64_t(256), &sum))
+    return -1;
+  return sum;
 }
 
 int launch_selfcheck(const SelfcheckArgs& a, cudaStream_t stream) {
@@ -173,18 +189,20 @@ int launch_selfcheck(const SelfcheckArgs& a, cudaStream_t stream) {
 namespace mxfp8 {
 
 // Device address of the fixed workspace, looked up once per device with that device
-// current (host code must not use the array's name as a device address).
+// current (host code must not use the array's name as a device address). The per-device
+// cache is guarded by a mutex, so host threads that make their first calls at the same
+// time do not race on it.
 int selfcheck_noalloc_workspace(void** out) {
+  static std::mutex mu;
   static void* addr[64] = {};
-  static bool done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MXFP8_ERR_CUDA;
-  if (!done[dev]) {
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_selfcheck_scratch) != cudaSuccess || p == nullptr)
       return MXFP8_ERR_CUDA;
     addr[dev] = p;
-    done[dev] = true;
   }
   *out = addr[dev];
   return MXFP8_OK;

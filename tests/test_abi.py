@@ -144,3 +144,27 @@ def test_valid_call_without_a_gpu_fails_cleanly(lib):
     assert lib.mxfp8_quantize(p, 64, 64, m.ROW, p, p, m.SWIZZLED, None) in (
         m.ERR_CUDA, m.ERR_UNSUPPORTED_ARCH)
     assert lib.mxfp8_get_device_status(None) in (m.ERR_CUDA, m.ERR_UNSUPPORTED_ARCH)
+
+
+def test_selfcheck_sizes_and_argument_errors_need_no_device(lib):
+    """Workspace sizes near the 2^31 argument limits overflow 64 bits; they are invalid (0),
+    never a wrapped-around small size that would pass the capacity checks."""
+    wb = lib.mxfp8_selfcheck_workspace_bytes
+    up = lambda b: (b + 255) // 256 * 256
+    t, n, k = 128, 1024, 2048
+    assert wb(t, n, k) == up(t * k) + up(1 * 16 * 512) + up(t * n * 4) + 256
+    big = 0x7FFFFF00
+    assert wb(big // 16 * 16, big // 16 * 16, big // 32 * 32) == 0
+    assert wb(1 << 30, 1 << 30, 1 << 30) == 0
+    assert wb(8, 64, 64) == 0 and wb(16, 8, 64) == 0 and wb(16, 64, 48) == 0
+    p = ctypes.c_void_p(0x10000)
+    # the allocation-free variant rejects what does not fit its fixed array, and sizes
+    # whose workspace overflows, before touching the device
+    na = lib.mxfp8_selfcheck_noalloc
+    assert na(p, p, p, p, 8192, 8192, p, 1024, p, None) == m.ERR_INVALID_ARG
+    assert na(p, p, p, p, 1 << 30, 1 << 30, p, 1 << 20, p, None) == m.ERR_INVALID_ARG
+    assert na(p, p, p, p, 1024, 2048, p, 40, p, None) == m.ERR_ALIGNMENT   # tokens % 16
+    sc = lib.mxfp8_selfcheck
+    assert sc(p, p, p, p, 1 << 30, 1 << 30, p, 1 << 20, p, 1 << 40, p, None) == m.ERR_INVALID_ARG
+    assert sc(p, p, p, p, 1024, 2048, p, 128, p, 100, p, None) == m.ERR_INVALID_ARG  # too small
+    assert sc(p, p, p, p, 64, 64, p, 32 * 65535 + 16, p, 1 << 62, p, None) == m.ERR_INVALID_ARG
