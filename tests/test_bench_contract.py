@@ -62,3 +62,13 @@ def test_dense_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] > 0 and line["e2e"]["d2h_bytes_per_step"] > 0
     assert line["quantize"]["GB/s"] > 0 and line["gemm"]["TFLOP/s"] > 0
+    rq = line["roofline_quantize"]
+    assert rq["bound"] == "hbm" and rq["unit"] == "GB/s"
+    assert rq["frac"] == pytest.approx(rq["achieved"] / rq["peak"])
+    sec = line["secondary"]
+    moe = sec["moe_qwen3_30b_a3b"]
+    for proj in ("gate_up", "down"):
+        for op in ("fprop", "dgrad", "wgrad"):
+            assert moe[proj][op]["TFLOP/s"] > 0 and moe[proj][op]["frac_of_roof"] > 0
+    assert sec["weight_sync_qwen3_8b"]["weights"] == 144
+    assert [r["tokens"] for r in sec["microbatch_sweep"]] == [1024, 2048, 4096, 4608, 8192, 16384]

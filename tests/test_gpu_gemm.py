@@ -8,7 +8,8 @@ import torch
 
 import oracle.mxfp8_oracle as O
 from mxfp8_block_scaled_05_gb300 import workloads as W
-from tests.oracle_helpers import assert_gemm_within, bf16_bits, bits_to_bf16, gpu_ready
+from tests.oracle_helpers import (assert_gemm_within, bf16_bits, bits_to_bf16, gpu_ready,
+                                  rows_of, sampled_gemm_check)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -103,20 +104,7 @@ def test_gpu_quantize_then_gemm_small_layer(m):
 
 
 def _sampled_check(m, c_gpu, a_rows_fn, b_rows_fn, mdim, ndim, seed, bf16_out, what):
-    """Checks two full 128 x 128 tiles (first and an interior one) and a 64 x 128 grid of
-    random entries of a full-size GEMM output; a_rows_fn(idx) / b_rows_fn(idx) give the
-    oracle-quantized rows (codes, linear scales) of the two K-major operands."""
-    g = np.random.default_rng(seed)
-    mt, nt = (mdim // 2) // 128 * 128, (ndim // 2) // 128 * 128
-    samples = [(np.arange(0, 128), np.arange(0, 128)),
-               (np.arange(mt, mt + 128), np.arange(nt, nt + 128)),
-               (np.sort(g.choice(mdim, 64, replace=False)), np.sort(g.choice(ndim, 128, replace=False)))]
-    for mi, ni in samples:
-        qa, sa = a_rows_fn(mi)
-        qb, sb = b_rows_fn(ni)
-        ref, ab = O.gemm(qa, sa, qb, sb), O.gemm_abs(qa, sa, qb, sb)
-        got = c_gpu[torch.from_numpy(mi).to(DEV)][:, torch.from_numpy(ni).to(DEV)]
-        assert_gemm_within(got.double().cpu().numpy(), ref, ab, bf16_out, what)
+    sampled_gemm_check(c_gpu, a_rows_fn, b_rows_fn, mdim, ndim, seed, bf16_out, what)
 
 
 def test_qwen3_8b_layer_set_full_size(m):
@@ -215,43 +203,71 @@ def test_grouped_bad_offsets_latched(m):
     assert m.device_status() == m.OK
 
 
-def test_qwen3_30b_a3b_experts_full_size_sampled(m):
+@pytest.fixture(scope="module")
+def moe_layer():
+    return W.moe_expert_layer(DEV)
+
+
+@pytest.mark.parametrize("proj", ["gate_up", "down"])
+def test_qwen3_30b_a3b_experts_full_size_sampled(m, moe_layer, proj):
     """Config: 128 experts, 8192 tokens routed top-8 with Zipf(1.1) counts, segments
-    padded to 32; gate_up (2048 -> 1536) fprop / dgrad / wgrad at full size, sampled
-    against the oracle for the most and least loaded non-empty experts."""
-    d = W.moe_expert_layer(DEV)
+    padded to 32 (section "A held-out workload, and end to end", Table 4). Both expert
+    projections - gate_up (2048 -> 1536) and down (768 -> 2048) - run fprop, dgrad and
+    wgrad at full size, with the operands quantized as the bench step quantizes them
+    (grouped dual for the routed rows and their gradients, batched row- and column-wise
+    for the expert weights). Sampled against the oracle for the most and the least loaded
+    non-empty experts and one of median load; empty experts' dW must be zero."""
+    d = moe_layer
     counts, off = d["counts"].numpy(), d["offsets"].numpy()
     offs = d["offsets"].to(DEV)
-    x, w, dy = d["x"], d["w_gate_up"], d["dy_gate_up"]
+    x, w, dy = ((d["x"], d["w_gate_up"], d["dy_gate_up"]) if proj == "gate_up"
+                else (d["h"], d["w_down"], d["dy_down"]))
     E, n, k = w.shape
-    qx, sx = m.quantize_grouped(x, offs, m.ROW)
-    qw, sw = m.quantize_batched(w, m.ROW)
-    y = m.grouped_gemm(qx, sx, qw, sw, offs, m.FPROP)
-    qdyt, sdyt = m.quantize_grouped(dy, offs, m.COL)
-    qxt, sxt = m.quantize_grouped(x, offs, m.COL)
-    dw = m.grouped_gemm(qdyt, sdyt, qxt, sxt, offs, m.WGRAD)
+    xr, xrs, xc, xcs = m.quantize_grouped_dual(x, offs)
+    dyr, dyrs, dyc, dycs = m.quantize_grouped_dual(dy, offs)
+    wr, wrs = m.quantize_batched(w, m.ROW)
+    wc, wcs = m.quantize_batched(w, m.COL)
+    y = m.grouped_gemm(xr, xrs, wr, wrs, offs, m.FPROP)
+    dx = m.grouped_gemm(dyr, dyrs, wc, wcs, offs, m.DGRAD)
+    dw = m.grouped_gemm(dyc, dycs, xc, xcs, offs, m.WGRAD)
     assert m.device_status() == m.OK
     nz = np.nonzero(counts)[0]
-    picks = [nz[np.argmax(counts[nz])], nz[np.argmin(counts[nz])]]
-    rng = np.random.default_rng(4)
+    order = nz[np.argsort(counts[nz], kind="stable")]
+    picks = [order[-1], order[0], order[len(order) // 2]]
+    rng = np.random.default_rng(4 if proj == "gate_up" else 5)
     for e in picks:
+        e = int(e)
         lo, hi = int(off[e]), int(off[e + 1])
-        xe = bf16_bits(x[lo:hi])
-        we = bf16_bits(w[e])
-        dye = bf16_bits(dy[lo:hi])
+        seg = torch.arange(lo, hi, device=DEV)
+        xe, dye, we = x[seg], dy[seg], w[e]
         rows = np.sort(rng.choice(hi - lo, min(64, hi - lo), replace=False))
+        rsel = torch.from_numpy(lo + rows).to(DEV)
+        # fprop: Y[rows, cols] = X_e[rows] . W_e[cols]^T
         cols = np.sort(rng.choice(n, 128, replace=False))
-        qa, sa = O.quantize(xe[rows], O.ROW)
-        qb, sb = O.quantize(we[cols], O.ROW)
-        got = y[torch.from_numpy(lo + rows).to(DEV)][:, torch.from_numpy(cols).to(DEV)]
+        qa, sa = rows_of(xe, O.ROW)(rows)
+        qb, sb = rows_of(we, O.ROW)(cols)
+        got = y[rsel][:, torch.from_numpy(cols).to(DEV)]
         assert_gemm_within(got.double().cpu().numpy(), O.gemm(qa, sa, qb, sb),
-                           O.gemm_abs(qa, sa, qb, sb), True, f"moe fprop e{e}")
+                           O.gemm_abs(qa, sa, qb, sb), True, f"{proj} fprop e{e}")
+        # dgrad: dX[rows, cols] = dY_e[rows] . W_e[:, cols] (B = W_e column-wise)
+        cols = np.sort(rng.choice(k, 128, replace=False))
+        qa, sa = rows_of(dye, O.ROW)(rows)
+        qb, sb = rows_of(we, O.COL)(cols)
+        got = dx[rsel][:, torch.from_numpy(cols).to(DEV)]
+        assert_gemm_within(got.double().cpu().numpy(), O.gemm(qa, sa, qb, sb),
+                           O.gemm_abs(qa, sa, qb, sb), True, f"{proj} dgrad e{e}")
+        # wgrad: dW_e[ni, ki] = sum over the expert's tokens of dY_e[:, ni] X_e[:, ki]
         ni = np.sort(rng.choice(n, 64, replace=False))
         ki = np.sort(rng.choice(k, 128, replace=False))
-        qa, sa = O.quantize(np.ascontiguousarray(dye[:, ni]), O.COL)
-        qb, sb = O.quantize(np.ascontiguousarray(xe[:, ki]), O.COL)
+        qa, sa = rows_of(dye, O.COL)(ni)
+        qb, sb = rows_of(xe, O.COL)(ki)
         got = dw[e][torch.from_numpy(ni).to(DEV)][:, torch.from_numpy(ki).to(DEV)]
         assert_gemm_within(got.double().cpu().numpy(), O.gemm(qa, sa, qb, sb),
-                           O.gemm_abs(qa, sa, qb, sb), True, f"moe wgrad e{e}")
+                           O.gemm_abs(qa, sa, qb, sb), True, f"{proj} wgrad e{e}")
     for e in np.nonzero(counts == 0)[0]:
         assert torch.all(dw[int(e)] == 0)
+    # rows of no token (segment padding) are zero inputs: their outputs are exact zeros
+    pad = np.concatenate([np.arange(off[e] + counts[e], off[e + 1]) for e in range(E)])
+    if pad.size:
+        psel = torch.from_numpy(pad).to(DEV)
+        assert torch.all(y[psel] == 0) and torch.all(dx[psel] == 0)

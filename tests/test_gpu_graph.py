@@ -2,11 +2,15 @@
 MXFP8 RL on Blackwell", section "Where the time goes": CUDA graphs over the micro-batch
 should remove most of the host dispatch). The library's compute calls enqueue work only
 (no host synchronization, no allocation), so a whole layer - dual quantize of X, W, dY
-and the three GEMMs - captures; replays give the same bytes as eager calls."""
+and the three GEMMs - captures; replays give the same bytes as eager calls, and the
+replayed results match the oracle: every quantized copy bit for bit and Y, dX, dW within
+the GEMM gate, in full."""
+import numpy as np
 import pytest
 import torch
 
-from tests.oracle_helpers import gpu_ready
+import oracle.mxfp8_oracle as O
+from tests.oracle_helpers import assert_gemm_within, bf16_bits, gpu_ready, u8
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -59,3 +63,22 @@ def test_layer_step_in_a_cuda_graph_matches_eager():
     for a, b in zip(eager, got):
         assert torch.equal(a, b)
     assert m.device_status() == m.OK
+    # the replayed step against the oracle, in full
+    oq = {}
+    for name, src in (("x", x), ("w", w), ("dy", dy)):
+        bits = bf16_bits(src)
+        rq, rs = O.quantize(bits, O.ROW)
+        cq, cs = O.quantize(bits, O.COL)
+        r, r_s, c, c_s = bufs[name]
+        np.testing.assert_array_equal(u8(r), rq)
+        np.testing.assert_array_equal(u8(r_s), O.swizzle_scales(rs))
+        np.testing.assert_array_equal(u8(c), cq)
+        np.testing.assert_array_equal(u8(c_s), O.swizzle_scales(cs))
+        oq[name] = (rq, rs, cq, cs)
+    for out, (a, ai), (b, bi), what in ((y, ("x", 0), ("w", 0), "fprop"),
+                                        (dx, ("dy", 0), ("w", 2), "dgrad"),
+                                        (dw, ("dy", 2), ("x", 2), "wgrad")):
+        qa, sa = oq[a][ai], oq[a][ai + 1]
+        qb, sb = oq[b][bi], oq[b][bi + 1]
+        assert_gemm_within(out.double().cpu().numpy(), O.gemm(qa, sa, qb, sb),
+                           O.gemm_abs(qa, sa, qb, sb), True, f"graph replay {what}")

@@ -189,19 +189,35 @@ def test_qwen3_8b_layer_set_full_size_sampled(m):
 
 def test_weight_sync_pass_byte_equality(m):
     """Config: the weight-synchronization pass of a Qwen3-8B-shaped model (36 layers x 4
-    projections, 6.95 G elements): every weight quantized by a separate sync call equals
-    its forward-path quantization byte for byte, including when the sync shards it by
-    rows (128-row multiples) or columns (128-column multiples); sampled rows also match
-    the oracle."""
+    projections, 6.95 G elements). Section "The grid, byte for byte": the synced weights
+    must be the forward GEMM's weight quantization byte for byte. The two come from
+    different kernel paths here:
+      - the sync call is mxfp8_quantize (ROW, swizzled scales): the register-tile
+        row-wise kernel;
+      - the forward operand is the row-wise copy that the forward step makes with
+        mxfp8_quantize_dual_multi, the weight quantized in one launch beside its layer's
+        activations: the shared-tile dual kernel (the bench step's own call).
+    Every one of the 144 weights is compared in full, codes and scales, so a single
+    diverging byte between the two row passes fails the test. One weight of each of the
+    four shapes is also compared in full with the oracle, and sharded sync calls (row
+    shards at 128-row multiples, column shards at 128-column multiples) equal the whole."""
     shapes = W.sync_weight_shapes()
     assert len(shapes) == 144
-    total = 0
+    g = torch.Generator(device=DEV).manual_seed(40)
+    xs = {k: W.activations_bf16(4096, k, g, DEV, 0.005, 30.0) for k in (4096, 12288)}
+    total, oracle_checked = 0, set()
     for i, (layer, name, n, k) in enumerate(shapes):
         wt = W.sync_weight(layer, name, n, k, DEV)
         total += wt.numel()
-        q_f, s_f = m.quantize(wt, m.ROW, m.SWIZZLED)         # forward-path operand
-        q_s, s_s = m.quantize(wt, m.ROW, m.SWIZZLED)         # sync path
+        q_s, s_s = m.quantize(wt, m.ROW, m.SWIZZLED)                   # sync path
+        _, (q_f, s_f, _, _) = m.quantize_dual_multi([xs[k], wt], m.SWIZZLED)  # forward path
+        assert q_f.data_ptr() != q_s.data_ptr()
         assert torch.equal(q_f, q_s) and torch.equal(s_f, s_s), (layer, name)
+        if name not in oracle_checked:
+            rq, rs = O.quantize(bf16_bits(wt), O.ROW)
+            np.testing.assert_array_equal(u8(q_s), rq)
+            np.testing.assert_array_equal(u8(s_s), O.swizzle_scales(rs))
+            oracle_checked.add(name)
         if i % 37 == 0:
             # sharded sync: two row shards (128-multiple split) and two column shards
             cut = (n // 2) // 128 * 128
@@ -215,9 +231,8 @@ def test_weight_sync_pass_byte_equality(m):
             q_lin, s_lin = m.quantize(wt, m.ROW, m.LINEAR)
             assert torch.equal(torch.cat([ql, qr], dim=1), q_lin)
             assert torch.equal(torch.cat([sl, sr], dim=1), s_lin)
-        if i % 12 == 0:
-            _sample_rows_check(m, wt, m.ROW, 8, seed=i)
         del wt, q_f, s_f, q_s, s_s
+    assert oracle_checked == {"qkv_proj", "o_proj", "gate_up_proj", "down_proj"}
     assert total == 36 * (6144 * 4096 + 4096 * 4096 + 24576 * 4096 + 4096 * 12288)
     torch.cuda.empty_cache()
 

@@ -4,7 +4,8 @@ Some callers cannot allocate device memory when they check a freshly synchronize
 weight - a serving engine whose caching allocator already holds the free memory, or a
 plugin without a handle to the framework's allocator. mxfp8_selfcheck_noalloc keeps its
 workspace in a fixed array inside the library instead. This test compares it with
-mxfp8_selfcheck (caller-provided workspace) on the same inputs, on two calls in a row.
+mxfp8_selfcheck (caller-provided workspace) on the same inputs, on two calls in a row, and
+both with the oracle's relative error for the same weight and input.
 The file is named to be collected last, so a run that stops at the first failure has
 already run every other test."""
 import ctypes
@@ -12,7 +13,8 @@ import ctypes
 import pytest
 import torch
 
-from tests.oracle_helpers import gpu_ready
+import oracle.mxfp8_oracle as O
+from tests.oracle_helpers import bf16_bits, gpu_ready
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -46,6 +48,9 @@ def test_noalloc_selfcheck_matches_workspace_variant_twice():
         r, v = ref.item(), got.item()
         assert 0 < r < m.SELF_CHECK_TOLERANCE
         assert abs(v - r) <= 2e-3 * r + 1e-6, (call, v, r)
+        rq, rs = O.quantize(bf16_bits(w), O.ROW)
+        want = O.selfcheck_rel_error(bf16_bits(x), rq, rs, rq, rs)
+        assert abs(v - want) <= 2e-3 * want + 1e-6, (call, v, want)
     assert m.device_status() == m.OK
 
 
