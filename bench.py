@@ -21,6 +21,8 @@ the micro-batch sweep.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --workload moe|sync|sweep     # one of the other configurations alone
+  python bench.py --workload gemm --shapes 4096,4096,4096[;M,N,K...]   # single GEMMs
+  python bench.py --workload quantize --shapes 4096,4096 --mode dual   # single quantizes
 """
 from __future__ import annotations
 
@@ -826,12 +828,86 @@ def secondary_obj(m, dev, stream, pk):
     return out
 
 
+def _parse_shapes(text):
+    return [tuple(int(v) for v in part.split(",")) for part in text.split(";") if part.strip()]
+
+
+def measure_gemm_shapes(m, dev, stream, pk, shapes, reps=20, op_name="fprop"):
+    """Single dense GEMMs (C = A . B^T, BF16 out) on random operands quantized by the
+    library: per shape, the mean launch time back to back and with events around every
+    launch; TFLOP/s from 2 M N K."""
+    op = {"fprop": m.FPROP, "dgrad": m.DGRAD, "wgrad": m.WGRAD}[op_name]
+    g = torch.Generator(device=dev).manual_seed(7)
+    rows = []
+    for mm, nn, kk in shapes:
+        a = torch.randn((mm, kk), generator=g, device=dev).to(torch.bfloat16)
+        b = (torch.randn((nn, kk), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        qa, sa = m.quantize(a, m.ROW)
+        qb, sb = m.quantize(b, m.ROW)
+        c = torch.empty((mm, nn), dtype=torch.bfloat16, device=dev)
+        fn = lambda: m.gemm(qa, sa, qb, sb, op, out=c, stream=stream)
+        ms = _timed_ms(fn, stream, reps)
+        evs = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        ev_ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+        flops = 2.0 * mm * nn * kk
+        rows.append({"M": mm, "N": nn, "K": kk, "op": op_name,
+                     "us_back_to_back": ms * 1e3, "us_event_median": ev_ms * 1e3,
+                     "TFLOP/s": flops / (ms * 1e-3) / 1e12,
+                     "frac_of_burst": flops / (ms * 1e-3) / 1e12 / (pk["bf16"] * FP8_OVER_BF16)})
+        del a, b, qa, sa, qb, sb, c
+    torch.cuda.empty_cache()
+    return rows
+
+
+def measure_quantize_shapes(m, dev, stream, pk, shapes, reps=20, mode="dual"):
+    """Single quantize launches on N(0,1) BF16 inputs: mean launch time back to back and
+    GB/s over the algorithmic bytes (dual: 2 + 2 x 1.03125 B per element; row or col:
+    3.03125 B per element)."""
+    g = torch.Generator(device=dev).manual_seed(8)
+    rows = []
+    for r, c in shapes:
+        x = torch.randn((r, c), generator=g, device=dev).to(torch.bfloat16)
+        if mode == "dual":
+            outs = m.quantize_dual(x)
+            fn = lambda: m.quantize_dual(x, m.SWIZZLED, *outs, stream=stream)
+            per = DUAL_BYTES_PER_ELEM
+        else:
+            axis = m.ROW if mode == "row" else m.COL
+            q, sc = m.quantize(x, axis)
+            fn = lambda: m.quantize(x, axis, m.SWIZZLED, out=q, scales=sc, stream=stream)
+            per = QBYTES_PER_ELEM
+        ms = _timed_ms(fn, stream, reps)
+        gbs = r * c * per / (ms * 1e-3) / 1e9
+        rows.append({"rows": r, "cols": c, "mode": mode, "us_back_to_back": ms * 1e3,
+                     "GB/s": gbs, "frac_of_hbm": gbs / pk["hbm"]})
+        del x
+    torch.cuda.empty_cache()
+    return rows
+
+
 def run_workload(args):
-    """One secondary configuration alone, one JSON line."""
+    """One secondary configuration alone, one JSON line (or one line per shape)."""
     import mxfp8_block_scaled_05_gb300 as m
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
     pk = peaks()
+    if args.workload == "gemm":
+        for row in measure_gemm_shapes(m, dev, stream, pk, _parse_shapes(args.shapes),
+                                       reps=args.reps, op_name=args.op):
+            print(json.dumps(row), flush=True)
+        return
+    if args.workload == "quantize":
+        for row in measure_quantize_shapes(m, dev, stream, pk, _parse_shapes(args.shapes),
+                                           reps=args.reps, mode=args.mode):
+            print(json.dumps(row), flush=True)
+        return
     if args.workload == "sync":
         line = measure_sync(m, dev, stream, pk, reps=5)
         from mxfp8_block_scaled_05_gb300 import workloads as W
@@ -872,7 +948,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--tokens", type=int, default=4096)
-    ap.add_argument("--workload", choices=("dense", "moe", "sync", "sweep"), default="dense")
+    ap.add_argument("--workload", choices=("dense", "moe", "sync", "sweep", "gemm", "quantize"),
+                    default="dense")
+    ap.add_argument("--shapes", default="4096,4096,4096",
+                    help="--workload gemm: M,N,K[;M,N,K...]; --workload quantize: R,C[;R,C...]")
+    ap.add_argument("--op", choices=("fprop", "dgrad", "wgrad"), default="fprop")
+    ap.add_argument("--mode", choices=("dual", "row", "col"), default="dual")
+    ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--quant", choices=("dual", "separate"), default="dual",
                     help="quantize each tensor once for both copies (dual) or per copy")
     ap.add_argument("--no-secondary", action="store_true",
