@@ -349,6 +349,20 @@ int mxfp8_selfcheck_noalloc(const void* w_codes_dev, const void* w_scales_dev,
                             float* rel_err_dev, void* stream);
 
 /*
+ * Sets how long a GEMM kernel's pipeline waits (a stage's copies, the tensor cores, the
+ * accumulator hand-over) may take before the kernel gives up, for every GEMM launched
+ * after the call, in any host thread: `ns` nanoseconds, or the default for ns == 0
+ * (MXFP8_WAIT_LIMIT_MS from the environment, else 4 s). Failure detection (the post's
+ * section "Correctness: how it fails" lists the failures a pipeline must not hang on): a
+ * kernel whose wait runs out latches MXFP8_ERR_TIMEOUT, stops issuing work, waits for the
+ * copies and tensor-core operations it has in flight (for at least 2 s, independently of
+ * this limit), frees its tensor memory and returns; its outputs are then unspecified. A
+ * limit shorter than a tile's computation makes every GEMM time out, which is how the
+ * tests exercise that path. The pages have no counterpart for this call. Returns MXFP8_OK.
+ */
+int mxfp8_set_wait_limit_ns(uint64_t ns);
+
+/*
  * Synchronizes `stream`, then returns and clears the current device's status word:
  * MXFP8_OK, or the first device-side error latched since the last call
  * (MXFP8_ERR_BAD_OFFSETS, MXFP8_ERR_TIMEOUT), or MXFP8_ERR_CUDA if the synchronization

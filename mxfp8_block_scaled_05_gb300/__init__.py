@@ -47,6 +47,7 @@ SIGNATURES = {
     "mxfp8_selfcheck_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "mxfp8_selfcheck": (_I, [_P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _SZ, _P, _P]),
     "mxfp8_selfcheck_noalloc": (_I, [_P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _P]),
+    "mxfp8_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "mxfp8_get_device_status": (_I, [_P]),
 }
 
@@ -353,6 +354,12 @@ def selfcheck(w_codes: torch.Tensor, w_scales: torch.Tensor, ref_codes: torch.Te
                                  workspace.numel(), _ptr(out), _stream(stream)),
            "mxfp8_selfcheck")
     return out
+
+
+def set_wait_limit_ns(ns: int = 0) -> None:
+    """Pipeline wait limit of later GEMM launches, in nanoseconds (0: the default, 4 s or
+    MXFP8_WAIT_LIMIT_MS); a kernel whose wait runs out latches ERR_TIMEOUT."""
+    _check(lib().mxfp8_set_wait_limit_ns(ns), "mxfp8_set_wait_limit_ns")
 
 
 def device_status(stream=None) -> int:

@@ -420,6 +420,11 @@ int mxfp8_selfcheck_noalloc(const void* w_codes_dev, const void* w_scales_dev,
   return launch_selfcheck(a, static_cast<cudaStream_t>(stream));
 }
 
+int mxfp8_set_wait_limit_ns(uint64_t ns) {
+  set_wait_limit_ns(ns);
+  return MXFP8_OK;
+}
+
 int mxfp8_get_device_status(void* stream) {
   DeviceState* d = nullptr;
   const int st = device_state(&d);

@@ -90,4 +90,7 @@ int launch_selfcheck(const SelfcheckArgs& a, cudaStream_t stream);
 
 int num_sms();  // of the current device (cached)
 
+// Pipeline wait limit of the GEMM kernels for later launches (0: the default).
+void set_wait_limit_ns(uint64_t ns);
+
 }  // namespace mxfp8
