@@ -63,14 +63,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete. Gives up - returning false -
 // after `limit_ns` of wall time or as soon as *abort is set by another role of the CTA,
-// so that a lost arrival can never hang the GPU.
+// so that a lost arrival can never hang the GPU. A failed try_wait may itself suspend the
+// thread for a short, hardware-defined time, so the clock and the abort flag are checked
+// every 8 polls: the limit is noticed within a few such suspensions.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 0) {
+    if ((i & 7) == 0) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) return false;
     }
@@ -85,7 +87,7 @@ __device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity,
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    if ((i & 7) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -333,11 +335,6 @@ __device__ __forceinline__ void bulk_commit_group() {
 // Waits until this thread's committed bulk stores have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Waits until this thread's committed bulk stores are complete.
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy reads.

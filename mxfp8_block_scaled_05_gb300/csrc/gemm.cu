@@ -102,10 +102,8 @@ struct Params {
   int* status;
   uint64_t wait_ns;      // pipeline waits give up after this (MXFP8_ERR_TIMEOUT)
   uint64_t drain_ns;     // waits for work already in flight, on the way out (never shorter)
-  // dense 2SM kernel: pair tiles from this index on each run as split_parts narrower tiles
-  // (halves; thirds of a 384-wide tile)
+  // dense 2SM kernel: pair tiles from this index on each run as two half-width tiles
   int64_t split_from = INT64_MAX;
-  int split_parts = 2;
 };
 
 // Everything a role needs to know about one output tile.
@@ -267,7 +265,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   // drain records: [0] stage uses issued by the producer, [1] stage uses consumed by the
-  // MMA issuer, [2] accumulator commits
+  // MMA issuer, [2] accumulator commits, [3] the producer's tail completed
   volatile uint32_t* rec = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 8);
   __shared__ SegShared seg_storage;
   SegShared* seg = (kMode == kDense) ? nullptr : &seg_storage;
@@ -373,6 +371,13 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
       latch_error(p.status, MXFP8_ERR_TIMEOUT);
     }
     if (issuer) rec[0] = it;  // the copies still in flight are waited for on the way out
+    // Producer tail: the MMA issuer's release of the last stage uses must have arrived on
+    // their empty barriers before the CTA exits. Waiting here overlaps the epilogue's last
+    // tile; after an abort the drain below does it instead.
+    bool tail_ok = ok;
+    for (uint32_t i = it > C::kStages ? it - C::kStages : 0; tail_ok && i < it; ++i)
+      tail_ok = warp_wait(&empty[i % C::kStages], (i / C::kStages) & 1, abort_flag, p.wait_ns);
+    if (issuer) rec[3] = tail_ok ? 1u : 0u;
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
@@ -449,21 +454,11 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     const int half = (warp - 2) >> 2;  // which half of the BN columns
     constexpr int kChunks = BN / 64;   // 32-column chunks per warp
     uint8_t* box = smem + C::kOffOut + (warp - 2) * C::kStageBoxBytes;
-    // On the CTA's last tile the pipeline stages are idle - its MMAs have completed and the
-    // producer has nothing left to load - so each warp stages every box of that tile in its
-    // own slice of them and issues all its stores back to back, instead of one box at a
-    // time through its single staging box (whose store latency is otherwise exposed at the
-    // end of the kernel).
-    constexpr int kLastBoxes = 2 * kChunks;  // FP32 output: two boxes per 32-column chunk
-    static_assert(kEpiWarps * kLastBoxes * C::kStageBoxBytes <= C::kOffBar - C::kOffA,
-                  "last-tile boxes must fit in the stage area");
-    uint8_t* const last_boxes = smem + C::kOffA + (warp - 2) * kLastBoxes * C::kStageBoxBytes;
     uint32_t acc_it = 0;
     bool ok = true;
     for (int64_t id = first_id; ok; id += id_step) {
       const Tile t = make_tile<BN, kMode>(p, seg, id);
       if (!t.live) break;
-      const bool last = !make_tile<BN, kMode>(p, seg, id + id_step).live;
       if (t.nk > 0) {
         // one lane waits, the warp follows its verdict (keeps the warp converged)
         int got = 0;
@@ -520,20 +515,15 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
               for (int j = 0; j < 4; ++j)
                 w[j] = make_uint4(b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
             }
-            uint8_t* bx = box;
-            if (last) {
-              bx = last_boxes + (2 * u + g) * C::kStageBoxBytes;
-            } else {
-              if (lane == 0) bulk_wait_read_all();  // the box is free again
-              __syncwarp();
-            }
+            if (lane == 0) bulk_wait_read_all();  // the box is free again
+            __syncwarp();
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4*>(bx + lane * 64 + 16 * (j ^ ((lane >> 1) & 3))) = w[j];
+              *reinterpret_cast<uint4*>(box + lane * 64 + 16 * (j ^ ((lane >> 1) & 3))) = w[j];
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_3d(&map_c, bx, static_cast<int32_t>(t.n0 + col),
+              tma_store_3d(&map_c, box, static_cast<int32_t>(t.n0 + col),
                            static_cast<int32_t>(t.m0 + 32 * q), t.c_z);
               bulk_commit_group();
             }
@@ -541,7 +531,9 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         }
       }
     }
-    if (lane == 0) bulk_wait_all();  // every store has landed before the CTA can exit
+    // Before the CTA exits its stores must have finished reading its shared memory; the
+    // kernel's completion makes their global writes visible to later work.
+    if (lane == 0) bulk_wait_read_all();
     __syncwarp();
     if (!ok && lane == 0) {
       *abort_flag = 1;
@@ -551,12 +543,14 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 
   tc_fence_before();
   __syncthreads();
-  // Drain: whatever stopped the loops, nothing this CTA started may still be writing its
-  // shared memory or arriving on its barriers when it exits. Loads of the stage uses that
-  // the MMA issuer never consumed complete by themselves (every byte of a stage comes from
-  // this CTA's own copies); the last arrivals of the MMA issuer's commits are waited for
-  // too. These waits have their own limit, never shorter than the pipeline's.
-  if (threadIdx.x == 0)
+  // Drain, after an abort: whatever stopped the loops, nothing this CTA started may still be
+  // writing its shared memory or arriving on its barriers when it exits. Loads of the stage
+  // uses that the MMA issuer never consumed complete by themselves (every byte of a stage
+  // comes from this CTA's own copies); the last arrivals of the MMA issuer's commits are
+  // waited for too. These waits have their own limit, never shorter than the pipeline's.
+  // Without an abort every use was consumed, the producer's tail has seen the last releases
+  // and the epilogue every accumulator commit, so there is nothing left to wait for.
+  if (threadIdx.x == 0 && !(rec[3] && !*abort_flag && rec[0] == rec[1]))
     drain_stages<C::kStages, 1>(full, empty, acc_full, rec[0], rec[1], rec[2], p.drain_ns);
   __syncthreads();
   tc_fence_after();
@@ -652,24 +646,22 @@ struct DuoTile {
   int64_t sfa_idx = 0;         // grouped: flat scale tile index of this CTA's A rows, stage 0
   int64_t sfb_idx0 = 0, sfb_idx1 = 0;  // grouped: the two B scale tiles at stage 0
   int b_z = 0, c_z = 0;        // expert index for the B (grouped rows) and C (wgrad) maps
-  int width = 0;               // output columns of the tile: BN, or BN / parts for a split one
+  int width = 0;               // output columns of the tile: BN, or BN / 2 for a half tile
 };
 
-// Dense pair tiles. Work item `pid` below p.split_from is pair tile pid; from there on,
-// p.split_parts items share one pair tile, each taking an equal share of its columns: two
-// halves (256 x BN/2), or for 384-wide tiles three thirds (256 x 128). The host puts the
-// split at the last, partial wave of clusters when its parts fit in one wave, so that wave
-// takes about as long as one part.
+// Dense pair tiles. Work item `pid` below p.split_from is pair tile pid; from there on, two
+// items share one pair tile, each taking half of its columns (256 x BN/2). The host puts the
+// split at the last, partial wave of clusters when its halves fit in one wave, so that wave
+// takes about half as long.
 template <int BN>
 __device__ __forceinline__ DuoTile duo_tile(const Params& p, int64_t item, uint32_t crank) {
   DuoTile t;
   const int64_t n_pm = (p.num_m_tiles + 1) / 2;
   int64_t pid = item;
-  int part = -1;  // -1: the whole tile; else which of its split_parts column ranges
+  int half = -1;  // -1: the whole tile; 0 / 1: its left / right half
   if (item >= p.split_from) {
-    const int64_t r = item - p.split_from;
-    pid = p.split_from + r / p.split_parts;
-    part = static_cast<int>(r % p.split_parts);
+    pid = p.split_from + (item - p.split_from) / 2;
+    half = static_cast<int>((item - p.split_from) & 1);
   }
   t.live = pid < n_pm * p.num_n_tiles;
   if (!t.live) return t;
@@ -681,8 +673,8 @@ __device__ __forceinline__ DuoTile duo_tile(const Params& p, int64_t item, uint3
   const int64_t nt = (pid % band) / gp;
   t.mt = 2 * pm + crank;
   t.m0 = t.mt * BM;
-  t.width = part < 0 ? BN : BN / p.split_parts;
-  t.n0 = nt * BN + (part > 0 ? part * t.width : 0);
+  t.width = half < 0 ? BN : BN / 2;
+  t.n0 = nt * BN + (half > 0 ? BN / 2 : 0);
   t.sfb_tile = t.n0 / 128;
   t.sfb_shift = static_cast<int>((t.n0 % 128) / 32);
   const int64_t left = p.M - t.m0;
@@ -805,8 +797,9 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
   uint64_t* mma_done = acc_empty + D::kAcc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + D::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + D::kOffMisc + 4);
-  // drain records: [0] / [1] stage uses issued by the producer of CTA 0 / 1 (the leader's
-  // copy), [2] stage uses consumed by the MMA issuer, [3] accumulator commits (both copies)
+  // drain records, in both CTAs: [0] / [1] stage uses issued by the producer of CTA 0 / 1,
+  // [2] stage uses consumed by the MMA issuer, [3] accumulator commits; [4] this CTA's
+  // producer tail completed
   volatile uint32_t* rec = reinterpret_cast<volatile uint32_t*>(smem + D::kOffMisc + 8);
 
   const int warp = threadIdx.x >> 5;
@@ -905,13 +898,10 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
             tma_load_3d_2sm(smem + D::kOffB + s * D::kBBytes, &map_b, kx,
                             static_cast<int32_t>(t.n0 + crank * (BN / 2)), t.b_z, bar);
           else if constexpr (D::kWide) {
-            // rows 96c.. of each 192-column half of the pair tile. A split tile uses the
-            // first box only, which then starts at its own B rows (c * width / 2: 96 for a
-            // half, 64 for a third); the second box is loaded all the same, as the byte
-            // count expects.
+            // rows 96c.. of each 192-column half of the pair tile (a half tile uses the
+            // first box only; the second is loaded all the same, as the byte count expects)
             uint8_t* bs = smem + D::kOffB + s * D::kBBytes;
-            const int32_t rows0 = t.width == BN ? 96 : t.width / 2;
-            tma_load_2d_2sm(bs, &map_b, kx, static_cast<int32_t>(t.n0 + rows0 * crank), bar);
+            tma_load_2d_2sm(bs, &map_b, kx, static_cast<int32_t>(t.n0 + 96 * crank), bar);
             tma_load_2d_2sm(bs + 96 * BK, &map_b, kx,
                             static_cast<int32_t>(t.n0 + 192 + 96 * crank), bar);
           } else {
@@ -940,8 +930,18 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
       latch_error(p.status, MXFP8_ERR_TIMEOUT);
     }
     // the copies still in flight are waited for on the way out, by the leader, whose full
-    // barriers count both CTAs' bytes
-    if (issuer) st_cluster_u32(cluster_map(const_cast<uint32_t*>(&rec[crank]), 0), it);
+    // barriers count both CTAs' bytes; both CTAs learn what each producer issued
+    if (issuer)
+      for (uint32_t r = 0; r < 2; ++r)
+        st_cluster_u32(cluster_map(const_cast<uint32_t*>(&rec[crank]), r), it);
+    // Producer tail: the leader's release (a multicast commit) of the last stage uses must
+    // have arrived on this CTA's empty barriers before it exits; those arrivals can land
+    // after the epilogue has seen the last accumulator. Waiting here overlaps the epilogue's
+    // last tile; after an abort the drain below does it instead.
+    bool tail_ok = ok;
+    for (uint32_t i = it > kStages ? it - kStages : 0; tail_ok && i < it; ++i)
+      tail_ok = warp_wait(&empty[i % kStages], (i / kStages) & 1, abort_flag, p.wait_ns);
+    if (issuer) rec[4] = tail_ok ? 1u : 0u;
     __syncwarp();
   } else if (warp == 1 && leader) {
     // ------------------------------------------------------------- MMA issuer (leader)
@@ -957,10 +957,8 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     constexpr uint32_t kId0 = mxf8_idesc(2 * BM, kN, 0, 0), kId1 = mxf8_idesc(2 * BM, kN, 1, 1);
     constexpr uint32_t kId2 = mxf8_idesc(2 * BM, kN, 2, 2), kId3 = mxf8_idesc(2 * BM, kN, 3, 3);
     // half tiles of the 256-wide kernel: N = 128, the same B scale bytes (their columns
-    // start at a 128-row tile); a 384-wide kernel's half tile is its first MMA alone, and
-    // its third is that MMA with N = 128 (its columns start at a 128-row scale tile too)
+    // start at a 128-row tile); a 384-wide kernel's half tile is its first MMA alone
     constexpr uint32_t kHalfN = D::kWide ? 0u : (mxf8_idesc(2 * BM, BN / 2, 0, 0) ^ kId0);
-    constexpr uint32_t kThirdN = D::kWide ? (mxf8_idesc(2 * BM, 128, 0, 0) ^ kId0) : 0u;
     for (int64_t id = first_id; ok; id += id_step) {
       const DuoTile t = duo_tile_of<BN, kMode>(p, seg, id, crank);
       if (!t.live) break;
@@ -973,8 +971,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
       tc_fence_after();
       const uint32_t d_t = tmem + buf * BN;
       const uint32_t shift = static_cast<uint32_t>(t.sfb_shift);
-      // flips the N field to that of a split tile
-      const uint32_t nx = t.width == BN ? 0u : (D::kWide && t.width == 128 ? kThirdN : kHalfN);
+      const uint32_t nx = t.width == BN ? 0u : kHalfN;  // flips the N field to BN / 2
       const bool second = D::kWide && t.width == BN;     // the columns [192, 384) too
       for (int64_t kb = 0; kb < t.nk; ++kb, ++it) {
         const uint32_t s = it % kStages, ph = (it / kStages) & 1;
@@ -1046,20 +1043,11 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     constexpr int kChunks = BN / 64;   // 32-column chunks per warp
     const uint32_t acc_empty0 = cluster_map(&acc_empty[0], 0);
     uint8_t* box = smem + D::kOffOut + (warp - 2) * D::kStageBoxBytes;
-    // On the CTA's last tile the pipeline stages are idle (all MMAs of the pair have
-    // completed, no load is left), so each warp stages every box of that tile in its own
-    // slice of them and issues all its stores back to back: the store latency at the end
-    // of the kernel is paid once per warp instead of once per box.
-    constexpr int kLastBoxes = D::kWide ? 12 : 2 * kChunks;  // boxes per warp at most
-    static_assert(kEpiWarps * kLastBoxes * D::kStageBoxBytes <= D::kOffBar - D::kOffA,
-                  "last-tile boxes must fit in the stage area");
-    uint8_t* const last_boxes = smem + D::kOffA + (warp - 2) * kLastBoxes * D::kStageBoxBytes;
     uint32_t acc_it = 0;
     bool ok = true;
     for (int64_t id = first_id; ok; id += id_step) {
       const DuoTile t = duo_tile_of<BN, kMode>(p, seg, id, crank);
       if (!t.live) break;
-      const bool last = !duo_tile_of<BN, kMode>(p, seg, id + id_step, crank).live;
       if constexpr (D::kWide) {
         // 384-wide (BF16 out): 6 chunks of 32 columns per warp, converted to BF16 pairs as
         // they leave TMEM in 3 rounds of 2 chunks, so that the accumulator is handed back
@@ -1105,21 +1093,16 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
             for (int g = 0; g < 2; ++g) {
               const int col = 32 * (half * 6 + c6) + 16 * g;  // first column of this box
               if (col >= t.cols_valid) continue;
-              uint8_t* bx = box;
-              if (last) {
-                bx = last_boxes + (2 * c6 + g) * D::kStageBoxBytes;
-              } else {
-                if (lane == 0) bulk_wait_read_all();  // the box is free again
-                __syncwarp();
-              }
-              *reinterpret_cast<uint4*>(bx + lane * 32 + 16 * sw) =
+              if (lane == 0) bulk_wait_read_all();  // the box is free again
+              __syncwarp();
+              *reinterpret_cast<uint4*>(box + lane * 32 + 16 * sw) =
                   make_uint4(b[c6][8 * g], b[c6][8 * g + 1], b[c6][8 * g + 2], b[c6][8 * g + 3]);
-              *reinterpret_cast<uint4*>(bx + lane * 32 + 16 * (sw ^ 1)) =
+              *reinterpret_cast<uint4*>(box + lane * 32 + 16 * (sw ^ 1)) =
                   make_uint4(b[c6][8 * g + 4], b[c6][8 * g + 5], b[c6][8 * g + 6], b[c6][8 * g + 7]);
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                tma_store_2d(&map_c, bx, static_cast<int32_t>(t.n0 + col),
+                tma_store_2d(&map_c, box, static_cast<int32_t>(t.n0 + col),
                              static_cast<int32_t>(t.m0 + 32 * q));
                 bulk_commit_group();
               }
@@ -1182,24 +1165,19 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
             }
             const int col = 32 * c + 16 * g;  // first column of this group
             if (p.out_fp32 && col >= t.cols_valid) continue;
-            uint8_t* bx = box;
-            if (last) {
-              bx = last_boxes + (2 * u + g) * D::kStageBoxBytes;
-            } else {
-              if (lane == 0) bulk_wait_read_all();  // the box is free again
-              __syncwarp();
-            }
+            if (lane == 0) bulk_wait_read_all();  // the box is free again
+            __syncwarp();
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4*>(bx + lane * 64 + 16 * (j ^ ((lane >> 1) & 3))) = w[j];
+              *reinterpret_cast<uint4*>(box + lane * 64 + 16 * (j ^ ((lane >> 1) & 3))) = w[j];
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
               if constexpr (kMode == kDense)
-                tma_store_2d(&map_c, bx, static_cast<int32_t>(t.n0 + col),
+                tma_store_2d(&map_c, box, static_cast<int32_t>(t.n0 + col),
                              static_cast<int32_t>(t.m0 + 32 * q));
               else
-                tma_store_3d(&map_c, bx, static_cast<int32_t>(t.n0 + col),
+                tma_store_3d(&map_c, box, static_cast<int32_t>(t.n0 + col),
                              static_cast<int32_t>(t.m0 + 32 * q), t.c_z);
               bulk_commit_group();
             }
@@ -1207,7 +1185,9 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
         }
       }
     }
-    if (lane == 0) bulk_wait_all();  // every store has landed before the CTA can exit
+    // Before the CTA exits its stores must have finished reading its shared memory; the
+    // kernel's completion makes their global writes visible to later work.
+    if (lane == 0) bulk_wait_read_all();
     __syncwarp();
     if (!ok && lane == 0) {
       *abort_flag = 1;
@@ -1225,11 +1205,14 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
   // them to land, so both CTAs' copies are in. Each CTA then waits for the last arrival of
   // the MMA issuer's commits on its own empty and accumulator barriers. The waits have
   // their own limit, never shorter than the pipeline's.
-  if (threadIdx.x == 0) {
-    const uint32_t consumed = rec[2], commits = rec[3];
+  // Without an abort every issued stage use was consumed, the producer's tail has seen the
+  // last releases and the epilogue every accumulator commit: nothing is left to wait for,
+  // and the second cluster barrier is skipped (both CTAs read the same issue counts, so
+  // they take the same branch).
+  const uint32_t i0 = rec[0], i1 = rec[1], consumed = rec[2], commits = rec[3];
+  const uint32_t issued = i0 > i1 ? i0 : i1;
+  if (threadIdx.x == 0 && !(rec[4] && !*abort_flag && issued == consumed)) {
     if (leader) {
-      const uint32_t i0 = rec[0], i1 = rec[1];
-      const uint32_t issued = i0 > i1 ? i0 : i1;
       for (uint32_t i = consumed; i < issued; ++i) {
         uint64_t* b = &full[i % kStages];
         if (i < i0 && i >= i1) mbar_complete_tx(b, D::kStageBytes);
@@ -1242,7 +1225,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     }
   }
   __syncthreads();
-  cluster_sync();  // the leader's drain covered the peer's copies too
+  if (issued > consumed) cluster_sync();  // the leader's drain covered the peer's copies too
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -1444,31 +1427,12 @@ bool half_tail_enabled() {
   return on;
 }
 
-// Thirds of a 384-wide tile for the last wave; MXFP8_GEMM_THIRD_TAIL=0 turns them off.
-bool third_tail_enabled() {
-  static const bool on = [] {
-    const char* e = getenv("MXFP8_GEMM_THIRD_TAIL");
-    return !(e && e[0] == '0');
-  }();
-  return on;
-}
-
-// How many parts each tile of a last wave of `tail` pair tiles (of `clusters` that fit at
-// once) runs as: 3 (384-wide thirds), 2 (halves) or 1 (whole tiles).
-int tail_split_parts(int bn, int64_t tail, int64_t clusters) {
-  if (bn == 192 || tail <= 0 || !half_tail_enabled()) return 1;
-  if (bn == 384 && third_tail_enabled() && 3 * tail <= clusters) return 3;
-  return 2 * tail <= clusters ? 2 : 1;
-}
-
 // Tile width of the 2SM kernel for one problem: 192, 256 or 384 (BF16 output only), the
 // one with the least estimated time. A tile's time per K stage relative to a 256-wide tile,
 // as measured on GB300 (narrow tiles pay the per-stage scale copies and fills over fewer
 // FLOPs; the 384-wide tile, two MMAs sharing A, is slightly cheaper per FLOP): 192 -> 0.78,
 // 256 -> 1, 384 -> 1.46; a last wave of half tiles costs 0.93 (256) or 0.78 (384, two
-// 192-wide halves), one of 384-wide thirds about kThirdCost. MXFP8_GEMM_BN=192, 256 or 384
-// forces a width.
-constexpr double kThirdCost = 0.72;
+// 192-wide halves). MXFP8_GEMM_BN=192, 256 or 384 forces a width.
 int duo_width(int64_t M, int64_t N, bool fp32) {
   static const int forced = [] {
     const char* e = getenv("MXFP8_GEMM_BN");
@@ -1483,8 +1447,8 @@ int duo_width(int64_t M, int64_t N, bool fp32) {
     const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
     const int64_t waves = tiles / clusters, tail = tiles % clusters;
     double t = static_cast<double>(waves) * full;
-    const int parts = tail_split_parts(bn, tail, clusters);
-    if (tail > 0) t += parts == 3 ? kThirdCost : (parts == 2 ? halfc : full);
+    if (tail > 0)
+      t += (bn != 192 && half_tail_enabled() && 2 * tail <= clusters) ? halfc : full;
     return t;
   };
   int best = 256;
@@ -1517,15 +1481,13 @@ int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
   const int64_t pair_tiles = static_cast<int64_t>((p.num_m_tiles + 1) / 2) * p.num_n_tiles;
   const int64_t fit = max_duo_clusters<BN>();
   if (fit <= 0) return MXFP8_ERR_CUDA;
-  // The tiles of the last, partial wave run as narrower tiles when those still fit in one
-  // wave of clusters: thirds of a 384-wide tile, else halves (256- and 384-wide tiles).
+  // The tiles of the last, partial wave run as half-width tiles when their halves still fit
+  // in one wave of clusters (256- and 384-wide tiles).
   int64_t items = pair_tiles;
   const int64_t tail = pair_tiles % fit;
-  const int parts = tail_split_parts(BN, tail, fit);
-  if (parts > 1) {
+  if (BN != 192 && half_tail_enabled() && tail > 0 && 2 * tail <= fit) {
     p.split_from = pair_tiles - tail;
-    p.split_parts = parts;
-    items = pair_tiles + (parts - 1) * tail;
+    items = pair_tiles + tail;
   }
   const int64_t clusters = items < fit ? items : fit;
   if (clusters <= 0) return MXFP8_OK;

@@ -56,9 +56,9 @@ def test_tiny_config_fprop(m):
                                  (2304, 2560, 256), (512, 4608, 256), (512, 4560, 256)])
 def test_shapes_random_operands(m, mnk):
     """Random finite codes and scales spanning 2^-17..2^12: any mistake in the scale
-    layout, a tile origin or a tail mask shows up as a gross error. With 256 x 384 tiles,
-    (512, 4608, 256) has 24 pair tiles, all in the last wave, which run as 72 thirds
-    (256 x 128); (512, 4560, 256) also ends in a ragged third."""
+    layout, a tile origin or a tail mask shows up as a gross error. (512, 4608, 256) and
+    (512, 4560, 256) have all their pair tiles in one partial wave, run as half tiles, the
+    second ending in a ragged half."""
     mm, n, k = mnk
     g = np.random.default_rng(mm * 7 + n * 3 + k)
     qa, sa = _rand_q(g, mm, k)

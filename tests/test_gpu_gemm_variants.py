@@ -1,8 +1,8 @@
 """Every dense GEMM kernel variant through the same oracle parity tests.
 
 The library picks a kernel per problem: the 2SM kernel (tcgen05.mma.cta_group::2) with
-256 x 384 tiles (BF16 output; two N = 192 MMAs sharing A; a last, partial wave as thirds
-or halves), 256 x 256 tiles (a last wave as halves) or 256 x 192 tiles, or the one-SM kernel (128 x 256
+256 x 384 tiles (BF16 output; two N = 192 MMAs sharing A), 256 x 256 tiles (the last,
+partial wave of either as half tiles) or 256 x 192 tiles, or the one-SM kernel (128 x 256
 or 128 x 128 tiles); grouped (MoE) GEMMs run on the 2SM kernel too, or on the one-SM
 kernel. The choice is read from the environment once per process, so each forced
 variant runs the parity tests of test_gpu_gemm.py in a child process. The shapes there
@@ -26,8 +26,6 @@ VARIANTS = {
     "2sm_384": {"MXFP8_GEMM_2SM": "1", "MXFP8_GEMM_BN": "384"},
     "2sm_384_whole_tiles": {"MXFP8_GEMM_2SM": "1", "MXFP8_GEMM_BN": "384",
                             "MXFP8_GEMM_HALF_TAIL": "0"},
-    "2sm_384_halves": {"MXFP8_GEMM_2SM": "1", "MXFP8_GEMM_BN": "384",
-                       "MXFP8_GEMM_THIRD_TAIL": "0"},
     "1sm": {"MXFP8_GEMM_2SM": "0"},
 }
 SELECT = ("shapes_random_operands or extreme_scales or small_layer or layer_set_full_size "
@@ -37,8 +35,7 @@ SELECT = ("shapes_random_operands or extreme_scales or small_layer or layer_set_
 @pytest.mark.parametrize("name", sorted(VARIANTS))
 def test_gemm_variant_parity(name):
     env = dict(os.environ)
-    for key in ("MXFP8_GEMM_2SM", "MXFP8_GEMM_BN", "MXFP8_GEMM_HALF_TAIL", "MXFP8_GEMM_WIDE",
-                "MXFP8_GEMM_THIRD_TAIL"):
+    for key in ("MXFP8_GEMM_2SM", "MXFP8_GEMM_BN", "MXFP8_GEMM_HALF_TAIL", "MXFP8_GEMM_WIDE"):
         env.pop(key, None)
     env.update(VARIANTS[name])
     cmd = [sys.executable, "-m", "pytest", "tests/test_gpu_gemm.py", "-q", "-x", "-m", "gpu",

@@ -1,11 +1,12 @@
 """Failure detection of the GEMM pipeline without a GPU fault: a wait that runs out.
 
 Every mbarrier wait in the GEMM kernels is bounded. With the pipeline limit set far below
-one tile's computation (100 ns), the epilogue's wait for its first accumulator runs out,
-the kernel latches MXFP8_ERR_TIMEOUT, stops issuing, waits for the copies and tensor-core
-operations it has in flight (under its own drain limit of at least 2 s) and returns. The
-context stays usable: with the default limit restored, the same GEMM matches the oracle and
-the status word stays clear. The post lists the failures a pipeline must survive in its
+one tile's computation (100 ns; the kernel notices it within a few polls of its barrier,
+each of which may suspend the thread briefly), the epilogue's wait for its first
+accumulator runs out. The kernel latches MXFP8_ERR_TIMEOUT, stops issuing, waits for the
+copies and tensor-core operations it has in flight (under its own drain limit of at least
+2 s) and returns. The context stays usable: with the default limit restored, the same GEMM
+matches the oracle and the status word stays clear. The post lists the failures a pipeline must survive in its
 section "Correctness: how it fails"; this is the library's own bounded-wait path, not a
 fault. It runs in a child process, so the rest of the suite keeps its own CUDA context.
 """
@@ -51,7 +52,9 @@ CHILD = textwrap.dedent(r"""
     counts = [300, 0, 700, 64, 1000]
     off = np.concatenate([[0], np.cumsum([(c + 31) // 32 * 32 for c in counts])]).astype(np.int32)
     offs = torch.from_numpy(off).to(dev)
-    total, kk, nn = int(off[-1]), 2048, 1536
+    # a long reduction (K = 16384: every pair tile takes tens of microseconds) so that the
+    # epilogue's first wait certainly outlasts the limit and the time it takes to notice it
+    total, kk, nn = int(off[-1]), 16384, 1536
     x = torch.randn((total, kk), generator=g, device=dev).to(torch.bfloat16)
     w = (torch.randn((len(counts), nn, kk), generator=g, device=dev) * 0.02).to(torch.bfloat16)
     qx, sx = m.quantize_grouped(x, offs, m.ROW)
