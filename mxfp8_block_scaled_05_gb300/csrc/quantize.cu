@@ -118,6 +118,8 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+
+
 // Scale byte from the largest |BF16| bits of a block; 0xFF for a NaN/Inf block.
 // Floor rule (OCP): floor(log2 amax) - 8 = biased exponent - 135, byte = E - 8.
 // Round-up rule: one more when the mantissa of amax exceeds 1.75 (amax > 448 * 2^e), so
@@ -210,6 +212,145 @@ struct QJobs {
   uint8_t* scales_col[kMaxQuantizeJobs];
   int64_t tile_base[kMaxQuantizeJobs + 1];
 };
+
+// Row-wise copy of a 128 x 128 tile staged in shared memory: one thread per 32-block (8
+// consecutive rows per 8 lanes, conflict-free with the padded pitch), 32 code bytes per
+// thread; the scale bytes go to the 512-byte tile stile_r (swizzled) or straight out.
+template <bool kSwizzled>
+__device__ __forceinline__ void row_pass_smem(const uint16_t (*tile)[kTilePitch],
+                                              uint8_t* stile_r, const QOut& ro, int64_t cols,
+                                              int64_t row0, int rows_valid, int64_t col0,
+                                              int cols_valid, int rule) {
+  const int t = threadIdx.x;
+  const int64_t s_cols = cols / 32;
+  const int w = t >> 5, l = t & 31;
+  const int b = l >> 3;
+  const bool block_ok = 32 * b < cols_valid;
+  const bool wide = (reinterpret_cast<uintptr_t>(ro.codes) & 31) == 0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = 8 * w + (l & 7) + 64 * i;
+    const uint4* rp = reinterpret_cast<const uint4*>(&tile[r][32 * b]);
+    const uint4 x0 = rp[0], x1 = rp[1], x2 = rp[2], x3 = rp[3];
+    uint32_t m2 = max_abs_bf16x2(
+        max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(x0.x, x0.y), max_abs_bf16x2(x0.z, x0.w)),
+                       max_abs_bf16x2(max_abs_bf16x2(x1.x, x1.y), max_abs_bf16x2(x1.z, x1.w))),
+        max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(x2.x, x2.y), max_abs_bf16x2(x2.z, x2.w)),
+                       max_abs_bf16x2(max_abs_bf16x2(x3.x, x3.y), max_abs_bf16x2(x3.z, x3.w))));
+    m2 &= kAbs2;
+    const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    const bool valid = block_ok && r < rows_valid;
+    const uint32_t s = scale_byte(m, rule);
+    if (valid) {
+      uint32_t o[8];
+      if (__builtin_expect(s != 0xFFu, 1)) {
+        const float mul = inv_scale(s);
+        o[0] = e4m3x4(x0.x, x0.y, mul); o[1] = e4m3x4(x0.z, x0.w, mul);
+        o[2] = e4m3x4(x1.x, x1.y, mul); o[3] = e4m3x4(x1.z, x1.w, mul);
+        o[4] = e4m3x4(x2.x, x2.y, mul); o[5] = e4m3x4(x2.z, x2.w, mul);
+        o[6] = e4m3x4(x3.x, x3.y, mul); o[7] = e4m3x4(x3.z, x3.w, mul);
+      } else {
+        o[0] = nan4(x0.x, x0.y); o[1] = nan4(x0.z, x0.w);
+        o[2] = nan4(x1.x, x1.y); o[3] = nan4(x1.z, x1.w);
+        o[4] = nan4(x2.x, x2.y); o[5] = nan4(x2.z, x2.w);
+        o[6] = nan4(x3.x, x3.y); o[7] = nan4(x3.z, x3.w);
+      }
+      uint8_t* dst = ro.codes + (row0 + r) * cols + col0 + 32 * b;
+      if (wide) {
+        st_global_v8(dst, o);
+      } else {
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    }
+    if (kSwizzled)
+      stile_r[(r & 31) * 16 + (r >> 5) * 4 + b] = valid ? static_cast<uint8_t>(s) : 0;
+    else if (valid)
+      ro.scales[(row0 + r) * s_cols + col0 / 32 + b] = static_cast<uint8_t>(s);
+  }
+}
+
+// Column-wise copy (transpose) of a 128 x 128 tile staged in shared memory; the tile
+// buffer is reused to stage the transposed codes, so it is dead once this returns.
+template <bool kSwizzled>
+__device__ __forceinline__ void col_pass_smem(uint16_t (*tile)[kTilePitch], uint8_t* stile_c,
+                                              const QOut& co, int64_t rows, int64_t row0,
+                                              int rows_valid, int64_t col0, int cols_valid,
+                                              int rule) {
+  const int t = threadIdx.x;
+  // thread = column pair (2cp, 2cp+1) x token block j (32 rows); each word read holds
+  // both columns of one row (column c in the low half)
+  const int w = t >> 5, lane = t & 31;
+  const int cp = (w & 1) * 32 + lane;
+  const int j = w >> 1;
+  const int c = 2 * cp;
+  const bool valid = c < cols_valid && 32 * j < rows_valid;
+  const uint32_t* colw = reinterpret_cast<const uint32_t*>(&tile[32 * j][c]);
+  constexpr int kRowWords = kTilePitch / 2;
+  uint32_t m01 = 0;  // both columns' block maxima, one per half
+#pragma unroll
+  for (int i = 0; i < 32; ++i) m01 = max_abs_bf16x2(m01, colw[i * kRowWords]);
+  m01 &= kAbs2;
+  const uint32_t s0 = scale_byte(m01 & 0xFFFFu, rule), s1 = scale_byte(m01 >> 16, rule);
+  uint4 stage_o0[2], stage_o1[2];
+  if (valid) {
+    const float mul0 = inv_scale(s0), mul1 = inv_scale(s1);
+    uint32_t o0[8], o1[8];
+    if (__builtin_expect(s0 != 0xFFu && s1 != 0xFFu, 1)) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t a0 = colw[(4 * q) * kRowWords], a1 = colw[(4 * q + 1) * kRowWords];
+        const uint32_t a2 = colw[(4 * q + 2) * kRowWords], a3 = colw[(4 * q + 3) * kRowWords];
+        // column c: low halves; column c+1: high halves
+        o0[q] = e4m3x4_col<false>(a0, a1, a2, a3, mul0);
+        o1[q] = e4m3x4_col<true>(a0, a1, a2, a3, mul1);
+      }
+    } else {  // a NaN/Inf block in either column (rare)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t a0 = colw[(4 * q) * kRowWords], a1 = colw[(4 * q + 1) * kRowWords];
+        const uint32_t a2 = colw[(4 * q + 2) * kRowWords], a3 = colw[(4 * q + 3) * kRowWords];
+        const uint32_t c0a = __byte_perm(a0, a1, 0x5410), c0b = __byte_perm(a2, a3, 0x5410);
+        const uint32_t c1a = __byte_perm(a0, a1, 0x7632), c1b = __byte_perm(a2, a3, 0x7632);
+        o0[q] = s0 == 0xFFu ? nan4(c0a, c0b) : e4m3x4(c0a, c0b, mul0);
+        o1[q] = s1 == 0xFFu ? nan4(c1a, c1b) : e4m3x4(c1a, c1b, mul1);
+      }
+    }
+    stage_o0[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+    stage_o0[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
+    stage_o1[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+    stage_o1[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+  }
+  if (kSwizzled) {
+    stile_c[(c & 31) * 16 + (c >> 5) * 4 + j] = valid ? static_cast<uint8_t>(s0) : 0;
+    stile_c[((c + 1) & 31) * 16 + ((c + 1) >> 5) * 4 + j] = valid ? static_cast<uint8_t>(s1) : 0;
+  } else if (valid) {
+    const int64_t s_cols = rows / 32;
+    co.scales[(col0 + c) * s_cols + row0 / 32 + j] = static_cast<uint8_t>(s0);
+    co.scales[(col0 + c + 1) * s_cols + row0 / 32 + j] = static_cast<uint8_t>(s1);
+  }
+  // The transposed codes go through shared memory so that each output row's 128 bytes
+  // leave in one coalesced piece: stage[row][chunk] holds 16-byte chunks, chunk index
+  // XOR (row & 7) against bank conflicts; the BF16 tile buffer is reused once every
+  // thread has read what it needs of it.
+  __syncthreads();
+  uint4* stage = reinterpret_cast<uint4*>(&tile[0][0]);
+  if (valid) {
+    stage[c * 8 + ((2 * j) ^ (c & 7))] = stage_o0[0];
+    stage[c * 8 + ((2 * j + 1) ^ (c & 7))] = stage_o0[1];
+    stage[(c + 1) * 8 + ((2 * j) ^ ((c + 1) & 7))] = stage_o1[0];
+    stage[(c + 1) * 8 + ((2 * j + 1) ^ ((c + 1) & 7))] = stage_o1[1];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = (t >> 3) + 32 * i;  // output row = tile column
+    const int ch = t & 7;             // 16 tokens per chunk
+    if (r < cols_valid && 16 * ch < rows_valid)
+      *reinterpret_cast<uint4*>(co.codes + (col0 + r) * rows + row0 + 16 * ch) =
+          stage[r * 8 + (ch ^ (r & 7))];
+  }
+}
 
 template <bool kRow, bool kCol, bool kSwizzled, bool kGrouped, bool kMulti>
 __global__ void __launch_bounds__(kThreads, kCol ? 6 : 1)
@@ -307,56 +448,9 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
     }
   }
 
-  // ---- row-wise copy from the shared tile: one thread per 32-block (8 consecutive rows
-  // per 8 lanes, conflict-free with the padded pitch), 32 code bytes per thread
-  if (kRow && kCol) {
-    const int64_t s_cols = cols / 32;
-    const int w = t >> 5, l = t & 31;
-    const int b = l >> 3;
-    const bool block_ok = 32 * b < cols_valid;
-    const bool wide = (reinterpret_cast<uintptr_t>(ro.codes) & 31) == 0;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int r = 8 * w + (l & 7) + 64 * i;
-      const uint4* rp = reinterpret_cast<const uint4*>(&tile[r][32 * b]);
-      const uint4 x0 = rp[0], x1 = rp[1], x2 = rp[2], x3 = rp[3];
-      uint32_t m2 = max_abs_bf16x2(
-          max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(x0.x, x0.y), max_abs_bf16x2(x0.z, x0.w)),
-                         max_abs_bf16x2(max_abs_bf16x2(x1.x, x1.y), max_abs_bf16x2(x1.z, x1.w))),
-          max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(x2.x, x2.y), max_abs_bf16x2(x2.z, x2.w)),
-                         max_abs_bf16x2(max_abs_bf16x2(x3.x, x3.y), max_abs_bf16x2(x3.z, x3.w))));
-      m2 &= kAbs2;
-      const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-      const bool valid = block_ok && r < rows_valid;
-      const uint32_t s = scale_byte(m, rule);
-      if (valid) {
-        uint32_t o[8];
-        if (__builtin_expect(s != 0xFFu, 1)) {
-          const float mul = inv_scale(s);
-          o[0] = e4m3x4(x0.x, x0.y, mul); o[1] = e4m3x4(x0.z, x0.w, mul);
-          o[2] = e4m3x4(x1.x, x1.y, mul); o[3] = e4m3x4(x1.z, x1.w, mul);
-          o[4] = e4m3x4(x2.x, x2.y, mul); o[5] = e4m3x4(x2.z, x2.w, mul);
-          o[6] = e4m3x4(x3.x, x3.y, mul); o[7] = e4m3x4(x3.z, x3.w, mul);
-        } else {
-          o[0] = nan4(x0.x, x0.y); o[1] = nan4(x0.z, x0.w);
-          o[2] = nan4(x1.x, x1.y); o[3] = nan4(x1.z, x1.w);
-          o[4] = nan4(x2.x, x2.y); o[5] = nan4(x2.z, x2.w);
-          o[6] = nan4(x3.x, x3.y); o[7] = nan4(x3.z, x3.w);
-        }
-        uint8_t* dst = ro.codes + (row0 + r) * cols + col0 + 32 * b;
-        if (wide) {
-          st_global_v8(dst, o);
-        } else {
-          reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-          reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        }
-      }
-      if (kSwizzled)
-        stile_r[(r & 31) * 16 + (r >> 5) * 4 + b] = valid ? static_cast<uint8_t>(s) : 0;
-      else if (valid)
-        ro.scales[(row0 + r) * s_cols + col0 / 32 + b] = static_cast<uint8_t>(s);
-    }
-  }
+  // ---- row-wise copy from the shared tile
+  if constexpr (kRow && kCol)
+    row_pass_smem<kSwizzled>(tile, stile_r, ro, cols, row0, rows_valid, col0, cols_valid, rule);
 
   // ---- row-wise copy from registers: the 4 lanes of a 32-block share amax
   if (kRow && !kCol) {
@@ -395,80 +489,8 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
   }
 
   // ---- column-wise copy from the shared tile (transpose)
-  if (kCol) {
-    // thread = column pair (2cp, 2cp+1) x token block j (32 rows); each word read holds
-    // both columns of one row (column c in the low half)
-    const int w = t >> 5, lane = t & 31;
-    const int cp = (w & 1) * 32 + lane;
-    const int j = w >> 1;
-    const int c = 2 * cp;
-    const bool valid = c < cols_valid && 32 * j < rows_valid;
-    const uint32_t* colw = reinterpret_cast<const uint32_t*>(&tile[32 * j][c]);
-    constexpr int kRowWords = kTilePitch / 2;
-    uint32_t m01 = 0;  // both columns' block maxima, one per half
-#pragma unroll
-    for (int i = 0; i < 32; ++i) m01 = max_abs_bf16x2(m01, colw[i * kRowWords]);
-    m01 &= kAbs2;
-    const uint32_t s0 = scale_byte(m01 & 0xFFFFu, rule), s1 = scale_byte(m01 >> 16, rule);
-    uint4 stage_o0[2], stage_o1[2];
-    if (valid) {
-      const float mul0 = inv_scale(s0), mul1 = inv_scale(s1);
-      uint32_t o0[8], o1[8];
-      if (__builtin_expect(s0 != 0xFFu && s1 != 0xFFu, 1)) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint32_t a0 = colw[(4 * q) * kRowWords], a1 = colw[(4 * q + 1) * kRowWords];
-          const uint32_t a2 = colw[(4 * q + 2) * kRowWords], a3 = colw[(4 * q + 3) * kRowWords];
-          // column c: low halves; column c+1: high halves
-          o0[q] = e4m3x4_col<false>(a0, a1, a2, a3, mul0);
-          o1[q] = e4m3x4_col<true>(a0, a1, a2, a3, mul1);
-        }
-      } else {  // a NaN/Inf block in either column (rare)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint32_t a0 = colw[(4 * q) * kRowWords], a1 = colw[(4 * q + 1) * kRowWords];
-          const uint32_t a2 = colw[(4 * q + 2) * kRowWords], a3 = colw[(4 * q + 3) * kRowWords];
-          const uint32_t c0a = __byte_perm(a0, a1, 0x5410), c0b = __byte_perm(a2, a3, 0x5410);
-          const uint32_t c1a = __byte_perm(a0, a1, 0x7632), c1b = __byte_perm(a2, a3, 0x7632);
-          o0[q] = s0 == 0xFFu ? nan4(c0a, c0b) : e4m3x4(c0a, c0b, mul0);
-          o1[q] = s1 == 0xFFu ? nan4(c1a, c1b) : e4m3x4(c1a, c1b, mul1);
-        }
-      }
-      stage_o0[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-      stage_o0[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
-      stage_o1[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-      stage_o1[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
-    }
-    if (kSwizzled) {
-      stile_c[(c & 31) * 16 + (c >> 5) * 4 + j] = valid ? static_cast<uint8_t>(s0) : 0;
-      stile_c[((c + 1) & 31) * 16 + ((c + 1) >> 5) * 4 + j] = valid ? static_cast<uint8_t>(s1) : 0;
-    } else if (valid) {
-      const int64_t s_cols = rows / 32;
-      co.scales[(col0 + c) * s_cols + row0 / 32 + j] = static_cast<uint8_t>(s0);
-      co.scales[(col0 + c + 1) * s_cols + row0 / 32 + j] = static_cast<uint8_t>(s1);
-    }
-    // The transposed codes go through shared memory so that each output row's 128 bytes
-    // leave in one coalesced piece: stage[row][chunk] holds 16-byte chunks, chunk index
-    // XOR (row & 7) against bank conflicts; the BF16 tile buffer is reused once every
-    // thread has read what it needs of it.
-    __syncthreads();
-    uint4* stage = reinterpret_cast<uint4*>(&tile[0][0]);
-    if (valid) {
-      stage[c * 8 + ((2 * j) ^ (c & 7))] = stage_o0[0];
-      stage[c * 8 + ((2 * j + 1) ^ (c & 7))] = stage_o0[1];
-      stage[(c + 1) * 8 + ((2 * j) ^ ((c + 1) & 7))] = stage_o1[0];
-      stage[(c + 1) * 8 + ((2 * j + 1) ^ ((c + 1) & 7))] = stage_o1[1];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = (t >> 3) + 32 * i;  // output row = tile column
-      const int ch = t & 7;             // 16 tokens per chunk
-      if (r < cols_valid && 16 * ch < rows_valid)
-        *reinterpret_cast<uint4*>(co.codes + (col0 + r) * rows + row0 + 16 * ch) =
-            stage[r * 8 + (ch ^ (r & 7))];
-    }
-  }
+  if constexpr (kCol)
+    col_pass_smem<kSwizzled>(tile, stile_c, co, rows, row0, rows_valid, col0, cols_valid, rule);
 
   // ---- the tile's swizzled scale tiles, 16 bytes per thread
   if (kSwizzled) {
