@@ -6,13 +6,16 @@ row-wise and column-wise, then the fprop, dgrad and wgrad block-scaled GEMMs run
 Per step and layer (qkv 4096->6144, o 4096->4096, gate_up 4096->24576, down 12288->4096):
 two dual quantize launches (X and W together, as the forward pass has them; dY alone, as
 the backward pass has it), each giving both copies from one read, and 3 GEMM launches;
-20 launches per step (--quant separate: 6 single-axis quantizes per layer). Inputs are synthetic
+20 launches per step (--quant separate: 6 single-axis quantizes per layer). A layer's
+wgrad needs only the quantized copies, not the fprop or dgrad results, so it runs on a
+second stream beside them (--streams 1 keeps every launch on one stream); the per-launch
+split is measured with every launch on one stream. Inputs are synthetic
 (seeded, BF16) and live in HBM before the timed region; the step's working set (453 MB
 of BF16 inputs) is larger than L2, so no flush is needed between steps.
 
 Output: one JSON line (rank 0). `value` is the step's MXFP8 GEMM FLOPs divided by the
-step time (quantization included), in TFLOP/s, with the step's 20 launches issued on one
-stream (`cuda_graph` gives the same step replayed from a CUDA graph). The `quantize` and
+step time (quantization included), in TFLOP/s, with the step's 20 launches issued as
+above (`cuda_graph` gives the same step replayed from a CUDA graph). The `quantize` and
 `gemm` objects split the time, from CUDA events around every launch of further steps;
 `roofline` is for the dominant kernel (the GEMM) and `roofline_quantize` for the quantizer.
 `secondary` measures the other configurations after the headline, on the same GPU: the
@@ -169,9 +172,13 @@ class DenseStep:
     """Buffers and launches of one step over dense linear layers (name, N, K, X, W, dY);
     every launch goes through the C ABI."""
 
-    def __init__(self, m, layers, dev, dual: bool = True):
+    def __init__(self, m, layers, dev, dual: bool = True, streams: int = 1):
         self.m = m
         self.dual = dual
+        # streams == 2: each layer's wgrad runs on a second stream, beside its fprop and dgrad
+        # (they only share the quantized inputs), so that one GEMM's partial last wave of
+        # clusters overlaps the next GEMM's first one
+        self.side = torch.cuda.Stream(device=dev) if streams == 2 else None
         self.layers = []
         for name, n, k, x, w, dy in layers:
             t = x.shape[0]
@@ -192,10 +199,15 @@ class DenseStep:
         self.launches = (5 if dual else 9) * len(self.layers)
 
     def run(self, stream, events=None):
-        """Enqueues one step. With `events` (a list), appends (kind, units, start, end)."""
+        """Enqueues one step. With `events` (a list), appends (kind, units, start, end); the
+        per-launch events keep every launch on `stream`."""
+        side = self.side if events is None else None
+        done = None
         for L in self.layers:
             self.run_quantize(L, stream, events)
-            self.run_gemms(L, stream, events)
+            done = self.run_gemms(L, stream, events, side=side) or done
+        if done is not None:
+            stream.wait_event(done)  # the side stream rejoins before the step ends
 
     def run_quantize(self, L, stream, events=None):
         """The layer's quantize launches (they read x, w and dy)."""
@@ -227,17 +239,29 @@ class DenseStep:
                 m.quantize(src, axis, m.SWIZZLED, out=q, scales=s, stream=stream)
                 self._end(events, stream, ev)
 
-    def run_gemms(self, L, stream, events=None):
-        """The layer's three GEMMs (they write y, dx and dw)."""
+    def run_gemms(self, L, stream, events=None, side=None):
+        """The layer's three GEMMs (they write y, dx and dw). With a `side` stream the wgrad
+        runs there, after the layer's quantize launches; returns the event that marks its
+        end (None without a side stream)."""
         m = self.m
         t, n, k = L["t"], L["n"], L["k"]
+        done = None
+        if side is not None:
+            quantized = torch.cuda.Event()
+            quantized.record(stream)
+            side.wait_event(quantized)
         for op, a, b, out, mnk in ((m.FPROP, "xr", "wr", L["y"], (t, n, k)),
                                    (m.DGRAD, "dyr", "wc", L["dx"], (t, k, n)),
                                    (m.WGRAD, "dyc", "xc", L["dw"], (n, k, t))):
-            ev = self._ev(events, stream, "gemm", 2.0 * mnk[0] * mnk[1] * mnk[2],
+            st = side if (side is not None and op == m.WGRAD) else stream
+            ev = self._ev(events, st, "gemm", 2.0 * mnk[0] * mnk[1] * mnk[2],
                           f"{L['name']}.{('fprop', 'dgrad', 'wgrad')[op]} {mnk[0]}x{mnk[1]}x{mnk[2]}")
-            m.gemm(L[a][0], L[a][1], L[b][0], L[b][1], op, m.OUT_BF16, out=out, stream=stream)
-            self._end(events, stream, ev)
+            m.gemm(L[a][0], L[a][1], L[b][0], L[b][1], op, m.OUT_BF16, out=out, stream=st)
+            self._end(events, st, ev)
+            if st is side:
+                done = torch.cuda.Event()
+                done.record(side)
+        return done
 
     @staticmethod
     def _ev(events, stream, kind, units, label=""):
@@ -379,7 +403,7 @@ def run_ours(args, rank, ws):
     pk = peaks()
     from mxfp8_block_scaled_05_gb300 import workloads as W
     step = DenseStep(m, W.qwen3_8b_layer_set(args.tokens, dev, seed=1 + rank), dev,
-                     dual=args.quant == "dual")
+                     dual=args.quant == "dual", streams=args.streams)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         step.run(stream)
@@ -483,7 +507,9 @@ def run_ours(args, rank, ws):
         "e2e": e2e,
         "per_launch": breakdown,
         "calibration": cal,
-        "execution": "20 launches per step issued on one stream",
+        "execution": ("20 launches per step; each layer's wgrad on a second stream beside its "
+                      "fprop and dgrad" if args.streams == 2 else
+                      "20 launches per step issued on one stream"),
         "cuda_graph": {"ms_per_step": graph_ms,
                        "value": ws * step.flops / (graph_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                        "note": "the same step captured once in a CUDA graph and replayed"},
@@ -957,6 +983,9 @@ def main():
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--quant", choices=("dual", "separate"), default="dual",
                     help="quantize each tensor once for both copies (dual) or per copy")
+    ap.add_argument("--streams", type=int, choices=(1, 2), default=2,
+                    help="2 (default): each layer's wgrad on a second stream beside its fprop "
+                         "and dgrad; 1: every launch on one stream")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the secondary configurations after the headline line")
     args = ap.parse_args()
