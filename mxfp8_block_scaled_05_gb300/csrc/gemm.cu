@@ -148,13 +148,17 @@ __device__ Tile make_tile(const Params& p, const SegShared* seg, int64_t id) {
     if (id >= p.num_tiles) return t;
     // banded raster: bands of p.band M tiles sweep across N, M fastest within a band, so
     // that concurrent CTAs share operand tiles in L2 (the band width is chosen on the host)
-    const int64_t GM = p.band;
-    const int64_t band = GM * p.num_n_tiles;
-    const int64_t g = id / band;
-    const int64_t first_m = g * GM;
-    const int64_t gm = (p.num_m_tiles - first_m) < GM ? (p.num_m_tiles - first_m) : GM;
-    const int64_t mt = first_m + (id % band) % gm;
-    const int64_t nt = (id % band) / gm;
+    // 32-bit arithmetic: the host keeps tile counts below 2^31
+    const uint32_t uid = static_cast<uint32_t>(id);
+    const uint32_t GM = static_cast<uint32_t>(p.band);
+    const uint32_t band = GM * static_cast<uint32_t>(p.num_n_tiles);
+    const uint32_t g = uid / band, r = uid - g * band;
+    const uint32_t first_m = g * GM;
+    const uint32_t gm = (static_cast<uint32_t>(p.num_m_tiles) - first_m) < GM
+                            ? (static_cast<uint32_t>(p.num_m_tiles) - first_m) : GM;
+    const uint32_t nt32 = r / gm;
+    const int64_t mt = first_m + (r - nt32 * gm);
+    const int64_t nt = nt32;
     t.m0 = mt * BM;
     t.n0 = nt * BN;
     t.rows_valid = static_cast<int>((p.M - t.m0) < BM ? (p.M - t.m0) : BM);
@@ -175,8 +179,9 @@ __device__ Tile make_tile(const Params& p, const SegShared* seg, int64_t id) {
   if (kMode == kGroupRows) {
     const int64_t n_tiles = static_cast<int64_t>(seg->tile_base[p.E]) * p.num_n_tiles;
     if (!seg->ok || id >= n_tiles) return t;
-    const int64_t row_tile = id / p.num_n_tiles;
-    const int64_t nt = id % p.num_n_tiles;
+    const uint32_t uid = static_cast<uint32_t>(id), nnt = static_cast<uint32_t>(p.num_n_tiles);
+    const int64_t row_tile = uid / nnt;
+    const int64_t nt = uid - static_cast<uint32_t>(row_tile) * nnt;
     const int e = find_seg(*seg, p.E, row_tile);
     const int64_t i = row_tile - seg->tile_base[e];
     t.m0 = seg->off[e] + i * BM;
@@ -203,9 +208,12 @@ __device__ Tile make_tile(const Params& p, const SegShared* seg, int64_t id) {
   // spreads the long reductions evenly (longest-processing-time-first order).
   const int64_t per = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
   if (!seg->ok || id >= per * p.E) return t;
-  const int e = seg->order[id / per];
-  const int64_t r = id % per;
-  const int64_t mt = r / p.num_n_tiles, nt = r % p.num_n_tiles;
+  const uint32_t uid = static_cast<uint32_t>(id), uper = static_cast<uint32_t>(per);
+  const uint32_t nnt = static_cast<uint32_t>(p.num_n_tiles);
+  const uint32_t ei = uid / uper, r = uid - ei * uper;
+  const int e = seg->order[ei];
+  const uint32_t mt32 = r / nnt;
+  const int64_t mt = mt32, nt = r - mt32 * nnt;
   const int64_t cnt = seg->off[e + 1] - seg->off[e];
   const int64_t nk = (cnt + BK - 1) / BK;
   t.m0 = mt * BM;
@@ -653,24 +661,29 @@ struct DuoTile {
 // items share one pair tile, each taking half of its columns (256 x BN/2). The host puts the
 // split at the last, partial wave of clusters when its halves fit in one wave, so that wave
 // takes about half as long.
+// The work-item arithmetic is 32-bit: the host checks that the pair tiles and items of a
+// launch stay below 2^31, and 64-bit divisions (emulated in software) cost every role a
+// visible delay before its first tile.
 template <int BN>
 __device__ __forceinline__ DuoTile duo_tile(const Params& p, int64_t item, uint32_t crank) {
   DuoTile t;
-  const int64_t n_pm = (p.num_m_tiles + 1) / 2;
-  int64_t pid = item;
+  const uint32_t n_pm = static_cast<uint32_t>((p.num_m_tiles + 1) / 2);
+  uint32_t pid = static_cast<uint32_t>(item);
   int half = -1;  // -1: the whole tile; 0 / 1: its left / right half
   if (item >= p.split_from) {
-    pid = p.split_from + (item - p.split_from) / 2;
-    half = static_cast<int>((item - p.split_from) & 1);
+    const uint32_t r = static_cast<uint32_t>(item - p.split_from);
+    pid = static_cast<uint32_t>(p.split_from) + r / 2;
+    half = static_cast<int>(r & 1);
   }
-  t.live = pid < n_pm * p.num_n_tiles;
+  t.live = pid < n_pm * static_cast<uint32_t>(p.num_n_tiles);
   if (!t.live) return t;
-  const int64_t GP = p.band;  // bands of p.band pair rows sweep across N, pair rows fastest
-  const int64_t band = GP * p.num_n_tiles;
-  const int64_t first = (pid / band) * GP;
-  const int64_t gp = (n_pm - first) < GP ? (n_pm - first) : GP;
-  const int64_t pm = first + (pid % band) % gp;
-  const int64_t nt = (pid % band) / gp;
+  const uint32_t GP = static_cast<uint32_t>(p.band);  // bands of GP pair rows sweep across
+  const uint32_t band = GP * static_cast<uint32_t>(p.num_n_tiles);  // N, pair rows fastest
+  const uint32_t bi = pid / band, r = pid - bi * band;
+  const uint32_t first = bi * GP;
+  const uint32_t gp = (n_pm - first) < GP ? (n_pm - first) : GP;
+  const uint32_t nt = r / gp;
+  const int64_t pm = first + (r - nt * gp);
   t.mt = 2 * pm + crank;
   t.m0 = t.mt * BM;
   t.width = half < 0 ? BN : BN / 2;
@@ -703,7 +716,9 @@ __device__ DuoTile duo_tile_grouped(const Params& p, const DuoSeg* seg, int64_t 
   if (kMode == kGroupRows) {
     const int64_t total = static_cast<int64_t>(seg->pair_base[E]) * p.num_n_tiles;
     if (pid >= total) return t;
-    const int64_t rp = pid / p.num_n_tiles, nt = pid % p.num_n_tiles;
+    const uint32_t upid = static_cast<uint32_t>(pid), nnt = static_cast<uint32_t>(p.num_n_tiles);
+    const uint32_t rp32 = upid / nnt;
+    const int64_t rp = rp32, nt = upid - rp32 * nnt;
     int lo = 0, hi = E - 1;  // expert owning pair row rp
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -732,9 +747,12 @@ __device__ DuoTile duo_tile_grouped(const Params& p, const DuoSeg* seg, int64_t 
     const int64_t n_pm = ((p.M + 127) / 128 + 1) / 2;
     const int64_t per = n_pm * p.num_n_tiles;
     if (pid >= per * E) return t;
-    const int e = seg->order[pid / per];
-    const int64_t r = pid % per;
-    const int64_t pm = r / p.num_n_tiles, nt = r % p.num_n_tiles;
+    const uint32_t upid = static_cast<uint32_t>(pid), uper = static_cast<uint32_t>(per);
+    const uint32_t nnt = static_cast<uint32_t>(p.num_n_tiles);
+    const uint32_t ei = upid / uper, r = upid - ei * uper;
+    const int e = seg->order[ei];
+    const uint32_t pm32 = r / nnt;
+    const int64_t pm = pm32, nt = r - pm32 * nnt;
     const int64_t cnt = seg->off[e + 1] - seg->off[e];
     const int64_t nk = (cnt + BK - 1) / BK;
     const int64_t mt = 2 * pm + crank;
@@ -1479,6 +1497,7 @@ int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
   p.num_tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
   p.band = (band_tiles(a.M, a.N, a.K, p.num_m_tiles) + 1) / 2;
   const int64_t pair_tiles = static_cast<int64_t>((p.num_m_tiles + 1) / 2) * p.num_n_tiles;
+  if (2 * pair_tiles > INT32_MAX) return MXFP8_ERR_INVALID_ARG;  // 32-bit item arithmetic
   const int64_t fit = max_duo_clusters<BN>();
   if (fit <= 0) return MXFP8_ERR_CUDA;
   // The tiles of the last, partial wave run as half-width tiles when their halves still fit
@@ -1541,6 +1560,7 @@ int launch_duo_grouped(const GemmArgs& a, Params p, cudaStream_t stream) {
     if (!make_out_map(&mc, a.C, T, p.N, 1, fp32, 3)) return MXFP8_ERR_CUDA;
     pair_tiles = ((T + 127) / 128 / 2 + E) * p.num_n_tiles;  // bound on pair tiles
   }
+  if (pair_tiles > INT32_MAX) return MXFP8_ERR_INVALID_ARG;  // 32-bit item arithmetic
   const int64_t fit = max_duo_clusters<BN, kMode>();
   if (fit <= 0) return MXFP8_ERR_CUDA;
   const int64_t clusters = pair_tiles < fit ? pair_tiles : fit;
@@ -1592,6 +1612,7 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   if (!make_map(&ma, a.A, 2, a.K, a.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
   if (!make_out_map(&mc, a.C, a.M, a.N, 1, p.out_fp32 != 0, 3)) return MXFP8_ERR_CUDA;
   if (!make_map(&mb, a.B, 2, a.K, a.N, 1, BK, bn)) return MXFP8_ERR_CUDA;
+  if (p.num_tiles > INT32_MAX) return MXFP8_ERR_INVALID_ARG;  // 32-bit tile arithmetic
   const int64_t grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
   return wide ? launch<256, kDense>(ma, mb, mc, p, grid, stream)
               : launch<128, kDense>(ma, mb, mc, p, grid, stream);
@@ -1629,6 +1650,7 @@ int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     if (!make_map(&ma, a.A, 2, a.total_rows, p.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
     if (!make_map(&mb, a.B, 2, a.total_rows, p.N, 1, BK, bn)) return MXFP8_ERR_CUDA;
     if (!make_out_map(&mc, a.C, p.M, p.N, p.E, p.out_fp32 != 0, 3)) return MXFP8_ERR_CUDA;
+    if (tiles > INT32_MAX) return MXFP8_ERR_INVALID_ARG;  // 32-bit tile arithmetic
     const int64_t grid = tiles < num_sms() ? tiles : num_sms();
     return wide ? launch<256, kGroupWgrad>(ma, mb, mc, p, grid, stream)
                 : launch<128, kGroupWgrad>(ma, mb, mc, p, grid, stream);
@@ -1652,6 +1674,7 @@ int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   if (!make_map(&ma, a.A, 2, a.K, a.total_rows, 1, BK, BM)) return MXFP8_ERR_CUDA;
   if (!make_map(&mb, a.B, 3, a.K, a.N, a.num_experts, BK, bn)) return MXFP8_ERR_CUDA;
   if (!make_out_map(&mc, a.C, a.total_rows, p.N, 1, p.out_fp32 != 0, 3)) return MXFP8_ERR_CUDA;
+  if (tiles > INT32_MAX) return MXFP8_ERR_INVALID_ARG;  // 32-bit tile arithmetic
   const int64_t grid = tiles < num_sms() ? tiles : num_sms();
   return wide ? launch<256, kGroupRows>(ma, mb, mc, p, grid, stream)
               : launch<128, kGroupRows>(ma, mb, mc, p, grid, stream);
