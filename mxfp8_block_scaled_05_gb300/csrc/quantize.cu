@@ -22,9 +22,9 @@
 //
 // The block exponent is taken from the integer bits of the block's largest |BF16|
 // (biased exponent E): scale byte = max(E - 8, 0) (floor(log2 amax) - 8, clamped at
-// -127). Elements are widened to FP32, multiplied by 2^-e two at a time (mul.rn.f32x2,
-// an exact power-of-two scaling) and converted with cvt.rn.satfinite.e4m3x2 (round to
-// nearest even, saturating). The dual kernel's row pass gives each thread one 32-element
+// -127). Elements are widened to FP32, multiplied by 2^-e (IEEE single-precision products,
+// an exact power-of-two scaling) and converted two at a time with
+// cvt.rn.satfinite.e4m3x2 (round to nearest even, saturating). The dual kernel's row pass gives each thread one 32-element
 // block and stores its 32 code bytes at once; the column pass reads column pairs from the
 // shared tile, whose rows are padded so that both passes are free of bank conflicts.
 
@@ -137,31 +137,23 @@ __device__ __forceinline__ float inv_scale(uint32_t s) {
   return __uint_as_float((254u - s) << 23);
 }
 
-// Two elements given as FP32 bit patterns (lo first in memory order) -> 2 bytes: scaled
-// by one packed multiply (mul.rn.f32x2: IEEE single-precision products rounded to nearest,
-// exact for a power-of-two scale), then one RNE-saturating E4M3 conversion.
-__device__ __forceinline__ uint32_t e4m3x2_f32bits(uint32_t lo, uint32_t hi, uint64_t mul2) {
-  uint64_t x, y;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(lo), "r"(hi));
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(x), "l"(mul2));
+// Two elements given as FP32 bit patterns (lo first in memory order) -> 2 bytes: each
+// scaled by an IEEE single-precision product rounded to nearest (exact for a power-of-two
+// scale), then one RNE-saturating E4M3 conversion of the pair. Two scalar products measured
+// slightly faster than one packed mul.rn.f32x2 (whose operands must sit in a register pair).
+__device__ __forceinline__ uint32_t e4m3x2_f32bits(uint32_t lo, uint32_t hi, float mul) {
+  const float a = __fmul_rn(__uint_as_float(lo), mul);
+  const float b = __fmul_rn(__uint_as_float(hi), mul);
   uint16_t c;
-  asm("{ .reg .f32 lo, hi; mov.b64 {lo, hi}, %1; cvt.rn.satfinite.e4m3x2.f32 %0, hi, lo; }"
-      : "=h"(c) : "l"(y));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(b), "f"(a));
   return c;
-}
-
-__device__ __forceinline__ uint64_t splat2(float mul) {
-  uint64_t mul2;
-  asm("mov.b64 %0, {%1, %1};" : "=l"(mul2) : "r"(__float_as_uint(mul)));
-  return mul2;
 }
 
 // Two BF16 pairs (4 elements, memory order lo(w0), hi(w0), lo(w1), hi(w1)) -> 4 bytes.
 // A BF16 value's FP32 bit pattern is its 16 bits shifted to the top half.
 __device__ __forceinline__ uint32_t e4m3x4(uint32_t w0, uint32_t w1, float mul) {
-  const uint64_t mul2 = splat2(mul);
-  return e4m3x2_f32bits(w0 << 16, w0 & 0xFFFF0000u, mul2) |
-         (e4m3x2_f32bits(w1 << 16, w1 & 0xFFFF0000u, mul2) << 16);
+  return e4m3x2_f32bits(w0 << 16, w0 & 0xFFFF0000u, mul) |
+         (e4m3x2_f32bits(w1 << 16, w1 & 0xFFFF0000u, mul) << 16);
 }
 
 // One column of four consecutive rows of a two-column word pair -> 4 bytes: the low
@@ -169,9 +161,8 @@ __device__ __forceinline__ uint32_t e4m3x4(uint32_t w0, uint32_t w1, float mul) 
 template <bool kHigh>
 __device__ __forceinline__ uint32_t e4m3x4_col(uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, float mul) {
-  const uint64_t mul2 = splat2(mul);
   auto f = [](uint32_t w) { return kHigh ? (w & 0xFFFF0000u) : (w << 16); };
-  return e4m3x2_f32bits(f(a0), f(a1), mul2) | (e4m3x2_f32bits(f(a2), f(a3), mul2) << 16);
+  return e4m3x2_f32bits(f(a0), f(a1), mul) | (e4m3x2_f32bits(f(a2), f(a3), mul) << 16);
 }
 
 // 32 bytes global store in one instruction (the address must be 32-byte aligned).
