@@ -97,6 +97,13 @@ def test_argument_errors_need_no_device(lib):
     qg = lib.mxfp8_quantize_grouped
     assert qg(p, 64, 64, m.ROW, None, 4, p, p, None) == m.ERR_INVALID_ARG
     assert qg(p, 48, 64, m.ROW, p, 4, p, p, None) == m.ERR_ALIGNMENT
+    # the quantizer's grid holds at most 65535 tiles of 128 token rows; one more is refused
+    # before anything touches the device (the largest accepted size runs in the GPU tests)
+    assert q(p, 65536 * 128, 32, m.ROW, p, p, m.SWIZZLED, None) == m.ERR_INVALID_ARG
+    assert q(p, 65535 * 128 + 32, 32, m.COL, p, p, m.SWIZZLED, None) == m.ERR_INVALID_ARG
+    assert lib.mxfp8_quantize_dual(p, 65536 * 128, 32, p, p, p, p, m.SWIZZLED, None) == \
+        m.ERR_INVALID_ARG
+    assert qg(p, 65535 * 128, 32, m.ROW, p, 4, p, p, None) == m.ERR_INVALID_ARG  # + E tiles
 
 
 def test_blockwise_sizes_and_argument_errors_need_no_device(lib):

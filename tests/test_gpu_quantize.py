@@ -282,7 +282,8 @@ def test_multi_job_launch_equals_separate_calls(m, layout):
     """Several tensors in one launch: the oracle's bytes for a small job, and byte equality
     with one quantize_dual per job for ragged shapes, a large one and an empty one."""
     g = np.random.default_rng(23 + layout)
-    shapes = [(160, 96), (4096, 4096), (288, 4128), (0, 64), (6144, 4096), (32, 32)]
+    shapes = [(160, 96), (4096, 4096), (288, 4128), (0, 64), (6144, 4096), (32, 32),
+              (96, 4064), (4128, 160)]           # the maximum of 8 jobs per launch
     xs = [_rand_bf16(g, sh).to(DEV) if sh[0] else torch.empty(sh, dtype=torch.bfloat16, device=DEV)
           for sh in shapes]
     got = m.quantize_dual_multi(xs, layout)
@@ -360,3 +361,25 @@ def test_round_up_rule_golden_blocks_and_grid_difference(m):
     blocks_differ = (u8(qf).reshape(4096, 128, 32) != u8(qc).reshape(4096, 128, 32)).any(axis=2)
     assert not np.any(blocks_differ & ~over)
     assert 0.01 < over.mean() < 0.9
+
+
+def test_largest_token_grid(m):
+    """The largest input the quantizer's grid takes: 65535 tiles of 128 token rows (8388480
+    rows) x 32 columns, row-wise, column-wise and dual. Sampled rows and columns (every
+    token of those columns) against the oracle, first and last ones included."""
+    rows, cols = 65535 * 128, 32
+    g = torch.Generator(device=DEV).manual_seed(12)
+    x = (torch.randn((rows, cols), generator=g, device=DEV) *
+         torch.exp2(torch.randint(-20, 20, (rows, 1), generator=g, device=DEV).float())
+         ).to(torch.bfloat16)
+    from tests.oracle_helpers import check_quantized_sampled
+    qr, sr = m.quantize(x, m.ROW, m.SWIZZLED)
+    check_quantized_sampled(x, qr, sr, O.ROW, 64, seed=1)
+    qc, sc = m.quantize(x, m.COL, m.SWIZZLED)
+    check_quantized_sampled(x, qc, sc, O.COL, 2, seed=2)
+    dr, dsr, dc, dsc = m.quantize_dual(x, m.SWIZZLED)
+    assert torch.equal(dr, qr) and torch.equal(dsr, sr)
+    assert torch.equal(dc, qc) and torch.equal(dsc, sc)
+    assert m.device_status() == m.OK
+    del x, qr, sr, qc, sc, dr, dsr, dc, dsc
+    torch.cuda.empty_cache()
