@@ -681,7 +681,40 @@ def cpu_baseline_obj():
     step_s = float(np.mean(ests))
     return {"value": flops / step_s / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
             "kind": "oracle", "sample": f"{i} samples of: {desc}",
-            "seconds": time.perf_counter() - t0, "ms_per_step_extrapolated": step_s * 1e3}
+            "seconds": time.perf_counter() - t0, "ms_per_step_extrapolated": step_s * 1e3,
+            "single_core": cpu_baseline_single_core()}
+
+
+SINGLE_CORE_CHILD = """
+import json, os, sys, time
+os.sched_setaffinity(0, {min(os.sched_getaffinity(0))})
+sys.path.insert(0, sys.argv[1])
+import numpy as np
+import bench
+t0, ests, flops = time.perf_counter(), [], 0.0
+while time.perf_counter() - t0 < 5.0 and len(ests) < 20:
+    s, est, desc, flops = bench.oracle_step_sample(200 + len(ests))
+    ests.append(est)
+step_s = float(np.mean(ests))
+print(json.dumps({"value": flops / step_s / 1e12, "samples": len(ests),
+                  "ms_per_step_extrapolated": step_s * 1e3}))
+"""
+
+
+def cpu_baseline_single_core():
+    """The same oracle sample on one host core (a child process pinned to one CPU, with the
+    BLAS and OpenMP pools at one thread), for about 5 s; None if it could not run."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    try:
+        r = subprocess.run([sys.executable, "-c", SINGLE_CORE_CHILD, ROOT], env=env,
+                           capture_output=True, text=True, timeout=120)
+        out = json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.TimeoutExpired, ValueError, IndexError, OSError):
+        return None
+    return {"value": out["value"], "unit": "TFLOP/s", "cores": 1, "samples": out["samples"],
+            "ms_per_step_extrapolated": out["ms_per_step_extrapolated"]}
 
 
 # ------------------------------------------------------------ other configurations
