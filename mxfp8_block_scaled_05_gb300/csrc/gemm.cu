@@ -615,6 +615,8 @@ struct Duo {
   static constexpr int kSfbTiles = kWide ? 3 : 2;      // 128-row scale tiles of B per stage
   static constexpr int kSfbBytes = 512 * kSfbTiles;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  // a 384-wide kernel's half tile stages its first B box only
+  static constexpr int kHalfStageBytes = kWide ? kStageBytes - kBoxRows * BK : kStageBytes;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
   static constexpr int kOffSfa = kOffB + kStages * kBBytes;
@@ -795,6 +797,27 @@ __device__ __forceinline__ DuoTile duo_tile_of(const Params& p, const DuoSeg* se
   }
 }
 
+// Bytes one CTA stages for its stage use number `use` (the producer's running count):
+// found by walking the CTA's tiles again. Only the drain after an abort needs it.
+template <int BN, int kMode>
+__device__ uint32_t duo_use_bytes(const Params& p, const DuoSeg* seg, int64_t first_id,
+                                  int64_t id_step, uint32_t crank, uint32_t use) {
+  using D = Duo<BN, kMode>;
+  if constexpr (D::kHalfStageBytes == D::kStageBytes) {
+    return D::kStageBytes;
+  } else {
+    uint32_t at = 0;
+    for (int64_t id = first_id;; id += id_step) {
+      const DuoTile t = duo_tile_of<BN, kMode>(p, seg, id, crank);
+      if (!t.live) break;
+      if (use < at + static_cast<uint32_t>(t.nk))
+        return t.width == BN ? D::kStageBytes : D::kHalfStageBytes;
+      at += static_cast<uint32_t>(t.nk);
+    }
+    return D::kStageBytes;
+  }
+}
+
 template <int BN, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
@@ -903,25 +926,28 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     for (int64_t id = first_id; ok; id += id_step) {
       const DuoTile t = duo_tile_of<BN, kMode>(p, seg, id, crank);
       if (!t.live) break;
+      const bool whole = t.width == BN;
+      const uint32_t tx = whole ? D::kStageBytes : D::kHalfStageBytes;
       for (int64_t kb = 0; kb < t.nk; ++kb, ++it) {
         const uint32_t s = it % kStages, ph = (it / kStages) & 1;
         if (!warp_wait(&empty[s], ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
         const uint32_t bar = full0 + 8 * s;
         const int32_t kx = static_cast<int32_t>(t.k_origin + kb * BK);
         if (issuer) {
-          if (leader) mbar_arrive_expect_tx(&full[s], 2 * D::kStageBytes);
+          if (leader) mbar_arrive_expect_tx(&full[s], 2 * tx);
           tma_load_2d_2sm(smem + D::kOffA + s * D::kABytes, &map_a, kx,
                           static_cast<int32_t>(t.m0), bar);
           if constexpr (kMode == kGroupRows)
             tma_load_3d_2sm(smem + D::kOffB + s * D::kBBytes, &map_b, kx,
                             static_cast<int32_t>(t.n0 + crank * (BN / 2)), t.b_z, bar);
           else if constexpr (D::kWide) {
-            // rows 96c.. of each 192-column half of the pair tile (a half tile uses the
-            // first box only; the second is loaded all the same, as the byte count expects)
+            // rows 96c.. of each 192-column half of the pair tile; a half tile (its first
+            // MMA alone) loads the first box only
             uint8_t* bs = smem + D::kOffB + s * D::kBBytes;
             tma_load_2d_2sm(bs, &map_b, kx, static_cast<int32_t>(t.n0 + 96 * crank), bar);
-            tma_load_2d_2sm(bs + 96 * BK, &map_b, kx,
-                            static_cast<int32_t>(t.n0 + 192 + 96 * crank), bar);
+            if (whole)
+              tma_load_2d_2sm(bs + 96 * BK, &map_b, kx,
+                              static_cast<int32_t>(t.n0 + 192 + 96 * crank), bar);
           } else {
             tma_load_2d_2sm(smem + D::kOffB + s * D::kBBytes, &map_b, kx,
                             static_cast<int32_t>(t.n0 + crank * (t.width / 2)), bar);
@@ -1233,8 +1259,11 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     if (leader) {
       for (uint32_t i = consumed; i < issued; ++i) {
         uint64_t* b = &full[i % kStages];
-        if (i < i0 && i >= i1) mbar_complete_tx(b, D::kStageBytes);
-        else if (i >= i0 && i < i1) mbar_arrive_expect_tx(b, D::kStageBytes);
+        const bool only0 = i < i0 && i >= i1, only1 = i >= i0 && i < i1;
+        if (!only0 && !only1) continue;
+        const uint32_t bytes = duo_use_bytes<BN, kMode>(p, seg, first_id, id_step, crank, i);
+        if (only0) mbar_complete_tx(b, bytes);
+        else mbar_arrive_expect_tx(b, bytes);
       }
       drain_stages<kStages, D::kAcc>(full, empty, acc_full, issued, consumed, commits,
                                      p.drain_ns);
