@@ -509,7 +509,10 @@ def run_ours(args, rank, ws):
         "calibration": cal,
         "execution": ("20 launches per step; each layer's wgrad on a second stream beside its "
                       "fprop and dgrad" if args.streams == 2 else
-                      "20 launches per step issued on one stream"),
+                      "20 launches per step issued on one stream")
+                     + ("; programmatic dependent launch off (MXFP8_PDL=0)"
+                        if os.environ.get("MXFP8_PDL", "1").startswith("0") else
+                        "; kernels launched with programmatic stream serialization"),
         "cuda_graph": {"ms_per_step": graph_ms,
                        "value": ws * step.flops / (graph_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                        "note": "the same step captured once in a CUDA graph and replayed"},

@@ -19,7 +19,12 @@
  *    flags, set up on the first call on each device.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
  *    Every compute call only enqueues work on `stream` and returns; none synchronizes
- *    except mxfp8_get_device_status.
+ *    except mxfp8_get_device_status. Kernels are launched with programmatic stream
+ *    serialization: one may be scheduled while the previous kernel of its stream is
+ *    still running, and it waits inside the kernel, before its first read or write of
+ *    global memory, until that kernel has completed. Stream order therefore holds as
+ *    for a plain launch, against any kernel before it. MXFP8_PDL=0 in the environment
+ *    (read once per process) launches them plainly.
  *  - Return value: an mxfp8_status. Arguments are checked on the host before anything
  *    is enqueued; a failed check returns its code and enqueues nothing. Errors found
  *    by a kernel (bad expert offsets, a pipeline wait that ran out) are latched in the

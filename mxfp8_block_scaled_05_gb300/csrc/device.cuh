@@ -27,6 +27,23 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------------------ programmatic dependent launch
+// Every kernel of the library is launched with programmatic stream serialization, so it
+// may start while the kernel before it in the stream is still running (on SMs that kernel
+// leaves idle). It runs its prologue (barrier setup, TMEM allocation, descriptor
+// prefetch), then waits here, in every thread and before its first global memory access,
+// read or write, until the previous kernel has completed and its writes are visible.
+// Because each kernel waits for the one before it, the ordering is transitive.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel of the stream be scheduled once every CTA of this grid has said so
+// (or exited). Its CTAs then take free SMs and wait in grid_dependency_wait above.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -295,6 +295,7 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     tma_prefetch_desc(&map_b);
     tma_prefetch_desc(&map_c);
   }
+  if (kMode != kDense) grid_dependency_wait();  // the offsets may come from the previous kernel
   if (kMode != kDense) {
     // segment table: offsets checked (0-based, non-decreasing, 32-aligned, ending at
     // total_rows) and prefix sums of ceil(count / 128)
@@ -339,6 +340,8 @@ mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (kMode == kDense) grid_dependency_wait();
+  grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------- TMA producer
@@ -869,6 +872,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     tma_prefetch_desc(&map_sfb);
     tma_prefetch_desc(&map_c);
   }
+  if constexpr (D::kGrouped) grid_dependency_wait();  // the offsets may come from the previous kernel
   if constexpr (D::kGrouped) {
     // segment table: offsets checked (0-based, non-decreasing, 32-aligned, ending at
     // total_rows), prefix sums, and the heaviest-first expert order
@@ -915,6 +919,8 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
   cluster_sync();  // both CTAs' barriers exist before any cross-CTA copy, arrive or commit
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if constexpr (!D::kGrouped) grid_dependency_wait();
+  grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------- TMA producer (both)
@@ -1332,6 +1338,25 @@ uint64_t wait_limit_ns() {
   return o ? o : dflt;
 }
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("MXFP8_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
+}  // namespace
+
+int pdl_attr(cudaLaunchAttribute* attr) {
+  if (!pdl_enabled()) return 0;
+  attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr->val.programmaticStreamSerializationAllowed = 1;
+  return 1;
+}
+
+namespace {
+
 // The drain waits for work already in flight on the way out of a kernel: at least 2 s, and
 // never shorter than the pipeline limit, so that a short pipeline limit cannot cut them.
 constexpr uint64_t kMinDrainNs = 2000000000ull;
@@ -1353,8 +1378,15 @@ int launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, 
     attr_set[dev] = true;
   }
   if (grid <= 0) return MXFP8_OK;
-  k<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(ma, mb, mc, p);
-  return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(&attr[0]);
+  return cudaLaunchKernelEx(&cfg, k, ma, mb, mc, p) == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
 }
 
 // Raster band width, in M tiles. Tiles of a band are visited M tile first, so that while
@@ -1540,8 +1572,9 @@ int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
   const int64_t clusters = items < fit ? items : fit;
   if (clusters <= 0) return MXFP8_OK;
   auto k = mxfp8_gemm_2sm_kernel<BN, kDense>;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = cluster2_config(2 * clusters, D::kSmemBytes, stream, attr);
+  cfg.numAttrs += pdl_attr(&attr[1]);
   return cudaLaunchKernelEx(&cfg, k, ma, mb, msa, msb, mc, p) == cudaSuccess ? MXFP8_OK
                                                                               : MXFP8_ERR_CUDA;
 }
@@ -1595,8 +1628,9 @@ int launch_duo_grouped(const GemmArgs& a, Params p, cudaStream_t stream) {
   const int64_t clusters = pair_tiles < fit ? pair_tiles : fit;
   if (clusters <= 0) return MXFP8_OK;
   auto k = mxfp8_gemm_2sm_kernel<BN, kMode>;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = cluster2_config(2 * clusters, D::kSmemBytes, stream, attr);
+  cfg.numAttrs += pdl_attr(&attr[1]);
   return cudaLaunchKernelEx(&cfg, k, ma, mb, msa, msb, mc, p) == cudaSuccess ? MXFP8_OK
                                                                               : MXFP8_ERR_CUDA;
 }

@@ -28,6 +28,12 @@ struct QuantizeArgs {
 
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream);
 
+// Programmatic dependent launch: every kernel of the library is launched with
+// programmatic stream serialization (its kernels wait for the previous kernel of the
+// stream in the kernel itself), unless the environment sets MXFP8_PDL=0 (read once).
+// Writes the launch attribute to *attr and returns 1, or returns 0 when it is off.
+int pdl_attr(cudaLaunchAttribute* attr);
+
 // Several dual (row-wise + column-wise) quantizations in one launch.
 constexpr int kMaxQuantizeJobs = 8;
 struct QuantizeJobs {

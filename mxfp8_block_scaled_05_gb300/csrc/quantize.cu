@@ -353,6 +353,8 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
   __shared__ __align__(16) uint8_t stile_c[512];
   extern __shared__ __align__(16) uint8_t dyn[];  // Segments for grouped calls
   Segments* seg = reinterpret_cast<Segments*>(dyn);
+  grid_dependency_wait();
+  grid_launch_dependents();
   if (kGrouped) load_segments(*seg, offsets, E, rows, status);
 
   // ---- which tile, and where its two 512-byte scale tiles go
@@ -508,6 +510,8 @@ blockwise_quantize_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_
                           uint8_t* __restrict__ out, float* __restrict__ scale_inv, int pow2) {
   __shared__ uint32_t warp_max[kThreads / 32];
   __shared__ float s_factor;
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int t = threadIdx.x, v = t & 15, rsub = t >> 4;
   const int64_t row0 = static_cast<int64_t>(blockIdx.y) * kTile;
   const int64_t col0 = static_cast<int64_t>(blockIdx.x) * kTile;
@@ -574,6 +578,22 @@ blockwise_quantize_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_
   }
 }
 
+// One launch of kThreads-thread CTAs, with programmatic stream serialization unless it is
+// turned off (the kernels wait for the previous kernel of the stream themselves).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, size_t dyn, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(&attr[0]);
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 template <bool kRow, bool kCol, bool kSw, bool kGr>
 cudaError_t launch_tiles(const QuantizeArgs& a, cudaStream_t stream) {
   const int64_t col_tiles = (a.cols + kTile - 1) / kTile;
@@ -592,11 +612,10 @@ cudaError_t launch_tiles(const QuantizeArgs& a, cudaStream_t stream) {
                 a.scale_item_bytes};
   const QOut co{static_cast<uint8_t*>(a.out_col), static_cast<uint8_t*>(a.scales_col),
                 a.scale_item_bytes_col};
-  dim3 grid(static_cast<unsigned>(col_tiles), static_cast<unsigned>(row_tiles),
-            static_cast<unsigned>(a.batch));
-  k<<<grid, kThreads, dyn, stream>>>(static_cast<const uint16_t*>(a.src), a.rows, a.cols, ro, co,
-                                      a.offsets, a.num_experts, a.rule, a.status, QJobs{});
-  return cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(col_tiles), static_cast<unsigned>(row_tiles),
+                 static_cast<unsigned>(a.batch));
+  return launch_pdl(k, grid, dyn, stream, static_cast<const uint16_t*>(a.src), a.rows, a.cols,
+                    ro, co, a.offsets, a.num_experts, a.rule, a.status, QJobs{});
 }
 
 template <bool kRow, bool kCol>
@@ -631,15 +650,16 @@ cudaError_t launch_quantize_jobs(const QuantizeJobs& in, cudaStream_t stream) {
   if (tiles == 0) return cudaSuccess;
   if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const QOut none{nullptr, nullptr, 0};
+  const dim3 grid(static_cast<unsigned>(tiles));
+  const uint16_t* no_src = nullptr;
+  const int32_t* no_offsets = nullptr;
   if (in.layout == MXFP8_SCALES_SWIZZLED)
-    quantize_tile_kernel<true, true, true, false, true><<<static_cast<unsigned>(tiles), kThreads, 0,
-                                                          stream>>>(
-        nullptr, 0, 0, none, none, nullptr, 0, MXFP8_RULE_FLOOR, in.status, j);
-  else
-    quantize_tile_kernel<true, true, false, false, true><<<static_cast<unsigned>(tiles), kThreads, 0,
-                                                           stream>>>(
-        nullptr, 0, 0, none, none, nullptr, 0, MXFP8_RULE_FLOOR, in.status, j);
-  return cudaGetLastError();
+    return launch_pdl(quantize_tile_kernel<true, true, true, false, true>, grid, 0, stream,
+                      no_src, int64_t{0}, int64_t{0}, none, none, no_offsets, 0,
+                      int{MXFP8_RULE_FLOOR}, in.status, j);
+  return launch_pdl(quantize_tile_kernel<true, true, false, false, true>, grid, 0, stream, no_src,
+                    int64_t{0}, int64_t{0}, none, none, no_offsets, 0, int{MXFP8_RULE_FLOOR},
+                    in.status, j);
 }
 
 cudaError_t launch_blockwise(const void* src, int64_t rows, int64_t cols, void* out,
@@ -647,11 +667,10 @@ cudaError_t launch_blockwise(const void* src, int64_t rows, int64_t cols, void* 
   const int64_t gx = (cols + kTile - 1) / kTile, gy = (rows + kTile - 1) / kTile;
   if (gx == 0 || gy == 0) return cudaSuccess;
   if (gy > 65535 || gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
-  blockwise_quantize_kernel<<<grid, kThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(src), rows, cols, static_cast<uint8_t*>(out), scale_inv,
-      pow2 ? 1 : 0);
-  return cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+  return launch_pdl(blockwise_quantize_kernel, grid, 0, stream,
+                    static_cast<const uint16_t*>(src), rows, cols, static_cast<uint8_t*>(out),
+                    scale_inv, pow2 ? 1 : 0);
 }
 
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream) {
