@@ -156,13 +156,35 @@ __device__ __forceinline__ uint32_t e4m3x4(uint32_t w0, uint32_t w1, float mul) 
          (e4m3x2_f32bits(w1 << 16, w1 & 0xFFFF0000u, mul) << 16);
 }
 
-// One column of four consecutive rows of a two-column word pair -> 4 bytes: the low
-// halves (column c) or the high halves (column c + 1) of a0..a3, widened in place.
-template <bool kHigh>
-__device__ __forceinline__ uint32_t e4m3x4_col(uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, float mul) {
-  auto f = [](uint32_t w) { return kHigh ? (w & 0xFFFF0000u) : (w << 16); };
-  return e4m3x2_f32bits(f(a0), f(a1), mul) | (e4m3x2_f32bits(f(a2), f(a3), mul) << 16);
+// The MXFP8 kernels scale by an exact power of two, so they can scale two BF16 values with
+// one packed BF16 product (exact: the results lie in [2^-133, 2^9) or are far below E4M3's
+// smallest subnormal, and BF16 keeps subnormals) before widening them for the conversion.
+// The block-wise kernel's FP32 scale is not a power of two: it keeps the FP32 products.
+
+// BF16 bits of 2^-e for scale byte s = e + 127 (a normal number for s <= 253; the 0xFF of a
+// NaN/Inf block gives +Inf, whose products are discarded).
+__device__ __forceinline__ uint32_t inv_scale_bf16(uint32_t s) { return ((254u - s) & 0xFFu) << 7; }
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Two values given as FP32 bit patterns (lo first in memory order) -> 2 bytes, one
+// RNE-saturating E4M3 conversion of the pair.
+__device__ __forceinline__ uint32_t e4m3x2_of(uint32_t lo, uint32_t hi) {
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+      : "=h"(c) : "f"(__uint_as_float(hi)), "f"(__uint_as_float(lo)));
+  return c;
+}
+
+// Two BF16 pairs (4 elements, memory order lo(w0), hi(w0), lo(w1), hi(w1)) scaled by the
+// BF16 pair mul2 (2^-e in both halves) -> 4 bytes.
+__device__ __forceinline__ uint32_t e4m3x4_pow2(uint32_t w0, uint32_t w1, uint32_t mul2) {
+  const uint32_t v0 = mul_bf16x2(w0, mul2), v1 = mul_bf16x2(w1, mul2);
+  return e4m3x2_of(v0 << 16, v0 & 0xFFFF0000u) | (e4m3x2_of(v1 << 16, v1 & 0xFFFF0000u) << 16);
 }
 
 // 32 bytes global store in one instruction (the address must be 32-byte aligned).
@@ -235,11 +257,11 @@ __device__ __forceinline__ void row_pass_smem(const uint16_t (*tile)[kTilePitch]
     if (valid) {
       uint32_t o[8];
       if (__builtin_expect(s != 0xFFu, 1)) {
-        const float mul = inv_scale(s);
-        o[0] = e4m3x4(x0.x, x0.y, mul); o[1] = e4m3x4(x0.z, x0.w, mul);
-        o[2] = e4m3x4(x1.x, x1.y, mul); o[3] = e4m3x4(x1.z, x1.w, mul);
-        o[4] = e4m3x4(x2.x, x2.y, mul); o[5] = e4m3x4(x2.z, x2.w, mul);
-        o[6] = e4m3x4(x3.x, x3.y, mul); o[7] = e4m3x4(x3.z, x3.w, mul);
+        const uint32_t mul2 = inv_scale_bf16(s) * 0x10001u;
+        o[0] = e4m3x4_pow2(x0.x, x0.y, mul2); o[1] = e4m3x4_pow2(x0.z, x0.w, mul2);
+        o[2] = e4m3x4_pow2(x1.x, x1.y, mul2); o[3] = e4m3x4_pow2(x1.z, x1.w, mul2);
+        o[4] = e4m3x4_pow2(x2.x, x2.y, mul2); o[5] = e4m3x4_pow2(x2.z, x2.w, mul2);
+        o[6] = e4m3x4_pow2(x3.x, x3.y, mul2); o[7] = e4m3x4_pow2(x3.z, x3.w, mul2);
       } else {
         o[0] = nan4(x0.x, x0.y); o[1] = nan4(x0.z, x0.w);
         o[2] = nan4(x1.x, x1.y); o[3] = nan4(x1.z, x1.w);
@@ -285,18 +307,23 @@ __device__ __forceinline__ void col_pass_smem(uint16_t (*tile)[kTilePitch], uint
   const uint32_t s0 = scale_byte(m01 & 0xFFFFu, rule), s1 = scale_byte(m01 >> 16, rule);
   uint4 stage_o0[2], stage_o1[2];
   if (valid) {
-    const float mul0 = inv_scale(s0), mul1 = inv_scale(s1);
     uint32_t o0[8], o1[8];
     if (__builtin_expect(s0 != 0xFFu && s1 != 0xFFu, 1)) {
+      // each row word holds column c (low half) and c + 1 (high half): one packed product
+      // scales both by their own block's 2^-e
+      const uint32_t mulp = inv_scale_bf16(s0) | (inv_scale_bf16(s1) << 16);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const uint32_t a0 = colw[(4 * q) * kRowWords], a1 = colw[(4 * q + 1) * kRowWords];
-        const uint32_t a2 = colw[(4 * q + 2) * kRowWords], a3 = colw[(4 * q + 3) * kRowWords];
-        // column c: low halves; column c+1: high halves
-        o0[q] = e4m3x4_col<false>(a0, a1, a2, a3, mul0);
-        o1[q] = e4m3x4_col<true>(a0, a1, a2, a3, mul1);
+        const uint32_t b0 = mul_bf16x2(colw[(4 * q) * kRowWords], mulp);
+        const uint32_t b1 = mul_bf16x2(colw[(4 * q + 1) * kRowWords], mulp);
+        const uint32_t b2 = mul_bf16x2(colw[(4 * q + 2) * kRowWords], mulp);
+        const uint32_t b3 = mul_bf16x2(colw[(4 * q + 3) * kRowWords], mulp);
+        o0[q] = e4m3x2_of(b0 << 16, b1 << 16) | (e4m3x2_of(b2 << 16, b3 << 16) << 16);
+        o1[q] = e4m3x2_of(b0 & 0xFFFF0000u, b1 & 0xFFFF0000u) |
+                (e4m3x2_of(b2 & 0xFFFF0000u, b3 & 0xFFFF0000u) << 16);
       }
     } else {  // a NaN/Inf block in either column (rare)
+      const float mul0 = inv_scale(s0), mul1 = inv_scale(s1);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const uint32_t a0 = colw[(4 * q) * kRowWords], a1 = colw[(4 * q + 1) * kRowWords];
@@ -459,12 +486,12 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t col
       const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
       const bool valid = col_ok && r < rows_valid;
       const uint32_t s = scale_byte(m, rule);
-      const float mul = inv_scale(s);  // (a NaN/Inf block's codes are replaced below)
       if (valid) {
         uint2 o;
         if (__builtin_expect(s != 0xFFu, 1)) {
-          o.x = e4m3x4(xv.x, xv.y, mul);
-          o.y = e4m3x4(xv.z, xv.w, mul);
+          const uint32_t mul2 = inv_scale_bf16(s) * 0x10001u;
+          o.x = e4m3x4_pow2(xv.x, xv.y, mul2);
+          o.y = e4m3x4_pow2(xv.z, xv.w, mul2);
         } else {
           o.x = nan4(xv.x, xv.y);
           o.y = nan4(xv.z, xv.w);
