@@ -22,8 +22,8 @@
 //
 // The block exponent is taken from the integer bits of the block's largest |BF16|
 // (biased exponent E): scale byte = max(E - 8, 0) (floor(log2 amax) - 8, clamped at
-// -127). Elements are widened to FP32, multiplied by 2^-e (IEEE single-precision products,
-// an exact power-of-two scaling) and converted two at a time with
+// -127). Elements are scaled two at a time by 2^-e with one packed BF16 product (exact for a
+// power-of-two scale), widened to FP32 and converted two at a time with
 // cvt.rn.satfinite.e4m3x2 (round to nearest even, saturating). The dual kernel's row pass gives each thread one 32-element
 // block and stores its 32 code bytes at once; the column pass reads column pairs from the
 // shared tile, whose rows are padded so that both passes are free of bank conflicts.
