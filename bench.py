@@ -596,7 +596,7 @@ def run_e2e(args, m, step, dev, stream, ws):
     # the copies of consecutive steps overlap (see above), so the timed steps include one
     # pipeline fill and drain: enough steps keep that a small part of the region (each is
     # about 6 ms, bound by the host link)
-    steps = max(10, args.steps // 2)
+    steps = max(20, args.steps)
     n = len(step.layers)
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev = lambda: torch.cuda.Event()
