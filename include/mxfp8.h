@@ -282,6 +282,43 @@ int mxfp8_gemm(const void* A_dev, const void* sA_dev, const void* B_dev, const v
                void* stream);
 
 /*
+ * mxfp8_gemm with a caller-owned device workspace, which lets the GEMM run its last,
+ * partial wave of output tiles as split-K pieces. The rest of the tiles run as usual.
+ *  - Split-K: each tile of that wave is cut into 3 ranges of K on separate CTA pairs. Two
+ *    pieces leave FP32 partial sums in the workspace, and the third adds them before
+ *    rounding.
+ *  - Without a workspace: that wave runs as half-width tiles. On deep reductions the
+ *    pieces finish it sooner.
+ *  - Results: either way they meet the mxfp8_gemm accuracy bound. They are not bit-identical
+ *    to mxfp8_gemm's, because the FP32 sums are added in another order.
+ * Arguments as for mxfp8_gemm, plus:
+ *   workspace_dev    device memory, 16-byte aligned, or NULL; the library allocates nothing.
+ *   workspace_bytes  its size. Split-K runs only when it is at least
+ *                    mxfp8_gemm_workspace_bytes for the same problem, else the call
+ *                    proceeds as mxfp8_gemm.
+ * The workspace holds the partial sums and one arrival counter per tile, CTA and epilogue
+ * warp. It must be zero-filled before its first use. Each launch sets its counters back to
+ * zero, so it needs no reset between calls or CUDA-graph replays. There is one exception:
+ * after a call that latched MXFP8_ERR_TIMEOUT, zero-fill it again. Only one GEMM may use a
+ * workspace at a time, so GEMMs that can run concurrently (other streams) need workspaces of
+ * their own.
+ * Errors as for mxfp8_gemm, plus MXFP8_ERR_ALIGNMENT for a misaligned workspace. A piece
+ * whose partners do not arrive within the pipeline wait limit latches MXFP8_ERR_TIMEOUT.
+ */
+int mxfp8_gemm_ws(const void* A_dev, const void* sA_dev, const void* B_dev, const void* sB_dev,
+                  void* C_dev, int64_t M, int64_t N, int64_t K, int op, int out_dtype,
+                  void* workspace_dev, size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes with which mxfp8_gemm_ws runs this GEMM's last wave as split-K pieces
+ * on the current device. The size depends on the device's SM count. 0 means the GEMM never
+ * splits: its last wave is full or too wide, or K is too shallow (fewer than 120 stages of
+ * 128, where the half tiles finish first). The same 0 is returned for arguments mxfp8_gemm
+ * would refuse, and for an unsupported device.
+ */
+size_t mxfp8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int op, int out_dtype);
+
+/*
  * Grouped (MoE expert) block-scaled GEMMs over token segments off[e] .. off[e+1]
  * (expert_offsets_dev as for mxfp8_quantize_grouped).
  *   op FPROP / DGRAD:  A [total_rows][K] with grouped ROW scales (one block per expert,

@@ -43,6 +43,8 @@ SIGNATURES = {
     "mxfp8_quantize_grouped_dual": (_I, [_P, _I64, _I64, _P, _I, _P, _P, _P, _P, _P]),
     "mxfp8_quantize_grouped": (_I, [_P, _I64, _I64, _I, _P, _I, _P, _P, _P]),
     "mxfp8_gemm": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _P]),
+    "mxfp8_gemm_ws": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _P, _SZ, _P]),
+    "mxfp8_gemm_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I, _I]),
     "mxfp8_grouped_gemm": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _I, _P]),
     "mxfp8_selfcheck_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "mxfp8_selfcheck": (_I, [_P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _SZ, _P, _P]),
@@ -287,8 +289,10 @@ def quantize_grouped(src: torch.Tensor, offsets: torch.Tensor, axis: int = ROW, 
 # ----------------------------------------------------------------------------- GEMMs
 
 def gemm(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.Tensor, op: int = FPROP,
-         out_dtype: int = OUT_BF16, out=None, stream=None) -> torch.Tensor:
-    """C[M, N] = deq(A)[M, K] . deq(B)[N, K]^T with swizzled scales (both K-major)."""
+         out_dtype: int = OUT_BF16, out=None, stream=None, workspace=None) -> torch.Tensor:
+    """C[M, N] = deq(A)[M, K] . deq(B)[N, K]^T with swizzled scales (both K-major). With a
+    `workspace` (a zero-filled uint8 CUDA tensor of gemm_workspace_bytes(...) bytes, used by
+    one GEMM at a time) the last wave of tiles may run as split-K pieces (mxfp8_gemm_ws)."""
     _require(a, torch.uint8, "A")
     _require(b, torch.uint8, "B")
     m, k = a.shape
@@ -298,9 +302,21 @@ def gemm(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.Tensor, o
     if out is None:
         dt = torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32
         out = torch.empty((m, n), dtype=dt, device=a.device)
-    _check(lib().mxfp8_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out), m, n, k, op,
-                            out_dtype, _stream(stream)), "mxfp8_gemm")
+    if workspace is None:
+        _check(lib().mxfp8_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out), m, n, k, op,
+                                out_dtype, _stream(stream)), "mxfp8_gemm")
+    else:
+        _require(workspace, torch.uint8, "workspace")
+        _check(lib().mxfp8_gemm_ws(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out), m, n, k, op,
+                                   out_dtype, _ptr(workspace), workspace.numel(),
+                                   _stream(stream)), "mxfp8_gemm_ws")
     return out
+
+
+def gemm_workspace_bytes(m: int, n: int, k: int, op: int = FPROP, out_dtype: int = OUT_BF16) -> int:
+    """Bytes of workspace with which gemm(..., workspace=...) runs the split-K last wave on
+    the current device (0: it never does)."""
+    return int(lib().mxfp8_gemm_workspace_bytes(m, n, k, op, out_dtype))
 
 
 def grouped_gemm(a, sa, b, sb, offsets: torch.Tensor, op: int = FPROP,

@@ -323,16 +323,35 @@ static int gemm_checks(const void* A, const void* sA, const void* B, const void*
 int mxfp8_gemm(const void* A_dev, const void* sA_dev, const void* B_dev, const void* sB_dev,
                void* C_dev, int64_t M, int64_t N, int64_t K, int op, int out_dtype,
                void* stream) {
+  return mxfp8_gemm_ws(A_dev, sA_dev, B_dev, sB_dev, C_dev, M, N, K, op, out_dtype, nullptr,
+                       0, stream);
+}
+
+size_t mxfp8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int op, int out_dtype) {
+  if (M <= 0 || N <= 0 || K <= 0 || M > 0x7FFFFF00 || N > 0x7FFFFF00 || K > 0x7FFFFF00)
+    return 0;
+  if (op < MXFP8_OP_FPROP || op > MXFP8_OP_WGRAD) return 0;
+  if (out_dtype != MXFP8_OUT_BF16 && out_dtype != MXFP8_OUT_FP32) return 0;
+  DeviceState* d = nullptr;
+  if (device_state(&d) != MXFP8_OK) return 0;
+  return gemm_workspace_bytes(M, N, K, out_dtype);
+}
+
+int mxfp8_gemm_ws(const void* A_dev, const void* sA_dev, const void* B_dev, const void* sB_dev,
+                  void* C_dev, int64_t M, int64_t N, int64_t K, int op, int out_dtype,
+                  void* workspace_dev, size_t workspace_bytes, void* stream) {
   if (M <= 0 || N <= 0 || K <= 0) return MXFP8_ERR_INVALID_ARG;
   if (M > 0x7FFFFF00 || N > 0x7FFFFF00 || K > 0x7FFFFF00) return MXFP8_ERR_INVALID_ARG;
   if (K % 32 || M % 16 || N % 16) return MXFP8_ERR_ALIGNMENT;
   int st = gemm_checks(A_dev, sA_dev, B_dev, sB_dev, C_dev, op, out_dtype);
   if (st != MXFP8_OK) return st;
+  if (workspace_dev && (reinterpret_cast<uintptr_t>(workspace_dev) & 15))
+    return MXFP8_ERR_ALIGNMENT;
   DeviceState* d = nullptr;
   st = device_state(&d);
   if (st != MXFP8_OK) return st;
   GemmArgs a{A_dev, sA_dev, B_dev, sB_dev, C_dev, M, N, K, op, out_dtype, nullptr, 0, 0,
-             d->status};
+             d->status, workspace_dev, workspace_dev ? workspace_bytes : 0};
   return launch_gemm(a, static_cast<cudaStream_t>(stream));
 }
 

@@ -53,6 +53,8 @@ constexpr int BM = 128;           // accumulator rows = TMEM lanes
 constexpr int BK = 128;           // K elements (bytes) per pipeline stage
 constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, each half of the columns
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+// Split-K of a 384-wide kernel's last wave: each tile of it runs as this many K pieces.
+constexpr int kSplitK = 3;
 constexpr int kMaxExperts = 1024;
 
 enum Mode : int { kDense = 0, kGroupRows = 1, kGroupWgrad = 2 };
@@ -102,8 +104,13 @@ struct Params {
   int* status;
   uint64_t wait_ns;      // pipeline waits give up after this (MXFP8_ERR_TIMEOUT)
   uint64_t drain_ns;     // waits for work already in flight, on the way out (never shorter)
-  // dense 2SM kernel: pair tiles from this index on each run as two half-width tiles
+  // dense 2SM kernel: the pair tiles from this index on run as two half-width tiles, or
+  // (split_k >= 2) as split_k pieces that each take a range of K of the whole tile
   int64_t split_from = INT64_MAX;
+  int split_k = 0;
+  uint4* ws = nullptr;           // split_k: FP32 partials of pieces 0 .. split_k - 2
+  uint32_t* ws_flags = nullptr;  // split_k: one arrival counter per (tile, CTA rank, epilogue
+                                 // warp); zero between launches
 };
 
 // Everything a role needs to know about one output tile.
@@ -660,12 +667,17 @@ struct DuoTile {
   int64_t sfb_idx0 = 0, sfb_idx1 = 0;  // grouped: the two B scale tiles at stage 0
   int b_z = 0, c_z = 0;        // expert index for the B (grouped rows) and C (wgrad) maps
   int width = 0;               // output columns of the tile: BN, or BN / 2 for a half tile
+  int kb0 = 0;                 // first K stage of a split-K piece (else 0)
+  int piece = -1;              // split-K piece index, -1 for a whole tile or a half tile
+  int slot = 0;                // split-K: the tile's index among the split tiles
 };
 
-// Dense pair tiles. Work item `pid` below p.split_from is pair tile pid; from there on, two
-// items share one pair tile, each taking half of its columns (256 x BN/2). The host puts the
-// split at the last, partial wave of clusters when its halves fit in one wave, so that wave
-// takes about half as long.
+// Dense pair tiles. Work item `pid` below p.split_from is pair tile pid. From there on the
+// items share pair tiles, in one of two ways:
+// - two items per tile, each taking half of its columns (256 x BN/2);
+// - p.split_k items per tile, each taking a range of its K stages (split-K).
+// The host puts the split at the last, partial wave of clusters when the pieces fit in one
+// wave, so that wave takes a fraction as long.
 // The work-item arithmetic is 32-bit: the host checks that the pair tiles and items of a
 // launch stay below 2^31, and 64-bit divisions (emulated in software) cost every role a
 // visible delay before its first tile.
@@ -677,8 +689,15 @@ __device__ __forceinline__ DuoTile duo_tile(const Params& p, int64_t item, uint3
   int half = -1;  // -1: the whole tile; 0 / 1: its left / right half
   if (item >= p.split_from) {
     const uint32_t r = static_cast<uint32_t>(item - p.split_from);
-    pid = static_cast<uint32_t>(p.split_from) + r / 2;
-    half = static_cast<int>(r & 1);
+    if (p.split_k) {
+      const uint32_t slot = r / static_cast<uint32_t>(p.split_k);
+      pid = static_cast<uint32_t>(p.split_from) + slot;
+      t.piece = static_cast<int>(r - slot * static_cast<uint32_t>(p.split_k));
+      t.slot = static_cast<int>(slot);
+    } else {
+      pid = static_cast<uint32_t>(p.split_from) + r / 2;
+      half = static_cast<int>(r & 1);
+    }
   }
   t.live = pid < n_pm * static_cast<uint32_t>(p.num_n_tiles);
   if (!t.live) return t;
@@ -794,6 +813,12 @@ __device__ __forceinline__ DuoTile duo_tile_of(const Params& p, const DuoSeg* se
     t.nk = static_cast<int>((p.K + BK - 1) / BK);
     t.last_blocks = static_cast<int>(((p.K - (t.nk - 1) * BK) + 31) / 32);
     t.c_z = 0;
+    if (t.piece >= 0) {  // split-K: stages [nk * i / S, nk * (i + 1) / S) of the tile
+      const int S = p.split_k, nk = t.nk;
+      t.kb0 = nk * t.piece / S;
+      t.nk = nk * (t.piece + 1) / S - t.kb0;
+      if (t.piece != S - 1) t.last_blocks = 4;  // only the last piece holds the ragged stage
+    }
     return t;
   } else {
     return duo_tile_grouped<BN, kMode>(p, seg, pid, crank);
@@ -938,7 +963,8 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
         const uint32_t s = it % kStages, ph = (it / kStages) & 1;
         if (!warp_wait(&empty[s], ph ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
         const uint32_t bar = full0 + 8 * s;
-        const int32_t kx = static_cast<int32_t>(t.k_origin + kb * BK);
+        const int64_t kg = t.kb0 + kb;  // K stage within the whole tile
+        const int32_t kx = static_cast<int32_t>(t.k_origin + kg * BK);
         if (issuer) {
           if (leader) mbar_arrive_expect_tx(&full[s], 2 * tx);
           tma_load_2d_2sm(smem + D::kOffA + s * D::kABytes, &map_a, kx,
@@ -960,9 +986,9 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
           }
           if constexpr (kMode == kDense) {
             tma_load_3d_2sm(smem + D::kOffSfa + s * D::kSfaBytes, &map_sfa, 0,
-                            static_cast<int32_t>(kb), static_cast<int32_t>(t.mt), bar);
+                            static_cast<int32_t>(kg), static_cast<int32_t>(t.mt), bar);
             tma_load_3d_2sm(smem + D::kOffSfb + s * D::kSfbBytes, &map_sfb, 0,
-                            static_cast<int32_t>(kb), static_cast<int32_t>(t.sfb_tile), bar);
+                            static_cast<int32_t>(kg), static_cast<int32_t>(t.sfb_tile), bar);
           } else {  // scale tiles by flat index, one 512-byte tile per load
             tma_load_2d_2sm(smem + D::kOffSfa + s * D::kSfaBytes, &map_sfa, 0,
                             static_cast<int32_t>(t.sfa_idx + kb), bar);
@@ -1102,6 +1128,112 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
         // 384-wide (BF16 out): 6 chunks of 32 columns per warp, converted to BF16 pairs as
         // they leave TMEM in 3 rounds of 2 chunks, so that the accumulator is handed back
         // before any store; then 32-byte boxes (16 columns) with the 32-byte swizzle.
+        // One 32-row x 16-column box of BF16 pairs (lo: columns 0-7, hi: 8-15) through the
+        // warp's staging box, 16-byte chunks swapped on alternate row groups (32-byte swizzle).
+        auto store_box = [&](uint4 lo, uint4 hi, int col) {
+          const int sw = (lane >> 2) & 1;
+          if (lane == 0) bulk_wait_read_all();  // the box is free again
+          __syncwarp();
+          *reinterpret_cast<uint4*>(box + lane * 32 + 16 * sw) = lo;
+          *reinterpret_cast<uint4*>(box + lane * 32 + 16 * (sw ^ 1)) = hi;
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&map_c, box, static_cast<int32_t>(t.n0 + col),
+                         static_cast<int32_t>(t.m0 + 32 * q));
+            bulk_commit_group();
+          }
+        };
+        if (t.piece >= 0) {
+          // A split-K piece (the host gives each at least one stage). Pieces other than the
+          // last write their FP32 accumulator to the workspace and count themselves in on
+          // the warp's arrival counter (a release); the last piece waits until all have
+          // arrived, sets the counter back to zero for the next launch (or graph replay),
+          // and adds the partials before converting, round by round, storing each round
+          // at once (its tile is the CTA's last: holding the accumulator a little longer
+          // delays nothing). Workspace layout, in 16-byte units: [tile slot][piece][CTA
+          // rank][epilogue warp][round][column group][lane], so that a warp's 16-byte
+          // stores cover 512 contiguous bytes and each lane reads back what the same lane
+          // of the same warp wrote.
+          constexpr int S = kSplitK;
+          const bool writer = t.piece < S - 1;
+          const int ew = warp - 2;
+          auto ws_at = [&](int piece, int r) {
+            return p.ws + ((((static_cast<size_t>(t.slot) * (S - 1) + piece) * 2 + crank) *
+                                kEpiWarps + ew) * 3 + r) * (16 * 32) + lane;
+          };
+          uint32_t* const count = p.ws_flags + (static_cast<size_t>(t.slot) * 2 + crank) * kEpiWarps + ew;
+          int got = 0;
+          if (lane == 0) got = mbar_wait_bounded(&acc_full[0], acc_it & 1, abort_flag, p.wait_ns);
+          if (!writer && lane == 0 && got)
+            got = flag_wait_bounded(count, S - 1, abort_flag, p.wait_ns);
+          got = __shfl_sync(0xFFFFFFFFu, got, 0);
+          if (!got) { ok = false; break; }
+          if (!writer) {
+            (void)ld_acquire_gpu(count);  // every lane
+            __syncwarp();
+            if (lane == 0) *count = 0;    // every writer of this launch has arrived
+          }
+          tc_fence_after();
+          __syncwarp();
+          const uint32_t base = tmem + (static_cast<uint32_t>(32 * q) << 16) + half * 192;
+#pragma unroll 1
+          for (int r = 0; r < 3; ++r) {
+            uint32_t v[2][32];
+            tmem_ld_32x32b_x32(base + 64 * r, v[0]);
+            tmem_ld_32x32b_x32(base + 64 * r + 32, v[1]);
+            tmem_ld_wait();
+            if (writer) {
+              uint4* w = ws_at(t.piece, r);
+#pragma unroll
+              for (int g = 0; g < 16; ++g)
+                __stcg(w + 32 * g, make_uint4(v[g >> 3][4 * (g & 7)], v[g >> 3][4 * (g & 7) + 1],
+                                              v[g >> 3][4 * (g & 7) + 2],
+                                              v[g >> 3][4 * (g & 7) + 3]));
+              continue;
+            }
+#pragma unroll
+            for (int pp = 0; pp < S - 1; ++pp) {
+              const uint4* w = ws_at(pp, r);
+#pragma unroll
+              for (int g = 0; g < 16; ++g) {
+                const uint4 x = __ldcg(w + 32 * g);
+                const int u = g >> 3, c = 4 * (g & 7);
+                v[u][c] = __float_as_uint(__uint_as_float(v[u][c]) + __uint_as_float(x.x));
+                v[u][c + 1] = __float_as_uint(__uint_as_float(v[u][c + 1]) + __uint_as_float(x.y));
+                v[u][c + 2] = __float_as_uint(__uint_as_float(v[u][c + 2]) + __uint_as_float(x.z));
+                v[u][c + 3] = __float_as_uint(__uint_as_float(v[u][c + 3]) + __uint_as_float(x.w));
+              }
+            }
+            if (32 * q < t.rows_valid) {
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                uint32_t bb[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  bb[i] = cvt_bf16x2(__uint_as_float(v[u][2 * i + 1]), __uint_as_float(v[u][2 * i]));
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                  const int col = 32 * (half * 6 + 2 * r + u) + 16 * g;
+                  if (col < t.cols_valid)
+                    store_box(make_uint4(bb[8 * g], bb[8 * g + 1], bb[8 * g + 2], bb[8 * g + 3]),
+                              make_uint4(bb[8 * g + 4], bb[8 * g + 5], bb[8 * g + 6], bb[8 * g + 7]),
+                              col);
+                }
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty0);
+          ++acc_it;
+          if (writer) {  // the partial is out: release it to the last piece
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) red_release_add_gpu(count, 1u);
+          }
+          continue;
+        }
         uint32_t b[6][16];
         if (t.nk > 0) {
           const uint32_t aph = acc_it & 1;
@@ -1541,6 +1673,41 @@ int duo_width(int64_t M, int64_t N, bool fp32) {
   return best;
 }
 
+// Split-K last waves: a 384-wide kernel's partial last wave of `tail` pair tiles runs as
+// kSplitK K pieces per tile (instead of two half tiles) when the pieces fit in one wave
+// and every piece gets at least kSplitKMinStages K stages. The workspace holds the FP32
+// partials of kSplitK - 1 pieces per tile (the last piece adds them) and one arrival
+// counter per tile, CTA rank and epilogue warp. Measured on 4096 x 4096 x K (GB300): the
+// pieces run at about 600 ns per stage against 307 for a half tile, and the reduction
+// costs about 10 us, so split-K wins only on deep reductions. At K = 24576 it takes 245 to 235 us;
+// at K = 12288 it breaks even; at K <= 8192 it loses.
+constexpr int kSplitKMinStages = 40;  // per piece; MXFP8_GEMM_SPLITK_MIN_STAGES overrides
+constexpr size_t kSplitKPartialBytes = size_t(2) * BM * 384 * 4;  // FP32, one pair tile
+constexpr size_t kSplitKFlagBytes = size_t(2) * kEpiWarps * 4;  // one tile's counters
+
+struct SplitPlan {
+  int64_t tail = 0;      // split tiles (0: no split-K)
+  size_t bytes = 0;      // workspace bytes it needs
+};
+
+SplitPlan split_plan(int64_t pair_tiles, int64_t fit, int64_t n_kt) {
+  SplitPlan s;
+  static const bool on = [] {
+    const char* e = getenv("MXFP8_GEMM_SPLITK");
+    return !(e && e[0] == '0');
+  }();
+  static const int64_t min_stages = [] {
+    const char* e = getenv("MXFP8_GEMM_SPLITK_MIN_STAGES");
+    const long v = e ? atol(e) : 0;
+    return static_cast<int64_t>(v >= 1 ? v : kSplitKMinStages);
+  }();
+  const int64_t tail = pair_tiles % fit;
+  if (!on || tail == 0 || kSplitK * tail > fit || n_kt < kSplitK * min_stages) return s;
+  s.tail = tail;
+  s.bytes = static_cast<size_t>(tail) * ((kSplitK - 1) * kSplitKPartialBytes + kSplitKFlagBytes);
+  return s;
+}
+
 // Dense GEMM on CTA pairs with 256 x BN tiles (tcgen05 cta_group::2).
 template <int BN>
 int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
@@ -1561,11 +1728,22 @@ int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
   if (2 * pair_tiles > INT32_MAX) return MXFP8_ERR_INVALID_ARG;  // 32-bit item arithmetic
   const int64_t fit = max_duo_clusters<BN>();
   if (fit <= 0) return MXFP8_ERR_CUDA;
-  // The tiles of the last, partial wave run as half-width tiles when their halves still fit
-  // in one wave of clusters (256- and 384-wide tiles).
+  // The tiles of the last, partial wave run as split-K pieces (384-wide, deep K, with a
+  // large enough workspace), else as half-width tiles when their halves still fit in one
+  // wave of clusters (256- and 384-wide tiles).
   int64_t items = pair_tiles;
   const int64_t tail = pair_tiles % fit;
-  if (BN != 192 && half_tail_enabled() && tail > 0 && 2 * tail <= fit) {
+  const SplitPlan sp = BN == 384 ? split_plan(pair_tiles, fit, n_kt) : SplitPlan{};
+  if (sp.tail > 0 && a.workspace && a.workspace_bytes >= sp.bytes &&
+      (reinterpret_cast<uintptr_t>(a.workspace) & 15) == 0) {
+    p.split_from = pair_tiles - tail;
+    p.split_k = kSplitK;
+    p.ws = static_cast<uint4*>(a.workspace);
+    p.ws_flags = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.workspace) +
+                                             static_cast<size_t>(tail) * (kSplitK - 1) *
+                                                 kSplitKPartialBytes);
+    items = pair_tiles + (kSplitK - 1) * tail;
+  } else if (BN != 192 && half_tail_enabled() && tail > 0 && 2 * tail <= fit) {
     p.split_from = pair_tiles - tail;
     items = pair_tiles + tail;
   }
@@ -1646,6 +1824,16 @@ int duo_grouped_width(int) {
 }  // namespace
 
 void set_wait_limit_ns(uint64_t ns) { g_wait_override_ns.store(ns, std::memory_order_relaxed); }
+
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int out_dtype) {
+  const bool fp32 = out_dtype == MXFP8_OUT_FP32;
+  const int64_t num_m_tiles = (M + BM - 1) / BM;
+  if (N <= 128 || num_m_tiles < 2 || !duo_enabled() || duo_width(M, N, fp32) != 384) return 0;
+  const int64_t fit = max_duo_clusters<384>();
+  if (fit <= 0) return 0;
+  const int64_t pair_tiles = ((num_m_tiles + 1) / 2) * ((N + 383) / 384);
+  return split_plan(pair_tiles, fit, (K + BK - 1) / BK).bytes;
+}
 
 int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   Params p{};

@@ -68,10 +68,16 @@ struct GemmArgs {
   int num_experts;
   int64_t total_rows;
   int* status;
+  // dense call: caller-owned workspace for a split-K last wave (nullptr: none)
+  void* workspace = nullptr;
+  size_t workspace_bytes = 0;
 };
 
 // Returns MXFP8_OK or an mxfp8_status code.
 int launch_gemm(const GemmArgs& a, cudaStream_t stream);
+// Bytes of workspace with which launch_gemm runs this dense GEMM's last wave as split-K
+// pieces on the current device (0: it never does).
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int out_dtype);
 int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream);
 
 struct SelfcheckArgs {
