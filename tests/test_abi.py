@@ -146,6 +146,26 @@ def test_multi_job_argument_errors_need_no_device(lib):
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU failure path")
+def test_gemm_workspace_argument_errors_need_no_device(lib):
+    p = ctypes.c_void_p(0x10000)
+    bad = ctypes.c_void_p(0x10008)        # 8-byte aligned only
+    gw = lib.mxfp8_gemm_ws
+    # the plain GEMM's checks, then the workspace's alignment, all before the device
+    assert gw(p, p, p, p, p, 128, 128, 48, 0, 0, p, 1 << 20, None) == m.ERR_ALIGNMENT
+    assert gw(p, p, p, p, p, 0, 128, 64, 0, 0, p, 1 << 20, None) == m.ERR_INVALID_ARG
+    assert gw(p, None, p, p, p, 128, 128, 64, 0, 0, p, 1 << 20, None) == m.ERR_INVALID_ARG
+    assert gw(p, p, p, p, p, 128, 128, 64, 0, 0, bad, 1 << 20, None) == m.ERR_ALIGNMENT
+    # a NULL workspace is the plain GEMM: without a GPU it fails like one
+    assert gw(p, p, p, p, p, 128, 128, 64, 0, 0, None, 0, None) in (
+        m.ERR_CUDA, m.ERR_UNSUPPORTED_ARCH)
+    # sizes: 0 for invalid arguments, and 0 without a supported device
+    wb = lib.mxfp8_gemm_workspace_bytes
+    assert wb(-1, 4096, 24576, 0, 0) == 0
+    assert wb(4096, 4096, 24576, 3, 0) == 0
+    assert wb(4096, 4096, 24576, 0, 2) == 0
+    assert wb(4096, 4096, 24576, 0, 0) == 0   # no GPU here
+
+
 def test_valid_call_without_a_gpu_fails_cleanly(lib):
     p = ctypes.c_void_p(0x10000)
     assert lib.mxfp8_quantize(p, 64, 64, m.ROW, p, p, m.SWIZZLED, None) in (
