@@ -104,12 +104,11 @@ struct Params {
   int* status;
   uint64_t wait_ns;      // pipeline waits give up after this (MXFP8_ERR_TIMEOUT)
   uint64_t drain_ns;     // waits for work already in flight, on the way out (never shorter)
-  // dense 2SM kernel: the pair tiles from this index on run as two half-width tiles, or
-  // (split_k >= 2) as split_k pieces that each take a range of K of the whole tile
+  // dense 2SM kernel: the pair tiles from this index on run as two half-width tiles, or (the
+  // split-K kernel instance) as kSplitK pieces that each take a range of K of the whole tile
   int64_t split_from = INT64_MAX;
-  int split_k = 0;
-  uint4* ws = nullptr;           // split_k: FP32 partials of pieces 0 .. split_k - 2
-  uint32_t* ws_flags = nullptr;  // split_k: one arrival counter per (tile, CTA rank, epilogue
+  uint4* ws = nullptr;           // split-K: FP32 partials of pieces 0 .. kSplitK - 2
+  uint32_t* ws_flags = nullptr;  // split-K: one arrival counter per (tile, CTA rank, epilogue
                                  // warp); zero between launches
 };
 
@@ -675,13 +674,13 @@ struct DuoTile {
 // Dense pair tiles. Work item `pid` below p.split_from is pair tile pid. From there on the
 // items share pair tiles, in one of two ways:
 // - two items per tile, each taking half of its columns (256 x BN/2);
-// - p.split_k items per tile, each taking a range of its K stages (split-K).
+// - kSplitK items per tile, each taking a range of its K stages (the split-K instance).
 // The host puts the split at the last, partial wave of clusters when the pieces fit in one
 // wave, so that wave takes a fraction as long.
 // The work-item arithmetic is 32-bit: the host checks that the pair tiles and items of a
 // launch stay below 2^31, and 64-bit divisions (emulated in software) cost every role a
 // visible delay before its first tile.
-template <int BN>
+template <int BN, bool kSplit>
 __device__ __forceinline__ DuoTile duo_tile(const Params& p, int64_t item, uint32_t crank) {
   DuoTile t;
   const uint32_t n_pm = static_cast<uint32_t>((p.num_m_tiles + 1) / 2);
@@ -689,10 +688,10 @@ __device__ __forceinline__ DuoTile duo_tile(const Params& p, int64_t item, uint3
   int half = -1;  // -1: the whole tile; 0 / 1: its left / right half
   if (item >= p.split_from) {
     const uint32_t r = static_cast<uint32_t>(item - p.split_from);
-    if (p.split_k) {
-      const uint32_t slot = r / static_cast<uint32_t>(p.split_k);
+    if constexpr (kSplit) {
+      const uint32_t slot = r / static_cast<uint32_t>(kSplitK);
       pid = static_cast<uint32_t>(p.split_from) + slot;
-      t.piece = static_cast<int>(r - slot * static_cast<uint32_t>(p.split_k));
+      t.piece = static_cast<int>(r - slot * static_cast<uint32_t>(kSplitK));
       t.slot = static_cast<int>(slot);
     } else {
       pid = static_cast<uint32_t>(p.split_from) + r / 2;
@@ -805,16 +804,17 @@ __device__ DuoTile duo_tile_grouped(const Params& p, const DuoSeg* seg, int64_t 
   return t;
 }
 
-template <int BN, int kMode>
+template <int BN, int kMode, bool kSplit = false>
 __device__ __forceinline__ DuoTile duo_tile_of(const Params& p, const DuoSeg* seg, int64_t pid,
                                                uint32_t crank) {
   if constexpr (kMode == kDense) {
-    DuoTile t = duo_tile<BN>(p, pid, crank);
+    DuoTile t = duo_tile<BN, kSplit>(p, pid, crank);
     t.nk = static_cast<int>((p.K + BK - 1) / BK);
     t.last_blocks = static_cast<int>(((p.K - (t.nk - 1) * BK) + 31) / 32);
     t.c_z = 0;
-    if (t.piece >= 0) {  // split-K: stages [nk * i / S, nk * (i + 1) / S) of the tile
-      const int S = p.split_k, nk = t.nk;
+    if (kSplit && t.piece >= 0) {  // split-K: stages [nk * i / S, nk * (i + 1) / S)
+      constexpr int S = kSplitK;
+      const int nk = t.nk;
       t.kb0 = nk * t.piece / S;
       t.nk = nk * (t.piece + 1) / S - t.kb0;
       if (t.piece != S - 1) t.last_blocks = 4;  // only the last piece holds the ragged stage
@@ -827,7 +827,7 @@ __device__ __forceinline__ DuoTile duo_tile_of(const Params& p, const DuoSeg* se
 
 // Bytes one CTA stages for its stage use number `use` (the producer's running count):
 // found by walking the CTA's tiles again. Only the drain after an abort needs it.
-template <int BN, int kMode>
+template <int BN, int kMode, bool kSplit>
 __device__ uint32_t duo_use_bytes(const Params& p, const DuoSeg* seg, int64_t first_id,
                                   int64_t id_step, uint32_t crank, uint32_t use) {
   using D = Duo<BN, kMode>;
@@ -836,7 +836,7 @@ __device__ uint32_t duo_use_bytes(const Params& p, const DuoSeg* seg, int64_t fi
   } else {
     uint32_t at = 0;
     for (int64_t id = first_id;; id += id_step) {
-      const DuoTile t = duo_tile_of<BN, kMode>(p, seg, id, crank);
+      const DuoTile t = duo_tile_of<BN, kMode, kSplit>(p, seg, id, crank);
       if (!t.live) break;
       if (use < at + static_cast<uint32_t>(t.nk))
         return t.width == BN ? D::kStageBytes : D::kHalfStageBytes;
@@ -846,7 +846,9 @@ __device__ uint32_t duo_use_bytes(const Params& p, const DuoSeg* seg, int64_t fi
   }
 }
 
-template <int BN, int kMode>
+// kSplit: the dense kernel whose last wave runs as split-K pieces (a separate instance, so
+// that the split code costs the other launches nothing).
+template <int BN, int kMode, bool kSplit = false>
 __global__ void __launch_bounds__(kThreads, 1)
 mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
                       const __grid_constant__ CUtensorMap map_b,
@@ -955,7 +957,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     uint32_t it = 0;
     bool ok = true;
     for (int64_t id = first_id; ok; id += id_step) {
-      const DuoTile t = duo_tile_of<BN, kMode>(p, seg, id, crank);
+      const DuoTile t = duo_tile_of<BN, kMode, kSplit>(p, seg, id, crank);
       if (!t.live) break;
       const bool whole = t.width == BN;
       const uint32_t tx = whole ? D::kStageBytes : D::kHalfStageBytes;
@@ -1036,7 +1038,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     // start at a 128-row tile); a 384-wide kernel's half tile is its first MMA alone
     constexpr uint32_t kHalfN = D::kWide ? 0u : (mxf8_idesc(2 * BM, BN / 2, 0, 0) ^ kId0);
     for (int64_t id = first_id; ok; id += id_step) {
-      const DuoTile t = duo_tile_of<BN, kMode>(p, seg, id, crank);
+      const DuoTile t = duo_tile_of<BN, kMode, kSplit>(p, seg, id, crank);
       if (!t.live) break;
       if (t.nk == 0) continue;  // an empty expert's dW tile: the epilogue writes zeros
       const uint32_t buf = acc_it % D::kAcc, aph = (acc_it / D::kAcc) & 1;
@@ -1122,7 +1124,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
     uint32_t acc_it = 0;
     bool ok = true;
     for (int64_t id = first_id; ok; id += id_step) {
-      const DuoTile t = duo_tile_of<BN, kMode>(p, seg, id, crank);
+      const DuoTile t = duo_tile_of<BN, kMode, kSplit>(p, seg, id, crank);
       if (!t.live) break;
       if constexpr (D::kWide) {
         // 384-wide (BF16 out): 6 chunks of 32 columns per warp, converted to BF16 pairs as
@@ -1144,7 +1146,7 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
             bulk_commit_group();
           }
         };
-        if (t.piece >= 0) {
+        if constexpr (kSplit) if (t.piece >= 0) {
           // A split-K piece (the host gives each at least one stage). Pieces other than the
           // last write their FP32 accumulator to the workspace and count themselves in on
           // the warp's arrival counter (a release); the last piece waits until all have
@@ -1399,7 +1401,8 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
         uint64_t* b = &full[i % kStages];
         const bool only0 = i < i0 && i >= i1, only1 = i >= i0 && i < i1;
         if (!only0 && !only1) continue;
-        const uint32_t bytes = duo_use_bytes<BN, kMode>(p, seg, first_id, id_step, crank, i);
+        const uint32_t bytes =
+            duo_use_bytes<BN, kMode, kSplit>(p, seg, first_id, id_step, crank, i);
         if (only0) mbar_complete_tx(b, bytes);
         else mbar_arrive_expect_tx(b, bytes);
       }
@@ -1737,7 +1740,6 @@ int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
   if (sp.tail > 0 && a.workspace && a.workspace_bytes >= sp.bytes &&
       (reinterpret_cast<uintptr_t>(a.workspace) & 15) == 0) {
     p.split_from = pair_tiles - tail;
-    p.split_k = kSplitK;
     p.ws = static_cast<uint4*>(a.workspace);
     p.ws_flags = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.workspace) +
                                              static_cast<size_t>(tail) * (kSplitK - 1) *
@@ -1750,6 +1752,20 @@ int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
   const int64_t clusters = items < fit ? items : fit;
   if (clusters <= 0) return MXFP8_OK;
   auto k = mxfp8_gemm_2sm_kernel<BN, kDense>;
+  if constexpr (BN == 384) {
+    if (p.ws) {
+      k = mxfp8_gemm_2sm_kernel<BN, kDense, true>;
+      static bool attr_set[64] = {};  // per device
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess) return MXFP8_ERR_CUDA;
+      if (dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 D::kSmemBytes) != cudaSuccess)
+          return MXFP8_ERR_CUDA;
+        attr_set[dev] = true;
+      }
+    }
+  }
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = cluster2_config(2 * clusters, D::kSmemBytes, stream, attr);
   cfg.numAttrs += pdl_attr(&attr[1]);
