@@ -31,6 +31,10 @@
 // empty barrier, armed by tcgen05.commit, precedes its refill).
 // Every wait is bounded: past the limit the CTA latches MXFP8_ERR_TIMEOUT, all roles
 // leave their loops, outstanding copies and MMAs are waited for, TMEM is freed.
+// A partial last wave of 2SM tiles runs as half-width tiles, or, for deep reductions with
+// a caller-owned workspace (mxfp8_gemm_ws), as split-K pieces in a separate kernel
+// instance. Every kernel is launched with programmatic stream serialization: it sets up,
+// then waits for the previous kernel before touching global memory.
 
 #include <atomic>
 #include <cmath>
