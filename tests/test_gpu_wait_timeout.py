@@ -8,7 +8,8 @@ copies and tensor-core operations it has in flight (under its own drain limit of
 2 s) and returns. The context stays usable: with the default limit restored, the same GEMM
 matches the oracle and the status word stays clear. The post lists the failures a pipeline must survive in its
 section "Correctness: how it fails"; this is the library's own bounded-wait path, not a
-fault. It runs in a child process, so the rest of the suite keeps its own CUDA context.
+fault. The split-K instance is covered too: after its timeout the workspace is zero-filled
+again, as the header asks, and the next call matches the oracle. It runs in a child process, so the rest of the suite keeps its own CUDA context.
 """
 import os
 import subprocess
@@ -70,6 +71,26 @@ CHILD = textwrap.dedent(r"""
     lo, hi = int(off[e]), int(off[e + 1])
     sampled_gemm_check(y[lo:hi], rows_of(x[lo:hi], O.ROW), rows_of(w[e], O.ROW), hi - lo, nn,
                        5, True, "grouped after timeout")
+    # the split-K instance (forced on a shallow K by the parent's environment): a timed-out
+    # launch, then, with the workspace zero-filled again as documented, a clean one
+    mm, nn, kk = 4096, 4096, 3072
+    a, b, (qa, sa), (qb, sb) = operands(mm, nn, kk)
+    need = m.gemm_workspace_bytes(mm, nn, kk)
+    assert need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    m.set_wait_limit_ns(100)
+    m.gemm(qa, sa, qb, sb, m.FPROP, workspace=ws)
+    st = m.device_status()
+    m.set_wait_limit_ns(0)
+    assert st == m.ERR_TIMEOUT, st
+    ws.zero_()
+    c = m.gemm(qa, sa, qb, sb, m.FPROP, workspace=ws)
+    assert m.device_status() == m.OK
+    sampled_gemm_check(c, rows_of(a, O.ROW), rows_of(b, O.ROW), mm, nn, 9, True,
+                       "split-K after timeout")
+    # the split tiles: rows 2048-4095, columns 3072-4095
+    sampled_gemm_check(c[2048:, 3072:], rows_of(a[2048:], O.ROW), rows_of(b[3072:], O.ROW),
+                       2048, 1024, 10, True, "split-K region after timeout")
     print("TIMEOUT_PATH_OK")
 """)
 
@@ -77,6 +98,8 @@ CHILD = textwrap.dedent(r"""
 def test_pipeline_wait_runs_out_and_context_survives():
     env = dict(os.environ)
     env.pop("MXFP8_WAIT_LIMIT_MS", None)
+    env.pop("MXFP8_GEMM_SPLITK", None)
+    env["MXFP8_GEMM_SPLITK_MIN_STAGES"] = "1"  # lets a shallow GEMM take the split-K path
     r = subprocess.run([sys.executable, "-c", CHILD], cwd=ROOT, env=env, capture_output=True,
                        text=True, timeout=600)
     assert r.returncode == 0 and "TIMEOUT_PATH_OK" in r.stdout, \
