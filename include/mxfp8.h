@@ -292,7 +292,7 @@ int mxfp8_gemm(const void* A_dev, const void* sA_dev, const void* B_dev, const v
  *  - Results: either way they meet the mxfp8_gemm accuracy bound. They are not bit-identical
  *    to mxfp8_gemm's, because the FP32 sums are added in another order.
  * Arguments as for mxfp8_gemm, plus:
- *   workspace_dev    device memory, 16-byte aligned, or NULL; the library allocates nothing.
+ *   workspace_dev    device memory, 32-byte aligned, or NULL; the library allocates nothing.
  *   workspace_bytes  its size. Split-K runs only when it is at least
  *                    mxfp8_gemm_workspace_bytes for the same problem, else the call
  *                    proceeds as mxfp8_gemm.

@@ -291,8 +291,8 @@ def quantize_grouped(src: torch.Tensor, offsets: torch.Tensor, axis: int = ROW, 
 def gemm(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.Tensor, op: int = FPROP,
          out_dtype: int = OUT_BF16, out=None, stream=None, workspace=None) -> torch.Tensor:
     """C[M, N] = deq(A)[M, K] . deq(B)[N, K]^T with swizzled scales (both K-major). With a
-    `workspace` (a zero-filled uint8 CUDA tensor of gemm_workspace_bytes(...) bytes, used by
-    one GEMM at a time) the last wave of tiles may run as split-K pieces (mxfp8_gemm_ws)."""
+    `workspace` (a zero-filled, 32-byte aligned uint8 CUDA tensor of gemm_workspace_bytes(...)
+    bytes, used by one GEMM at a time) the last wave of tiles may run as split-K pieces (mxfp8_gemm_ws)."""
     _require(a, torch.uint8, "A")
     _require(b, torch.uint8, "B")
     m, k = a.shape

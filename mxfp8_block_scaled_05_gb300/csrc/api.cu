@@ -345,7 +345,7 @@ int mxfp8_gemm_ws(const void* A_dev, const void* sA_dev, const void* B_dev, cons
   if (K % 32 || M % 16 || N % 16) return MXFP8_ERR_ALIGNMENT;
   int st = gemm_checks(A_dev, sA_dev, B_dev, sB_dev, C_dev, op, out_dtype);
   if (st != MXFP8_OK) return st;
-  if (workspace_dev && (reinterpret_cast<uintptr_t>(workspace_dev) & 15))
+  if (workspace_dev && (reinterpret_cast<uintptr_t>(workspace_dev) & 31))
     return MXFP8_ERR_ALIGNMENT;
   DeviceState* d = nullptr;
   st = device_state(&d);

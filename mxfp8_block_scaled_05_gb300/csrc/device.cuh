@@ -52,6 +52,24 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   return v;
 }
 
+// 32 bytes to / from global memory in one instruction, cached in L2 only (the address must
+// be 32-byte aligned).
+__device__ __forceinline__ void st_global_cg_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2,
+                                                uint32_t a3, uint32_t a4, uint32_t a5,
+                                                uint32_t a6, uint32_t a7) {
+  asm volatile("st.global.cg.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               ::"l"(p), "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
+
+__device__ __forceinline__ void ld_global_cg_v8(const void* p, uint32_t (&d)[8]) {
+  asm volatile("ld.global.cg.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]), "=r"(d[4]), "=r"(d[5]),
+                 "=r"(d[6]), "=r"(d[7])
+               : "l"(p)
+               : "memory");
+}
+
 __device__ __forceinline__ void red_release_add_gpu(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

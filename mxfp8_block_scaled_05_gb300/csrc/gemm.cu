@@ -1157,16 +1157,17 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
           // arrived, sets the counter back to zero for the next launch (or graph replay),
           // and adds the partials before converting, round by round, storing each round
           // at once (its tile is the CTA's last: holding the accumulator a little longer
-          // delays nothing). Workspace layout, in 16-byte units: [tile slot][piece][CTA
-          // rank][epilogue warp][round][column group][lane], so that a warp's 16-byte
-          // stores cover 512 contiguous bytes and each lane reads back what the same lane
-          // of the same warp wrote.
+          // delays nothing). Workspace layout, in 32-byte units: [tile slot][piece][CTA
+          // rank][epilogue warp][round][column group of 8][lane], so that a warp's 32-byte
+          // stores cover 1 KB contiguous and each lane reads back what the same lane of the
+          // same warp wrote.
           constexpr int S = kSplitK;
           const bool writer = t.piece < S - 1;
           const int ew = warp - 2;
-          auto ws_at = [&](int piece, int r) {
-            return p.ws + ((((static_cast<size_t>(t.slot) * (S - 1) + piece) * 2 + crank) *
-                                kEpiWarps + ew) * 3 + r) * (16 * 32) + lane;
+          auto ws_at = [&](int piece, int r) {  // this lane's first 32-byte unit of round r
+            return reinterpret_cast<uint8_t*>(p.ws) +
+                   (((((static_cast<size_t>(t.slot) * (S - 1) + piece) * 2 + crank) * kEpiWarps +
+                      ew) * 3 + r) * (8 * 32) + lane) * 32;
           };
           uint32_t* const count = p.ws_flags + (static_cast<size_t>(t.slot) * 2 + crank) * kEpiWarps + ew;
           int got = 0;
@@ -1190,25 +1191,26 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
             tmem_ld_32x32b_x32(base + 64 * r + 32, v[1]);
             tmem_ld_wait();
             if (writer) {
-              uint4* w = ws_at(t.piece, r);
+              uint8_t* w = ws_at(t.piece, r);
 #pragma unroll
-              for (int g = 0; g < 16; ++g)
-                __stcg(w + 32 * g, make_uint4(v[g >> 3][4 * (g & 7)], v[g >> 3][4 * (g & 7) + 1],
-                                              v[g >> 3][4 * (g & 7) + 2],
-                                              v[g >> 3][4 * (g & 7) + 3]));
+              for (int g = 0; g < 8; ++g) {
+                const int u = g >> 2, c = 8 * (g & 3);
+                st_global_cg_v8(w + g * (32 * 32), v[u][c], v[u][c + 1], v[u][c + 2], v[u][c + 3],
+                                v[u][c + 4], v[u][c + 5], v[u][c + 6], v[u][c + 7]);
+              }
               continue;
             }
 #pragma unroll
             for (int pp = 0; pp < S - 1; ++pp) {
-              const uint4* w = ws_at(pp, r);
+              const uint8_t* w = ws_at(pp, r);
 #pragma unroll
-              for (int g = 0; g < 16; ++g) {
-                const uint4 x = __ldcg(w + 32 * g);
-                const int u = g >> 3, c = 4 * (g & 7);
-                v[u][c] = __float_as_uint(__uint_as_float(v[u][c]) + __uint_as_float(x.x));
-                v[u][c + 1] = __float_as_uint(__uint_as_float(v[u][c + 1]) + __uint_as_float(x.y));
-                v[u][c + 2] = __float_as_uint(__uint_as_float(v[u][c + 2]) + __uint_as_float(x.z));
-                v[u][c + 3] = __float_as_uint(__uint_as_float(v[u][c + 3]) + __uint_as_float(x.w));
+              for (int g = 0; g < 8; ++g) {
+                uint32_t x[8];
+                ld_global_cg_v8(w + g * (32 * 32), x);
+                const int u = g >> 2, c = 8 * (g & 3);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  v[u][c + j] = __float_as_uint(__uint_as_float(v[u][c + j]) + __uint_as_float(x[j]));
               }
             }
             if (32 * q < t.rows_valid) {
@@ -1742,7 +1744,7 @@ int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
   const int64_t tail = pair_tiles % fit;
   const SplitPlan sp = BN == 384 ? split_plan(pair_tiles, fit, n_kt) : SplitPlan{};
   if (sp.tail > 0 && a.workspace && a.workspace_bytes >= sp.bytes &&
-      (reinterpret_cast<uintptr_t>(a.workspace) & 15) == 0) {
+      (reinterpret_cast<uintptr_t>(a.workspace) & 31) == 0) {
     p.split_from = pair_tiles - tail;
     p.ws = static_cast<uint4*>(a.workspace);
     p.ws_flags = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.workspace) +

@@ -149,12 +149,14 @@ def test_multi_job_argument_errors_need_no_device(lib):
 def test_gemm_workspace_argument_errors_need_no_device(lib):
     p = ctypes.c_void_p(0x10000)
     bad = ctypes.c_void_p(0x10008)        # 8-byte aligned only
+    bad16 = ctypes.c_void_p(0x10010)      # 16-byte aligned, not 32
     gw = lib.mxfp8_gemm_ws
     # the plain GEMM's checks, then the workspace's alignment, all before the device
     assert gw(p, p, p, p, p, 128, 128, 48, 0, 0, p, 1 << 20, None) == m.ERR_ALIGNMENT
     assert gw(p, p, p, p, p, 0, 128, 64, 0, 0, p, 1 << 20, None) == m.ERR_INVALID_ARG
     assert gw(p, None, p, p, p, 128, 128, 64, 0, 0, p, 1 << 20, None) == m.ERR_INVALID_ARG
     assert gw(p, p, p, p, p, 128, 128, 64, 0, 0, bad, 1 << 20, None) == m.ERR_ALIGNMENT
+    assert gw(p, p, p, p, p, 128, 128, 64, 0, 0, bad16, 1 << 20, None) == m.ERR_ALIGNMENT
     # a NULL workspace is the plain GEMM: without a GPU it fails like one
     assert gw(p, p, p, p, p, 128, 128, 64, 0, 0, None, 0, None) in (
         m.ERR_CUDA, m.ERR_UNSUPPORTED_ARCH)

@@ -170,6 +170,6 @@ def test_workspace_sizes_and_alignment(m):
     assert m.gemm_workspace_bytes(-1, 4096, 24576) == 0
     qa = torch.zeros((256, 3072), dtype=torch.uint8, device=DEV)
     sa = torch.zeros(m.scale_bytes(256, 3072), dtype=torch.uint8, device=DEV)
-    ws = torch.zeros(64, dtype=torch.uint8, device=DEV)[1:]  # not 16-byte aligned
+    ws = torch.zeros(64, dtype=torch.uint8, device=DEV)[16:]  # 16-byte aligned, not 32
     with pytest.raises(Exception):
         m.gemm(qa, sa, qa, sa, m.FPROP, workspace=ws)
