@@ -617,7 +617,7 @@ template <int BN, int kMode = kDense>
 struct Duo {
   static constexpr bool kGrouped = kMode != kDense;
   static constexpr bool kWide = BN == 384;
-  static_assert(!kWide || !kGrouped, "384-wide tiles are dense only");
+  static_assert(!kWide || kMode != kGroupWgrad, "384-wide tiles: dense and grouped rows");
   static constexpr int kMmaN = kWide ? 192 : BN;       // N of one MMA instruction
   static constexpr int kBoxRows = kWide ? 96 : BN / 2; // B rows per TMA box
   static constexpr int kAcc = BN == 192 ? 2 : 1;       // accumulator buffers
@@ -667,7 +667,7 @@ struct DuoTile {
   int last_blocks = 0;         // 32-blocks of K in the last stage
   int64_t k_origin = 0;        // TMA K coordinate of the first stage (grouped wgrad)
   int64_t sfa_idx = 0;         // grouped: flat scale tile index of this CTA's A rows, stage 0
-  int64_t sfb_idx0 = 0, sfb_idx1 = 0;  // grouped: the two B scale tiles at stage 0
+  int64_t sfb_idx0 = 0, sfb_idx1 = 0, sfb_idx2 = 0;  // grouped: the B scale tiles, stage 0
   int b_z = 0, c_z = 0;        // expert index for the B (grouped rows) and C (wgrad) maps
   int width = 0;               // output columns of the tile: BN, or BN / 2 for a half tile
   int kb0 = 0;                 // first K stage of a split-K piece (else 0)
@@ -768,6 +768,7 @@ __device__ DuoTile duo_tile_grouped(const Params& p, const DuoSeg* seg, int64_t 
     const int64_t h = t.n0 / 128;
     t.sfb_idx0 = (e * n_rt_b + h) * n_kt;
     t.sfb_idx1 = h + 1 < n_rt_b ? t.sfb_idx0 + n_kt : t.sfb_idx0;
+    t.sfb_idx2 = h + 2 < n_rt_b ? t.sfb_idx0 + 2 * n_kt : t.sfb_idx1;  // 384-wide tiles
     t.b_z = e;
     t.c_z = 0;
   } else {
@@ -975,10 +976,16 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
           if (leader) mbar_arrive_expect_tx(&full[s], 2 * tx);
           tma_load_2d_2sm(smem + D::kOffA + s * D::kABytes, &map_a, kx,
                           static_cast<int32_t>(t.m0), bar);
-          if constexpr (kMode == kGroupRows)
+          if constexpr (kMode == kGroupRows && D::kWide) {
+            // expert b_z's rows 96c.. of each 192-column half of the pair tile
+            uint8_t* bs = smem + D::kOffB + s * D::kBBytes;
+            tma_load_3d_2sm(bs, &map_b, kx, static_cast<int32_t>(t.n0 + 96 * crank), t.b_z, bar);
+            tma_load_3d_2sm(bs + 96 * BK, &map_b, kx,
+                            static_cast<int32_t>(t.n0 + 192 + 96 * crank), t.b_z, bar);
+          } else if constexpr (kMode == kGroupRows) {
             tma_load_3d_2sm(smem + D::kOffB + s * D::kBBytes, &map_b, kx,
                             static_cast<int32_t>(t.n0 + crank * (BN / 2)), t.b_z, bar);
-          else if constexpr (D::kWide) {
+          } else if constexpr (D::kWide) {
             // rows 96c.. of each 192-column half of the pair tile; a half tile (its first
             // MMA alone) loads the first box only
             uint8_t* bs = smem + D::kOffB + s * D::kBBytes;
@@ -1002,6 +1009,9 @@ mxfp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap map_a,
                             static_cast<int32_t>(t.sfb_idx0 + kb), bar);
             tma_load_2d_2sm(smem + D::kOffSfb + s * D::kSfbBytes + 512, &map_sfb, 0,
                             static_cast<int32_t>(t.sfb_idx1 + kb), bar);
+            if constexpr (D::kWide)
+              tma_load_2d_2sm(smem + D::kOffSfb + s * D::kSfbBytes + 1024, &map_sfb, 0,
+                              static_cast<int32_t>(t.sfb_idx2 + kb), bar);
           }
         }
         __syncwarp();
@@ -1819,7 +1829,10 @@ int launch_duo_grouped(const GemmArgs& a, Params p, cudaStream_t stream) {
     if (!make_map(&mb, a.B, 3, p.K, p.N, E, BK, D::kBoxRows)) return MXFP8_ERR_CUDA;
     if (!make_sf_flat_map(&msa, a.sA, seg_tiles * n_kt)) return MXFP8_ERR_CUDA;
     if (!make_sf_flat_map(&msb, a.sB, E * ((p.N + 127) / 128) * n_kt)) return MXFP8_ERR_CUDA;
-    if (!make_out_map(&mc, a.C, T, p.N, 1, fp32, 3)) return MXFP8_ERR_CUDA;
+    // 384-wide tiles store 32-byte boxes through a 2-D map (the wide epilogue's path)
+    if (D::kWide ? !make_out_map(&mc, a.C, T, p.N, 1, fp32, 2, D::kBoxRowBytes)
+                 : !make_out_map(&mc, a.C, T, p.N, 1, fp32, 3))
+      return MXFP8_ERR_CUDA;
     pair_tiles = ((T + 127) / 128 / 2 + E) * p.num_n_tiles;  // bound on pair tiles
   }
   if (pair_tiles > INT32_MAX) return MXFP8_ERR_INVALID_ARG;  // 32-bit item arithmetic
@@ -1836,11 +1849,17 @@ int launch_duo_grouped(const GemmArgs& a, Params p, cudaStream_t stream) {
 }
 
 // Tile width for the grouped 2SM GEMMs: 256 (measured faster than 192 for both modes on
-// the Qwen3-30B-A3B expert layer, wgrad included); MXFP8_GEMM_BN forces a width.
-int duo_grouped_width(int) {
+// the Qwen3-30B-A3B expert layer, wgrad included), or 384 for fprop / dgrad with BF16 output
+// when N is a multiple of 384 of at least 4 tiles. On that layer 384 took gate_up fprop
+// (N = 1536) from 174.5 to 170.2 us, and down dgrad (N = 768, 2 tiles) from 96.7 to 97.5.
+// MXFP8_GEMM_BN forces a width; a forced 384 applies to any multiple of 384.
+int duo_grouped_width(int mode, int64_t N, bool fp32) {
   const char* e = getenv("MXFP8_GEMM_BN");
   const int w = e ? atoi(e) : 0;
-  return (w == 256 || w == 192) ? w : 256;
+  const bool wide_ok = mode == kGroupRows && !fp32 && N % 384 == 0 && wide_tiles_enabled();
+  if (w == 256 || w == 192) return w;
+  if (w == 384) return wide_ok ? 384 : 256;
+  return wide_ok && N >= 4 * 384 ? 384 : 256;
 }
 
 }  // namespace
@@ -1917,7 +1936,7 @@ int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles * p.E;
     p.num_tiles = tiles;
     if (wide && p.num_m_tiles >= 2 && p.E <= kMaxDuoExperts && duo_enabled())
-      return duo_grouped_width(kGroupWgrad) == 256
+      return duo_grouped_width(kGroupWgrad, p.N, p.out_fp32 != 0) == 256
                  ? launch_duo_grouped<256, kGroupWgrad>(a, p, stream)
                  : launch_duo_grouped<192, kGroupWgrad>(a, p, stream);
     if (!make_map(&ma, a.A, 2, a.total_rows, p.M, 1, BK, BM)) return MXFP8_ERR_CUDA;
@@ -1941,9 +1960,11 @@ int launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
   p.num_tiles = tiles;
   if (wide && p.E <= kMaxDuoExperts && duo_enabled())
-    return duo_grouped_width(kGroupRows) == 256
-               ? launch_duo_grouped<256, kGroupRows>(a, p, stream)
-               : launch_duo_grouped<192, kGroupRows>(a, p, stream);
+    switch (duo_grouped_width(kGroupRows, p.N, p.out_fp32 != 0)) {
+      case 384: return launch_duo_grouped<384, kGroupRows>(a, p, stream);
+      case 192: return launch_duo_grouped<192, kGroupRows>(a, p, stream);
+      default: return launch_duo_grouped<256, kGroupRows>(a, p, stream);
+    }
   if (!make_map(&ma, a.A, 2, a.K, a.total_rows, 1, BK, BM)) return MXFP8_ERR_CUDA;
   if (!make_map(&mb, a.B, 3, a.K, a.N, a.num_experts, BK, bn)) return MXFP8_ERR_CUDA;
   if (!make_out_map(&mc, a.C, a.total_rows, p.N, 1, p.out_fp32 != 0, 3)) return MXFP8_ERR_CUDA;

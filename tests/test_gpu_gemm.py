@@ -192,6 +192,37 @@ def test_grouped_fprop_dgrad_wgrad_small(m, counts):
     assert m.device_status() == m.OK
 
 
+@pytest.mark.parametrize("counts", [[64, 0, 160, 32, 0, 300, 96, 7], [0, 0, 40]])
+@pytest.mark.parametrize("kn", [768, 1536])
+def test_grouped_rows_bf16_384_wide_tiles(m, counts, kn):
+    """fprop and dgrad with BF16 output and N a multiple of 384: by default N = 1536 takes
+    the 384-wide grouped tiles (two N = 192 MMAs sharing each expert's A rows) and N = 768
+    the 256-wide ones; forced to 384 (MXFP8_GEMM_BN=384, the variant runs) both do. Empty
+    experts, odd tile counts and padded rows, compared in full with the oracle."""
+    k = n = kn
+    off, x, w, dy = _grouped_case(counts, k, n, seed=10 + len(counts))
+    E = len(counts)
+    offs = torch.from_numpy(off).to(DEV)
+    xb, wb, dyb = bf16_bits(x), bf16_bits(w), bf16_bits(dy)
+    qx, sx = m.quantize_grouped(x.to(DEV), offs, m.ROW)
+    qw, sw = m.quantize_batched(w.to(DEV), m.ROW, m.SWIZZLED)
+    y = m.grouped_gemm(qx, sx, qw, sw, offs, m.FPROP)
+    oq, osx = O.quantize(xb, O.ROW)
+    ow = [O.quantize(wb[e], O.ROW) for e in range(E)]
+    ref, ab = O.grouped_gemm_rows(oq, osx, np.stack([c for c, _ in ow]),
+                                  np.stack([s for _, s in ow]), off)
+    assert_gemm_within(y.double().cpu().numpy(), ref, ab, True, "grouped fprop, 384-wide")
+    qdy, sdy = m.quantize_grouped(dy.to(DEV), offs, m.ROW)
+    qwt, swt = m.quantize_batched(w.to(DEV), m.COL, m.SWIZZLED)
+    dx = m.grouped_gemm(qdy, sdy, qwt, swt, offs, m.DGRAD)
+    od, osd = O.quantize(dyb, O.ROW)
+    owt = [O.quantize(wb[e], O.COL) for e in range(E)]
+    ref, ab = O.grouped_gemm_rows(od, osd, np.stack([c for c, _ in owt]),
+                                  np.stack([s for _, s in owt]), off)
+    assert_gemm_within(dx.double().cpu().numpy(), ref, ab, True, "grouped dgrad, 384-wide")
+    assert m.device_status() == m.OK
+
+
 def test_grouped_bad_offsets_latched(m):
     qa = torch.zeros((128, 64), dtype=torch.uint8, device=DEV)
     sa = torch.zeros(m.grouped_scale_bytes(128, 64, 2, m.ROW), dtype=torch.uint8, device=DEV)

@@ -3,8 +3,8 @@
 The library picks a kernel per problem: the 2SM kernel (tcgen05.mma.cta_group::2) with
 256 x 384 tiles (BF16 output; two N = 192 MMAs sharing A), 256 x 256 tiles (the last,
 partial wave of either as half tiles) or 256 x 192 tiles, or the one-SM kernel (128 x 256
-or 128 x 128 tiles); grouped (MoE) GEMMs run on the 2SM kernel too, or on the one-SM
-kernel. The choice is read from the environment once per process, so each forced
+or 128 x 128 tiles); grouped (MoE) GEMMs run on the 2SM kernel too (256-wide, 192-wide, or
+384-wide for BF16 fprop / dgrad with N a multiple of 384), or on the one-SM kernel. The choice is read from the environment once per process, so each forced
 variant runs the parity tests of test_gpu_gemm.py in a child process. The shapes there
 cover ragged M, N and K, a CTA pair whose second M tile lies past M, and 192-wide tiles
 starting 64 rows into a B scale tile.
@@ -29,7 +29,8 @@ VARIANTS = {
     "1sm": {"MXFP8_GEMM_2SM": "0"},
 }
 SELECT = ("shapes_random_operands or extreme_scales or small_layer or layer_set_full_size "
-          "or grouped_fprop_dgrad_wgrad_small or experts_full_size")
+          "or grouped_fprop_dgrad_wgrad_small or grouped_rows_bf16_384_wide_tiles "
+          "or experts_full_size")
 
 
 @pytest.mark.parametrize("name", sorted(VARIANTS))
