@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <atomic>
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -20,7 +21,9 @@ __device__ int g_device_status;
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
-  bool ready = false;
+  // set up once per device under g_mu; `ready` is published last (release) and read first
+  // (acquire), so a caller that sees it set also sees the fields below
+  std::atomic<bool> ready{false};
   bool supported = false;
   int sms = 0;
   int* status = nullptr;
@@ -36,9 +39,9 @@ int device_state(DeviceState** out) {
   if (cudaGetDevice(&dev) != cudaSuccess) return MXFP8_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MXFP8_ERR_CUDA;
   DeviceState& d = g_dev[dev];
-  if (!d.ready) {
+  if (!d.ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_relaxed)) {
       int major = 0, minor = 0, sms = 0;
       if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
           cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -51,7 +54,7 @@ int device_state(DeviceState** out) {
         if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return MXFP8_ERR_CUDA;
         d.status = static_cast<int*>(p);
       }
-      d.ready = true;
+      d.ready.store(true, std::memory_order_release);
     }
   }
   if (!d.supported) return MXFP8_ERR_UNSUPPORTED_ARCH;

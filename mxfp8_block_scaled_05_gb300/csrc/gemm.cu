@@ -1519,14 +1519,14 @@ int launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, 
            int64_t grid, cudaStream_t stream) {
   using C = Cfg<BN>;
   auto k = mxfp8_gemm_kernel<BN, kMode>;
-  static bool attr_set[64] = {};  // per device
+  static std::atomic<bool> attr_set[64] = {};  // per device; setting it twice is harmless
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MXFP8_ERR_CUDA;
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
       return MXFP8_ERR_CUDA;
-    attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
   }
   if (grid <= 0) return MXFP8_OK;
   cudaLaunchConfig_t cfg = {};
@@ -1611,10 +1611,13 @@ cudaLaunchConfig_t cluster2_config(int64_t grid, int smem, cudaStream_t stream,
 // How many clusters of the 2SM kernel fit on the device at once (cached per device).
 template <int BN, int kMode = kDense>
 int64_t max_duo_clusters() {
-  static int64_t cached[64] = {};
+  static std::atomic<int64_t> cached[64] = {};  // per device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  if (dev >= 0 && dev < 64) {
+    const int64_t c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   auto k = mxfp8_gemm_2sm_kernel<BN, kMode>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Duo<BN, kMode>::kSmemBytes) != cudaSuccess)
@@ -1624,7 +1627,7 @@ int64_t max_duo_clusters() {
   int clusters = 0;
   if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess || clusters <= 0)
     clusters = num_sms() / 2;
-  if (dev >= 0 && dev < 64) cached[dev] = clusters;
+  if (dev >= 0 && dev < 64) cached[dev].store(clusters, std::memory_order_relaxed);
   return clusters;
 }
 
@@ -1771,14 +1774,14 @@ int launch_duo(const GemmArgs& a, Params p, cudaStream_t stream) {
   if constexpr (BN == 384) {
     if (p.ws) {
       k = mxfp8_gemm_2sm_kernel<BN, kDense, true>;
-      static bool attr_set[64] = {};  // per device
+      static std::atomic<bool> attr_set[64] = {};  // per device; setting it twice is harmless
       int dev = 0;
       if (cudaGetDevice(&dev) != cudaSuccess) return MXFP8_ERR_CUDA;
-      if (dev < 64 && !attr_set[dev]) {
+      if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  D::kSmemBytes) != cudaSuccess)
           return MXFP8_ERR_CUDA;
-        attr_set[dev] = true;
+        if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
       }
     }
   }
