@@ -11,7 +11,9 @@ chain below is issued without a synchronization and makes each hazard concrete:
   for the next kernel while it runs).
 Every output is compared with the oracle: the GEMMs on sampled tiles within the accuracy
 gate, the quantized GEMM output on sampled rows bit for bit. The chain runs with the
-default launch mode and again in a child process with MXFP8_PDL=0.
+default launch mode and again in a child process with MXFP8_PDL=0. A last test makes the
+library's first calls from four host threads at once (its per-device setup is then
+contended) and checks every result against the same calls made serially.
 """
 import os
 import subprocess
@@ -76,3 +78,58 @@ def test_chain_reusing_buffers_default_launch():
 
 def test_chain_reusing_buffers_without_programmatic_launch():
     _run("0")
+
+
+THREADS = textwrap.dedent(r"""
+    import threading
+    import torch
+    from tests.oracle_helpers import gpu_ready
+    m = gpu_ready()  # builds and loads the library; no call has touched a device yet
+    dev = "cuda"
+    g = torch.Generator(device=dev).manual_seed(9)
+    shapes = [(512, 1536, 1024), (1024, 768, 2048), (256, 4096, 512), (768, 384, 1536)]
+    ins = [((torch.randn((mm, kk), generator=g, device=dev)).to(torch.bfloat16),
+            (torch.randn((nn, kk), generator=g, device=dev) * 0.02).to(torch.bfloat16))
+           for mm, nn, kk in shapes]
+    torch.cuda.synchronize()
+    outs = [None] * len(shapes)
+    errs = []
+    gate = threading.Barrier(len(shapes))
+
+    def work(i):
+        try:
+            s = torch.cuda.Stream()
+            a, b = ins[i]
+            gate.wait()  # every thread makes its first library call at the same moment
+            with torch.cuda.stream(s):
+                qa, sa = m.quantize(a, m.ROW, stream=s)
+                qb, sb = m.quantize(b, m.ROW, stream=s)
+                outs[i] = m.gemm(qa, sa, qb, sb, m.FPROP, stream=s)
+            s.synchronize()
+        except Exception as e:  # reported below
+            errs.append(repr(e))
+
+    ts = [threading.Thread(target=work, args=(i,)) for i in range(len(shapes))]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errs, errs
+    assert m.device_status() == m.OK
+    for i, (a, b) in enumerate(ins):  # the same calls, one after another
+        qa, sa = m.quantize(a, m.ROW)
+        qb, sb = m.quantize(b, m.ROW)
+        assert torch.equal(outs[i], m.gemm(qa, sa, qb, sb, m.FPROP)), shapes[i]
+    print("THREADS_OK")
+""")
+
+
+def test_first_calls_from_several_host_threads():
+    """The library's per-device setup (device state, kernel attributes, occupancy) runs on
+    the first calls; four host threads make theirs at once, on their own streams, in a fresh
+    process. Every result equals the same calls made one after another, bit for bit."""
+    r = subprocess.run([sys.executable, "-c", THREADS], cwd=ROOT, env=dict(os.environ),
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "THREADS_OK" in r.stdout, \
+        f"{r.stdout[-3000:]}\n{r.stderr[-3000:]}"
+
