@@ -104,7 +104,7 @@ const char* mxfp8_status_string(int status);
  * S_rows x S_cols = rows x cols/32 (ROW) or cols x rows/32 (COL); LINEAR is
  * S_rows * S_cols bytes, SWIZZLED is ceil(S_rows/128) * ceil(S_cols/4) * 512 bytes.
  * Returns 0 for invalid arguments (negative sizes, a blocked dim not a multiple of 32,
- * unknown enums).
+ * unknown enums, a size that does not fit in int64).
  */
 size_t mxfp8_scale_bytes(int64_t rows, int64_t cols, int axis, int scale_layout);
 
@@ -189,7 +189,8 @@ typedef enum {
 
 /*
  * Number of float scales mxfp8_quantize_blockwise writes for a [rows][cols] weight:
- * ceil(rows/128) * ceil(cols/128). Returns 0 for invalid arguments.
+ * ceil(rows/128) * ceil(cols/128). Returns 0 for invalid arguments, including a count
+ * that does not fit in int64.
  */
 size_t mxfp8_blockwise_scale_count(int64_t rows, int64_t cols);
 
@@ -232,7 +233,7 @@ int mxfp8_quantize_batched(const void* src_dev, int64_t batch, int64_t rows, int
  * upper bound that needs no expert counts on the host:
  *   ROW: (ceil(total_rows/128) + num_experts) * ceil(cols/128) * 512
  *   COL: ceil(cols/128) * (ceil(total_rows/128) + num_experts) * 512
- * Returns 0 for invalid arguments.
+ * Returns 0 for invalid arguments, including a size that does not fit in int64.
  */
 size_t mxfp8_grouped_scale_bytes(int64_t total_rows, int64_t cols, int num_experts, int axis);
 

@@ -66,6 +66,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// a * b * c into *out, false if the product leaves int64 (sizes of impossible tensors).
+bool mul3(int64_t a, int64_t b, int64_t c, int64_t* out) {
+  int64_t ab = 0;
+  return !__builtin_mul_overflow(a, b, &ab) && !__builtin_mul_overflow(ab, c, out);
+}
+
 constexpr int64_t kMaxTokenTiles = 65535;  // grid.y limit of the quantizer launch
 // grid.y limit of the self-check's reference kernel (32 tokens per CTA row)
 constexpr int64_t kMaxSelfcheckTokens = int64_t(32) * 65535;
@@ -79,7 +85,7 @@ int num_sms() {
 }
 
 int64_t scale_bytes_host(int64_t rows, int64_t cols, int axis, int layout) {
-  if (rows < 0 || cols < 0) return -1;
+  if (rows < 0 || cols < 0 || rows > INT64_MAX - 127 || cols > INT64_MAX - 127) return -1;
   int64_t s_rows, s_cols;
   if (axis == MXFP8_AXIS_ROW) {
     if (cols % 32) return -1;
@@ -92,10 +98,11 @@ int64_t scale_bytes_host(int64_t rows, int64_t cols, int axis, int layout) {
   } else {
     return -1;
   }
-  if (layout == MXFP8_SCALES_LINEAR) return s_rows * s_cols;
+  int64_t bytes = 0;
+  if (layout == MXFP8_SCALES_LINEAR) return mul3(s_rows, s_cols, 1, &bytes) ? bytes : -1;
   if (layout == MXFP8_SCALES_SWIZZLED) {
     if (s_rows == 0 || s_cols == 0) return 0;
-    return cdiv(s_rows, 128) * cdiv(s_cols, 4) * 512;
+    return mul3(cdiv(s_rows, 128), cdiv(s_cols, 4), 512, &bytes) ? bytes : -1;
   }
   return -1;
 }
@@ -128,12 +135,15 @@ size_t mxfp8_scale_bytes(int64_t rows, int64_t cols, int axis, int scale_layout)
 
 size_t mxfp8_grouped_scale_bytes(int64_t total_rows, int64_t cols, int num_experts, int axis) {
   if (total_rows < 0 || cols <= 0 || num_experts <= 0 || total_rows % 32) return 0;
+  if (total_rows > INT64_MAX - 127) return 0;
+  int64_t bytes = 0;
+  const int64_t tiles = cdiv(total_rows, 128) + num_experts;  // bound on sum of ceil(count / 128)
   if (axis == MXFP8_AXIS_ROW) {
     if (cols % 32) return 0;
-    return static_cast<size_t>((cdiv(total_rows, 128) + num_experts) * cdiv(cols / 32, 4) * 512);
+    return mul3(tiles, cdiv(cols / 32, 4), 512, &bytes) ? static_cast<size_t>(bytes) : 0;
   }
   if (axis == MXFP8_AXIS_COL)
-    return static_cast<size_t>(cdiv(cols, 128) * (cdiv(total_rows, 128) + num_experts) * 512);
+    return mul3(cdiv(cols, 128), tiles, 512, &bytes) ? static_cast<size_t>(bytes) : 0;
   return 0;
 }
 
@@ -153,6 +163,8 @@ static int quantize_common(const void* src, int64_t batch, int64_t rows, int64_t
   if (row && cols % 32) return MXFP8_ERR_ALIGNMENT;
   if (col && (rows % 32 || cols % 8)) return MXFP8_ERR_ALIGNMENT;
   if (batch == 0 || rows == 0 || cols == 0) return MXFP8_OK;
+  int64_t elems = 0;  // BF16 input bytes = 2 * elems; the kernels index in int64
+  if (!mul3(batch, rows, cols, &elems) || elems > INT64_MAX / 2) return MXFP8_ERR_INVALID_ARG;
   if (!src || !out || !scales) return MXFP8_ERR_INVALID_ARG;
   if (axis == kAxisBoth && (!out2 || !scales2)) return MXFP8_ERR_INVALID_ARG;
   if (!aligned16(src) || !aligned16(out) || (out2 && !aligned16(out2)))
@@ -259,7 +271,9 @@ int mxfp8_quantize_dual_multi(const mxfp8_dual_job* jobs, int num_jobs, int scal
 
 size_t mxfp8_blockwise_scale_count(int64_t rows, int64_t cols) {
   if (rows < 0 || cols < 0 || cols % 8) return 0;
-  return static_cast<size_t>(cdiv(rows, 128) * cdiv(cols, 128));
+  if (rows > INT64_MAX - 127 || cols > INT64_MAX - 127) return 0;
+  int64_t n = 0;
+  return mul3(cdiv(rows, 128), cdiv(cols, 128), 1, &n) ? static_cast<size_t>(n) : 0;
 }
 
 int mxfp8_quantize_blockwise(const void* src_dev, int64_t rows, int64_t cols, void* out_dev,
@@ -374,8 +388,10 @@ int mxfp8_grouped_gemm(const void* A_dev, const void* sA_dev, const void* B_dev,
   if (total_rows == 0) {
     // no tokens: fprop/dgrad have no rows to write; every expert's dW is zero
     if (op != MXFP8_OP_WGRAD) return MXFP8_OK;
-    const size_t elem = out_dtype == MXFP8_OUT_FP32 ? 4 : 2;
-    return cudaMemsetAsync(C_dev, 0, static_cast<size_t>(num_experts) * N * K * elem,
+    const int64_t elem = out_dtype == MXFP8_OUT_FP32 ? 4 : 2;
+    int64_t nk = 0, bytes = 0;
+    if (!mul3(N, K, elem, &nk) || !mul3(nk, num_experts, 1, &bytes)) return MXFP8_ERR_INVALID_ARG;
+    return cudaMemsetAsync(C_dev, 0, static_cast<size_t>(bytes),
                            static_cast<cudaStream_t>(stream)) == cudaSuccess ? MXFP8_OK
                                                                              : MXFP8_ERR_CUDA;
   }

@@ -106,6 +106,27 @@ def test_argument_errors_need_no_device(lib):
     assert qg(p, 65535 * 128, 32, m.ROW, p, 4, p, p, None) == m.ERR_INVALID_ARG  # + E tiles
 
 
+def test_sizes_past_int64_are_refused(lib):
+    """Size helpers and the quantizer's checks compute in int64 with overflow checks: a
+    tensor whose byte size cannot be represented gets 0 (size helpers) or
+    MXFP8_ERR_INVALID_ARG (calls), never a wrapped-around size."""
+    big = 2 ** 62
+    assert lib.mxfp8_scale_bytes(big, 2 ** 40, m.ROW, m.LINEAR) == 0
+    assert lib.mxfp8_scale_bytes(big, 2 ** 40, m.ROW, m.SWIZZLED) == 0
+    assert lib.mxfp8_scale_bytes(2 ** 63 - 1, 32, m.ROW, m.SWIZZLED) == 0   # ceil would wrap
+    assert lib.mxfp8_scale_bytes(2 ** 40, 2 ** 35, m.COL, m.SWIZZLED) == 0   # 2^70 bytes
+    assert lib.mxfp8_scale_bytes(2 ** 40, 2 ** 20, m.COL, m.SWIZZLED) == \
+        (2 ** 20 // 128) * (2 ** 35 // 4) * 512                          # 2^55: representable
+    assert lib.mxfp8_grouped_scale_bytes(big, 2 ** 40, 128, m.ROW) == 0
+    assert lib.mxfp8_grouped_scale_bytes(2 ** 63 - 31, 64, 128, m.COL) == 0
+    assert lib.mxfp8_blockwise_scale_count(big, big) == 0
+    assert lib.mxfp8_blockwise_scale_count(2 ** 63 - 1, 8) == 0
+    p = ctypes.c_void_p(0x10000)  # never dereferenced
+    # 65535 x 8388480 x 2^40 elements: every per-dim check passes, the product does not fit
+    assert lib.mxfp8_quantize_batched(p, 65535, 65535 * 128, 2 ** 40, m.ROW, p, p, m.SWIZZLED,
+                                      None) == m.ERR_INVALID_ARG
+
+
 def test_blockwise_sizes_and_argument_errors_need_no_device(lib):
     P = ctypes.c_void_p(0x10000)
     assert lib.mxfp8_blockwise_scale_count(256, 384) == 2 * 3
