@@ -409,7 +409,9 @@ int mxfp8_set_wait_limit_ns(uint64_t ns);
  * Synchronizes `stream`, then returns and clears the current device's status word:
  * MXFP8_OK, or the first device-side error latched since the last call
  * (MXFP8_ERR_BAD_OFFSETS, MXFP8_ERR_TIMEOUT), or MXFP8_ERR_CUDA if the synchronization
- * itself failed.
+ * itself failed. The word is read and cleared in one atomic exchange, enqueued on
+ * `stream` after its earlier work. An error that a kernel on another stream latches
+ * concurrently is reported by this call or by the next one; it is never cleared unread.
  */
 int mxfp8_get_device_status(void* stream);
 

@@ -18,6 +18,18 @@ namespace {
 // First error a kernel detected on this device since the host last read it.
 __device__ int g_device_status;
 
+// mxfp8_get_device_status takes the word with one atomic exchange on the device, so an
+// error latched by a kernel on another stream is either taken by this read or left for the
+// next one, never cleared unread. Each call gets its own slot for the taken value, so that
+// calls from several host threads do not overwrite each other's result.
+constexpr unsigned kStatusSlots = 64;
+__device__ int g_status_taken[kStatusSlots];
+std::atomic<unsigned> g_status_slot{0};
+
+__global__ void take_status_kernel(unsigned slot) {
+  g_status_taken[slot] = atomicExch(&g_device_status, 0);
+}
+
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
@@ -467,12 +479,15 @@ int mxfp8_get_device_status(void* stream) {
   DeviceState* d = nullptr;
   const int st = device_state(&d);
   if (st != MXFP8_OK) return st;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return MXFP8_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const unsigned slot = g_status_slot.fetch_add(1, std::memory_order_relaxed) % kStatusSlots;
+  take_status_kernel<<<1, 1, 0, s>>>(slot);  // after the stream's earlier work
+  if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_CUDA;
   int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return MXFP8_ERR_CUDA;
-  const int zero = 0;
-  if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return MXFP8_ERR_CUDA;
+  if (cudaMemcpyFromSymbolAsync(&v, g_status_taken, sizeof(int), slot * sizeof(int),
+                                cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MXFP8_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MXFP8_ERR_CUDA;
   return v;
 }
 

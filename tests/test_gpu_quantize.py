@@ -153,6 +153,41 @@ def test_grouped_bad_offsets_latched(m):
     assert m.device_status() == m.OK
 
 
+def test_status_latched_on_another_stream_is_read_once(m):
+    """An error latched by a kernel on one stream is returned by a status read on another
+    stream once that kernel has finished, then cleared. The read takes the word with one
+    atomic exchange, so every host thread's read gets a status of its own: four threads
+    reading at once after one latch see the error exactly once."""
+    import threading
+    x = torch.zeros((128, 64), dtype=torch.bfloat16, device=DEV)
+    offs = torch.tensor([0, 40, 128], dtype=torch.int32, device=DEV)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        m.quantize_grouped(x, offs, m.ROW, stream=side)
+    side.synchronize()
+    assert m.device_status() == m.ERR_BAD_OFFSETS     # read on the default stream
+    assert m.device_status() == m.OK
+    for _ in range(3):
+        with torch.cuda.stream(side):
+            m.quantize_grouped(x, offs, m.ROW, stream=side)
+        side.synchronize()
+        seen = []
+        gate = threading.Barrier(4)
+
+        def read():
+            s = torch.cuda.Stream()
+            gate.wait()
+            seen.append(m.device_status(stream=s))
+
+        ts = [threading.Thread(target=read) for _ in range(4)]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+        assert sorted(seen) == [m.OK] * 3 + [m.ERR_BAD_OFFSETS], seen
+
+
 def _sample_rows_check(m, x_dev, axis, n_samples, seed):
     """Full-size quantize on the GPU; the oracle recomputes sampled rows (ROW) or sampled
     columns (COL) of the input and both codes and swizzled scale bytes are compared."""
