@@ -21,7 +21,8 @@ __device__ int g_device_status;
 // mxfp8_get_device_status takes the word with one atomic exchange on the device, so an
 // error latched by a kernel on another stream is either taken by this read or left for the
 // next one, never cleared unread. Each call gets its own slot for the taken value, so that
-// calls from several host threads do not overwrite each other's result.
+// calls from several host threads do not overwrite each other's result. Slots are handed out
+// round robin, so only more than 64 reads in flight at once could share one.
 constexpr unsigned kStatusSlots = 64;
 __device__ int g_status_taken[kStatusSlots];
 std::atomic<unsigned> g_status_slot{0};
