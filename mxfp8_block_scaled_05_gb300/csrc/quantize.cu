@@ -49,33 +49,58 @@ constexpr int kMaxExperts = 1024; // grouped calls: experts scanned in shared me
 struct Segments {
   int32_t off[kMaxExperts + 1];
   int32_t tile_base[kMaxExperts + 1];  // prefix sum of ceil(count_e / 128)
+  int32_t warp_sum[kThreads / 32];     // scratch of the block-wide scan
   int ok;
 };
 
+// The prefix sums come from a block-wide scan: each thread sums the tile counts of
+// kMaxExperts / kThreads consecutive experts, a warp shuffle scan and the warps' totals
+// place each thread's run, and the thread writes its experts' bases. A grouped launch runs
+// this in every CTA, so a serial loop over the experts by one thread would cost each CTA
+// microseconds.
 __device__ void load_segments(Segments& s, const int32_t* __restrict__ offsets, int E,
                               int64_t total_rows, int* status) {
-  const int t = threadIdx.x;
+  constexpr int kPer = kMaxExperts / kThreads;  // experts per thread
+  static_assert(kPer * kThreads == kMaxExperts, "experts must split evenly over the CTA");
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   if (t == 0) s.ok = 1;
   __syncthreads();
-  for (int i = t; i <= E; i += blockDim.x) s.off[i] = offsets[i];
+  for (int i = t; i <= E; i += kThreads) s.off[i] = offsets[i];
   __syncthreads();
-  for (int i = t; i < E; i += blockDim.x) {
-    const int32_t lo = s.off[i], hi = s.off[i + 1];
-    if (hi < lo || (lo & 31) || (hi & 31)) s.ok = 0;
+  int32_t tiles[kPer];
+  int32_t mine = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int e = t * kPer + j;
+    int32_t n = 0;
+    if (e < E) {
+      const int32_t lo = s.off[e], hi = s.off[e + 1];
+      if (hi < lo || (lo & 31) || (hi & 31)) s.ok = 0;
+      n = hi > lo ? (hi - lo + 127) / 128 : 0;
+    }
+    tiles[j] = n;
+    mine += n;
   }
   if (t == 0 && (s.off[0] != 0 || static_cast<int64_t>(s.off[E]) != total_rows)) s.ok = 0;
-  __syncthreads();
-  if (t == 0) {
-    int32_t acc = 0;
-    for (int e = 0; e < E; ++e) {
-      s.tile_base[e] = acc;
-      const int32_t cnt = s.off[e + 1] - s.off[e];
-      acc += cnt > 0 ? (cnt + 127) / 128 : 0;
-    }
-    s.tile_base[E] = acc;
-    if (!s.ok) latch_error(status, MXFP8_ERR_BAD_OFFSETS);
+  int32_t incl = mine;  // inclusive scan within the warp
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += v;
   }
+  if (lane == 31) s.warp_sum[warp] = incl;
   __syncthreads();
+  int32_t base = incl - mine;
+  for (int w = 0; w < warp; ++w) base += s.warp_sum[w];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int e = t * kPer + j;
+    if (e < E) s.tile_base[e] = base;
+    base += tiles[j];
+  }
+  if (t == kThreads - 1) s.tile_base[E] = base;  // the total: threads past E add nothing
+  __syncthreads();
+  if (t == 0 && !s.ok) latch_error(status, MXFP8_ERR_BAD_OFFSETS);
 }
 
 // Finds the expert owning global tile-row `t` (tile_base[e] <= t < tile_base[e+1]).
