@@ -9,7 +9,7 @@ import torch
 import oracle.mxfp8_oracle as O
 from mxfp8_block_scaled_05_gb300 import workloads as W
 from tests.oracle_helpers import (assert_gemm_within, bf16_bits, bits_to_bf16, gpu_ready,
-                                  rows_of, sampled_gemm_check)
+                                  rows_of, sampled_gemm_check, u8)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -186,6 +186,57 @@ def test_grouped_fprop_dgrad_wgrad_small(m, counts):
     ob, osb = O.quantize(xb, O.COL)
     ref, ab = O.grouped_gemm_wgrad(oa, osa, ob, osb, off)
     assert_gemm_within(dw.double().cpu().numpy(), ref, ab, False, "grouped wgrad")
+    for e, c in enumerate(counts):
+        if c == 0:
+            assert torch.all(dw[e] == 0)
+    assert m.device_status() == m.OK
+
+
+@pytest.mark.parametrize("E", [256, 1000])
+def test_grouped_many_experts(m, E):
+    """Expert counts at the limits of the per-CTA segment tables.
+    - E = 256: the most that the 2SM grouped GEMM takes.
+    - E = 1000: the one-SM grouped GEMM. In the quantizer's segment scan, every thread of
+      the CTA holds experts, four each.
+
+    Segments of 0 to 160 rows, about a fifth of them empty, go through the grouped
+    quantizer (row-wise, column-wise and dual) and through fprop and wgrad (FP32 out).
+    Everything is compared in full with the oracle."""
+    rng = np.random.default_rng(E)
+    counts = [int(c) for c in rng.choice([0, 8, 32, 40, 96, 128, 160], size=E,
+                                         p=[0.2, 0.1, 0.2, 0.1, 0.2, 0.1, 0.1])]
+    k, n = 128, 256
+    off, x, w, dy = _grouped_case(counts, k, n, seed=E)
+    offs = torch.from_numpy(off).to(DEV)
+    xb, wb, dyb = bf16_bits(x), bf16_bits(w), bf16_bits(dy)
+    # the quantizer: each axis, and both from one read
+    qx, sx = m.quantize_grouped(x.to(DEV), offs, m.ROW)
+    qxt, sxt = m.quantize_grouped(x.to(DEV), offs, m.COL)
+    rq, rs = O.quantize(xb, O.ROW)
+    cq, cs = O.quantize(xb, O.COL)
+    np.testing.assert_array_equal(u8(qx), rq)
+    want_r = O.swizzle_grouped_rows(rs, off)
+    np.testing.assert_array_equal(u8(sx)[:want_r.size], want_r)
+    np.testing.assert_array_equal(u8(qxt), cq)
+    want_c = O.swizzle_grouped_cols(cs, off)
+    np.testing.assert_array_equal(u8(sxt)[:want_c.size], want_c)
+    d = m.quantize_grouped_dual(x.to(DEV), offs)
+    assert torch.equal(d[0], qx) and torch.equal(d[2], qxt)
+    assert torch.equal(d[1][:want_r.size], sx[:want_r.size])
+    assert torch.equal(d[3][:want_c.size], sxt[:want_c.size])
+    # fprop: Y = X_e W_e^T
+    qw, sw = m.quantize_batched(w.to(DEV), m.ROW, m.SWIZZLED)
+    y = m.grouped_gemm(qx, sx, qw, sw, offs, m.FPROP, m.OUT_FP32)
+    ow = [O.quantize(wb[e], O.ROW) for e in range(E)]
+    ref, ab = O.grouped_gemm_rows(rq, rs, np.stack([c for c, _ in ow]),
+                                  np.stack([s_ for _, s_ in ow]), off)
+    assert_gemm_within(y.double().cpu().numpy(), ref, ab, False, f"grouped fprop, E={E}")
+    # wgrad: dW_e = dY_e^T X_e over the expert's tokens
+    qdyt, sdyt = m.quantize_grouped(dy.to(DEV), offs, m.COL)
+    dw = m.grouped_gemm(qdyt, sdyt, qxt, sxt, offs, m.WGRAD, m.OUT_FP32)
+    oa, osa = O.quantize(dyb, O.COL)
+    ref, ab = O.grouped_gemm_wgrad(oa, osa, cq, cs, off)
+    assert_gemm_within(dw.double().cpu().numpy(), ref, ab, False, f"grouped wgrad, E={E}")
     for e, c in enumerate(counts):
         if c == 0:
             assert torch.all(dw[e] == 0)
