@@ -331,6 +331,9 @@ size_t mxfp8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int op, int o
  *                      grouped COL scales); C [E][N][K], C[e] = A[:, seg e] .
  *                      B[:, seg e]^T; an expert with no tokens gets C[e] = 0.
  * Requires K % 32 == 0, N % 16 == 0, total_rows % 32 == 0, and for WGRAD K % 16 == 0.
+ * total_rows == 0 (no routed tokens) reads no operand and runs no kernel: A, B and their
+ * scales may then be NULL, the offsets are not read, FPROP / DGRAD return MXFP8_OK without
+ * writing, and WGRAD zero-fills C (which must then be valid and 16-byte aligned).
  */
 int mxfp8_grouped_gemm(const void* A_dev, const void* sA_dev, const void* B_dev,
                        const void* sB_dev, void* C_dev, const int32_t* expert_offsets_dev,

@@ -393,21 +393,29 @@ int mxfp8_grouped_gemm(const void* A_dev, const void* sA_dev, const void* B_dev,
   if (total_rows < 0 || N <= 0 || K <= 0) return MXFP8_ERR_INVALID_ARG;
   if (total_rows > 0x7FFFFF00 || N > 0x7FFFFF00 || K > 0x7FFFFF00) return MXFP8_ERR_INVALID_ARG;
   if (total_rows % 32 || K % 32 || N % 16) return MXFP8_ERR_ALIGNMENT;
+  if (op < MXFP8_OP_FPROP || op > MXFP8_OP_WGRAD) return MXFP8_ERR_INVALID_ARG;
+  if (out_dtype != MXFP8_OUT_BF16 && out_dtype != MXFP8_OUT_FP32) return MXFP8_ERR_INVALID_ARG;
+  if (total_rows == 0) {
+    // No tokens: no operand is read, so A, B and their scales may be empty (NULL); fprop
+    // and dgrad have no rows to write; every expert's dW is zero.
+    if (op != MXFP8_OP_WGRAD) return MXFP8_OK;
+    if (!C_dev) return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(C_dev)) return MXFP8_ERR_ALIGNMENT;
+    const int64_t elem = out_dtype == MXFP8_OUT_FP32 ? 4 : 2;
+    int64_t nk = 0, bytes = 0;
+    if (!mul3(N, K, elem, &nk) || !mul3(nk, num_experts, 1, &bytes)) return MXFP8_ERR_INVALID_ARG;
+    DeviceState* d = nullptr;
+    const int st = device_state(&d);
+    if (st != MXFP8_OK) return st;
+    return cudaMemsetAsync(C_dev, 0, static_cast<size_t>(bytes),
+                           static_cast<cudaStream_t>(stream)) == cudaSuccess ? MXFP8_OK
+                                                                             : MXFP8_ERR_CUDA;
+  }
   int st = gemm_checks(A_dev, sA_dev, B_dev, sB_dev, C_dev, op, out_dtype);
   if (st != MXFP8_OK) return st;
   DeviceState* d = nullptr;
   st = device_state(&d);
   if (st != MXFP8_OK) return st;
-  if (total_rows == 0) {
-    // no tokens: fprop/dgrad have no rows to write; every expert's dW is zero
-    if (op != MXFP8_OP_WGRAD) return MXFP8_OK;
-    const int64_t elem = out_dtype == MXFP8_OUT_FP32 ? 4 : 2;
-    int64_t nk = 0, bytes = 0;
-    if (!mul3(N, K, elem, &nk) || !mul3(nk, num_experts, 1, &bytes)) return MXFP8_ERR_INVALID_ARG;
-    return cudaMemsetAsync(C_dev, 0, static_cast<size_t>(bytes),
-                           static_cast<cudaStream_t>(stream)) == cudaSuccess ? MXFP8_OK
-                                                                             : MXFP8_ERR_CUDA;
-  }
   GemmArgs a{A_dev, sA_dev, B_dev, sB_dev, C_dev, 0, N, K, op, out_dtype,
              expert_offsets_dev, num_experts, total_rows, d->status};
   return launch_grouped_gemm(a, static_cast<cudaStream_t>(stream));

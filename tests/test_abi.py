@@ -92,6 +92,14 @@ def test_argument_errors_need_no_device(lib):
     assert gg(p, p, p, p, p, p, 2000, 64, 128, 64, 0, 0, None) == m.ERR_INVALID_ARG
     assert gg(p, p, p, p, p, None, 4, 64, 128, 64, 0, 0, None) == m.ERR_INVALID_ARG
     assert gg(p, p, p, p, p, p, 4, 48, 128, 64, 0, 0, None) == m.ERR_ALIGNMENT
+    # no routed tokens: nothing is read, so empty (NULL) operands are fine; fprop and dgrad
+    # are no-ops, wgrad needs its output (zero-filled on the device)
+    assert gg(None, None, None, None, None, p, 4, 0, 128, 64, m.FPROP, 0, None) == m.OK
+    assert gg(None, None, None, None, None, p, 4, 0, 128, 64, m.DGRAD, 1, None) == m.OK
+    assert gg(None, None, None, None, None, p, 4, 0, 128, 64, m.WGRAD, 0, None) == \
+        m.ERR_INVALID_ARG
+    assert gg(None, None, None, None, bad, p, 4, 0, 128, 64, m.WGRAD, 0, None) == m.ERR_ALIGNMENT
+    assert gg(None, None, None, None, None, p, 4, 0, 128, 64, 3, 0, None) == m.ERR_INVALID_ARG
     assert lib.mxfp8_quantize_rule(p, 64, 64, m.ROW, p, p, m.SWIZZLED, 7, None) == m.ERR_INVALID_ARG
     assert lib.mxfp8_quantize_rule(p, 64, 48, m.ROW, p, p, m.SWIZZLED, 1, None) == m.ERR_ALIGNMENT
     qg = lib.mxfp8_quantize_grouped

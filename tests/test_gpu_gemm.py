@@ -274,6 +274,31 @@ def test_grouped_rows_bf16_384_wide_tiles(m, counts, kn):
     assert m.device_status() == m.OK
 
 
+def test_grouped_no_tokens(m):
+    """An MoE batch that routes no token to any expert (total_rows = 0). The operands are
+    empty tensors. The quantizer writes nothing, fprop and dgrad have no rows, and every
+    expert's dW is zero, written over whatever the output held."""
+    E, k, n = 4, 256, 384
+    offs = torch.zeros(E + 1, dtype=torch.int32, device=DEV)
+    x = torch.empty((0, k), dtype=torch.bfloat16, device=DEV)
+    dy = torch.empty((0, n), dtype=torch.bfloat16, device=DEV)
+    w = (torch.randn((E, n, k), device=DEV) * 0.02).to(torch.bfloat16)
+    qx, sx = m.quantize_grouped(x, offs, m.ROW)
+    qw, sw = m.quantize_batched(w, m.ROW, m.SWIZZLED)
+    y = m.grouped_gemm(qx, sx, qw, sw, offs, m.FPROP)
+    assert y.shape == (0, n)
+    qdy, sdy = m.quantize_grouped(dy, offs, m.ROW)
+    qwt, swt = m.quantize_batched(w, m.COL, m.SWIZZLED)
+    assert m.grouped_gemm(qdy, sdy, qwt, swt, offs, m.DGRAD).shape == (0, k)
+    qdyt, sdyt = m.quantize_grouped(dy, offs, m.COL)
+    qxt, sxt = m.quantize_grouped(x, offs, m.COL)
+    for out_dtype, dt in ((m.OUT_BF16, torch.bfloat16), (m.OUT_FP32, torch.float32)):
+        dw = torch.full((E, n, k), 7.0, dtype=dt, device=DEV)
+        m.grouped_gemm(qdyt, sdyt, qxt, sxt, offs, m.WGRAD, out_dtype, out=dw)
+        assert torch.all(dw == 0)
+    assert m.device_status() == m.OK
+
+
 def test_grouped_bad_offsets_latched(m):
     qa = torch.zeros((128, 64), dtype=torch.uint8, device=DEV)
     sa = torch.zeros(m.grouped_scale_bytes(128, 64, 2, m.ROW), dtype=torch.uint8, device=DEV)
