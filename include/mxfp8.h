@@ -275,8 +275,11 @@ int mxfp8_quantize_grouped_dual(const void* src_dev, int64_t total_rows, int64_t
  *   C_dev          [M][N], BF16 or FP32 (out_dtype), fully overwritten.
  * Both operands are K-major ("TN"); `op` names which quantized copies are passed
  * (see mxfp8_op) and does not change the arithmetic. Requires K % 32 == 0,
- * M % 16 == 0 and N % 16 == 0 (M, N, K > 0). Accuracy: |C - C_exact| <=
- * 2^-9 * sum_k |a_k b_k| per element before the output rounding.
+ * M % 16 == 0 and N % 16 == 0. Accuracy: |C - C_exact| <= 2^-9 * sum_k |a_k b_k| per
+ * element before the output rounding.
+ * Empty sizes read no operand, so A, B and their scales may then be NULL:
+ *  - M == 0 or N == 0 writes nothing and returns MXFP8_OK.
+ *  - K == 0 zero-fills C, the empty sum; C must then be valid and 16-byte aligned.
  */
 int mxfp8_gemm(const void* A_dev, const void* sA_dev, const void* B_dev, const void* sB_dev,
                void* C_dev, int64_t M, int64_t N, int64_t K, int op, int out_dtype,
@@ -331,9 +334,12 @@ size_t mxfp8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int op, int o
  *                      grouped COL scales); C [E][N][K], C[e] = A[:, seg e] .
  *                      B[:, seg e]^T; an expert with no tokens gets C[e] = 0.
  * Requires K % 32 == 0, N % 16 == 0, total_rows % 32 == 0, and for WGRAD K % 16 == 0.
- * total_rows == 0 (no routed tokens) reads no operand and runs no kernel: A, B and their
- * scales may then be NULL, the offsets are not read, FPROP / DGRAD return MXFP8_OK without
- * writing, and WGRAD zero-fills C (which must then be valid and 16-byte aligned).
+ * Empty sizes read no operand and run no kernel: A, B and their scales may then be NULL,
+ * and the offsets are not read.
+ *  - An empty output is a no-op that returns MXFP8_OK: N == 0, or K == 0 for WGRAD, or
+ *    total_rows == 0 (no routed tokens) for FPROP / DGRAD.
+ *  - A reduction over nothing zero-fills C, which must then be valid and 16-byte aligned:
+ *    WGRAD with total_rows == 0, or FPROP / DGRAD with K == 0.
  */
 int mxfp8_grouped_gemm(const void* A_dev, const void* sA_dev, const void* B_dev,
                        const void* sB_dev, void* C_dev, const int32_t* expert_offsets_dev,

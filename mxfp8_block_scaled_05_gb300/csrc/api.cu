@@ -340,6 +340,22 @@ int mxfp8_quantize_grouped_dual(const void* src_dev, int64_t total_rows, int64_t
                          num_experts, stream);
 }
 
+// C = 0 for a reduction over nothing (K = 0, or no tokens for a grouped wgrad): `elems`
+// output elements zero-filled on the stream; C must be valid and 16-byte aligned.
+static int zero_fill_output(void* C, int64_t elems, int out_dtype, void* stream) {
+  if (!C) return MXFP8_ERR_INVALID_ARG;
+  if (!aligned16(C)) return MXFP8_ERR_ALIGNMENT;
+  int64_t bytes = 0;
+  if (!mul3(elems, out_dtype == MXFP8_OUT_FP32 ? 4 : 2, 1, &bytes)) return MXFP8_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  const int st = device_state(&d);
+  if (st != MXFP8_OK) return st;
+  return cudaMemsetAsync(C, 0, static_cast<size_t>(bytes), static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? MXFP8_OK
+             : MXFP8_ERR_CUDA;
+}
+
 static int gemm_checks(const void* A, const void* sA, const void* B, const void* sB, void* C,
                        int op, int out_dtype) {
   if (!A || !sA || !B || !sB || !C) return MXFP8_ERR_INVALID_ARG;
@@ -370,9 +386,13 @@ size_t mxfp8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int op, int o
 int mxfp8_gemm_ws(const void* A_dev, const void* sA_dev, const void* B_dev, const void* sB_dev,
                   void* C_dev, int64_t M, int64_t N, int64_t K, int op, int out_dtype,
                   void* workspace_dev, size_t workspace_bytes, void* stream) {
-  if (M <= 0 || N <= 0 || K <= 0) return MXFP8_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return MXFP8_ERR_INVALID_ARG;
   if (M > 0x7FFFFF00 || N > 0x7FFFFF00 || K > 0x7FFFFF00) return MXFP8_ERR_INVALID_ARG;
   if (K % 32 || M % 16 || N % 16) return MXFP8_ERR_ALIGNMENT;
+  if (op < MXFP8_OP_FPROP || op > MXFP8_OP_WGRAD) return MXFP8_ERR_INVALID_ARG;
+  if (out_dtype != MXFP8_OUT_BF16 && out_dtype != MXFP8_OUT_FP32) return MXFP8_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return MXFP8_OK;  // an empty output: nothing to read or write
+  if (K == 0) return zero_fill_output(C_dev, M * N, out_dtype, stream);  // the empty sum
   int st = gemm_checks(A_dev, sA_dev, B_dev, sB_dev, C_dev, op, out_dtype);
   if (st != MXFP8_OK) return st;
   if (workspace_dev && (reinterpret_cast<uintptr_t>(workspace_dev) & 31))
@@ -390,27 +410,23 @@ int mxfp8_grouped_gemm(const void* A_dev, const void* sA_dev, const void* B_dev,
                        int num_experts, int64_t total_rows, int64_t N, int64_t K, int op,
                        int out_dtype, void* stream) {
   if (num_experts <= 0 || num_experts > 1024 || !expert_offsets_dev) return MXFP8_ERR_INVALID_ARG;
-  if (total_rows < 0 || N <= 0 || K <= 0) return MXFP8_ERR_INVALID_ARG;
+  if (total_rows < 0 || N < 0 || K < 0) return MXFP8_ERR_INVALID_ARG;
   if (total_rows > 0x7FFFFF00 || N > 0x7FFFFF00 || K > 0x7FFFFF00) return MXFP8_ERR_INVALID_ARG;
   if (total_rows % 32 || K % 32 || N % 16) return MXFP8_ERR_ALIGNMENT;
   if (op < MXFP8_OP_FPROP || op > MXFP8_OP_WGRAD) return MXFP8_ERR_INVALID_ARG;
   if (out_dtype != MXFP8_OUT_BF16 && out_dtype != MXFP8_OUT_FP32) return MXFP8_ERR_INVALID_ARG;
-  if (total_rows == 0) {
-    // No tokens: no operand is read, so A, B and their scales may be empty (NULL); fprop
-    // and dgrad have no rows to write; every expert's dW is zero.
-    if (op != MXFP8_OP_WGRAD) return MXFP8_OK;
-    if (!C_dev) return MXFP8_ERR_INVALID_ARG;
-    if (!aligned16(C_dev)) return MXFP8_ERR_ALIGNMENT;
-    const int64_t elem = out_dtype == MXFP8_OUT_FP32 ? 4 : 2;
-    int64_t nk = 0, bytes = 0;
-    if (!mul3(N, K, elem, &nk) || !mul3(nk, num_experts, 1, &bytes)) return MXFP8_ERR_INVALID_ARG;
-    DeviceState* d = nullptr;
-    const int st = device_state(&d);
-    if (st != MXFP8_OK) return st;
-    return cudaMemsetAsync(C_dev, 0, static_cast<size_t>(bytes),
-                           static_cast<cudaStream_t>(stream)) == cudaSuccess ? MXFP8_OK
-                                                                             : MXFP8_ERR_CUDA;
+  // Empty cases read no operand, so A, B and their scales may then be empty (NULL), and the
+  // offsets are not read: an empty output (N = 0, K = 0 for wgrad, no tokens for fprop and
+  // dgrad) is a no-op; a reduction over nothing (no tokens for wgrad, K = 0 for fprop and
+  // dgrad) zero-fills C.
+  const bool wgrad = op == MXFP8_OP_WGRAD;
+  if (N == 0 || (wgrad ? K == 0 : total_rows == 0)) return MXFP8_OK;
+  if (wgrad && total_rows == 0) {
+    int64_t elems = 0;
+    if (!mul3(N, K, num_experts, &elems)) return MXFP8_ERR_INVALID_ARG;
+    return zero_fill_output(C_dev, elems, out_dtype, stream);
   }
+  if (!wgrad && K == 0) return zero_fill_output(C_dev, total_rows * N, out_dtype, stream);
   int st = gemm_checks(A_dev, sA_dev, B_dev, sB_dev, C_dev, op, out_dtype);
   if (st != MXFP8_OK) return st;
   DeviceState* d = nullptr;

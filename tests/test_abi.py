@@ -82,7 +82,14 @@ def test_argument_errors_need_no_device(lib):
     g = lib.mxfp8_gemm
     assert g(p, p, p, p, p, 128, 128, 48, 0, 0, None) == m.ERR_ALIGNMENT
     assert g(p, p, p, p, p, 120, 128, 64, 0, 0, None) == m.ERR_ALIGNMENT
-    assert g(p, p, p, p, p, 0, 128, 64, 0, 0, None) == m.ERR_INVALID_ARG
+    assert g(p, p, p, p, p, -16, 128, 64, 0, 0, None) == m.ERR_INVALID_ARG
+    # empty sizes: M or N = 0 is a no-op that reads and writes nothing (NULL operands are
+    # fine); K = 0 zero-fills C on the device, so it needs a valid C
+    assert g(None, None, None, None, None, 0, 128, 64, 0, 0, None) == m.OK
+    assert g(None, None, None, None, None, 128, 0, 64, 0, 1, None) == m.OK
+    assert g(None, None, None, None, None, 128, 128, 0, 0, 0, None) == m.ERR_INVALID_ARG
+    assert g(None, None, None, None, bad, 128, 128, 0, 0, 0, None) == m.ERR_ALIGNMENT
+    assert g(None, None, None, None, None, 0, 128, 64, 3, 0, None) == m.ERR_INVALID_ARG
     assert g(p, p, p, p, p, 128, 128, 64, 3, 0, None) == m.ERR_INVALID_ARG
     assert g(p, p, p, p, p, 128, 128, 64, 0, 2, None) == m.ERR_INVALID_ARG
     assert g(p, p, bad, p, p, 128, 128, 64, 0, 0, None) == m.ERR_ALIGNMENT
@@ -100,6 +107,10 @@ def test_argument_errors_need_no_device(lib):
         m.ERR_INVALID_ARG
     assert gg(None, None, None, None, bad, p, 4, 0, 128, 64, m.WGRAD, 0, None) == m.ERR_ALIGNMENT
     assert gg(None, None, None, None, None, p, 4, 0, 128, 64, 3, 0, None) == m.ERR_INVALID_ARG
+    assert gg(None, None, None, None, None, p, 4, 64, 0, 64, m.FPROP, 0, None) == m.OK    # N = 0
+    assert gg(None, None, None, None, None, p, 4, 64, 128, 0, m.WGRAD, 0, None) == m.OK   # K = 0
+    assert gg(None, None, None, None, None, p, 4, 64, 128, 0, m.FPROP, 0, None) == \
+        m.ERR_INVALID_ARG                                   # K = 0: zero-fills C, which is NULL
     assert lib.mxfp8_quantize_rule(p, 64, 64, m.ROW, p, p, m.SWIZZLED, 7, None) == m.ERR_INVALID_ARG
     assert lib.mxfp8_quantize_rule(p, 64, 48, m.ROW, p, p, m.SWIZZLED, 1, None) == m.ERR_ALIGNMENT
     qg = lib.mxfp8_quantize_grouped
@@ -183,7 +194,7 @@ def test_gemm_workspace_argument_errors_need_no_device(lib):
     gw = lib.mxfp8_gemm_ws
     # the plain GEMM's checks, then the workspace's alignment, all before the device
     assert gw(p, p, p, p, p, 128, 128, 48, 0, 0, p, 1 << 20, None) == m.ERR_ALIGNMENT
-    assert gw(p, p, p, p, p, 0, 128, 64, 0, 0, p, 1 << 20, None) == m.ERR_INVALID_ARG
+    assert gw(p, p, p, p, p, -16, 128, 64, 0, 0, p, 1 << 20, None) == m.ERR_INVALID_ARG
     assert gw(p, None, p, p, p, 128, 128, 64, 0, 0, p, 1 << 20, None) == m.ERR_INVALID_ARG
     assert gw(p, p, p, p, p, 128, 128, 64, 0, 0, bad, 1 << 20, None) == m.ERR_ALIGNMENT
     assert gw(p, p, p, p, p, 128, 128, 64, 0, 0, bad16, 1 << 20, None) == m.ERR_ALIGNMENT

@@ -299,6 +299,29 @@ def test_grouped_no_tokens(m):
     assert m.device_status() == m.OK
 
 
+def test_empty_sizes(m):
+    """Empty GEMMs through the binding, with empty (NULL) operand tensors.
+    - M = 0 or N = 0: an empty output, nothing written.
+    - K = 0: the empty sum. C is zero-filled over whatever it held, for the dense GEMM and for
+      grouped fprop; grouped wgrad with K = 0 has an empty output."""
+    e8 = lambda *shape: torch.empty(shape, dtype=torch.uint8, device=DEV)
+    for out_dtype, dt in ((m.OUT_BF16, torch.bfloat16), (m.OUT_FP32, torch.float32)):
+        assert m.gemm(e8(0, 64), e8(0), e8(128, 64), e8(m.scale_bytes(128, 64)), m.FPROP,
+                      out_dtype).shape == (0, 128)
+        assert m.gemm(e8(128, 64), e8(m.scale_bytes(128, 64)), e8(0, 64), e8(0), m.FPROP,
+                      out_dtype).shape == (128, 0)
+        c = torch.full((256, 384), 7.0, dtype=dt, device=DEV)
+        m.gemm(e8(256, 0), e8(0), e8(384, 0), e8(0), m.FPROP, out_dtype, out=c)
+        assert torch.all(c == 0)
+        offs = torch.tensor([0, 64, 64, 160], dtype=torch.int32, device=DEV)
+        y = torch.full((160, 384), 7.0, dtype=dt, device=DEV)
+        m.grouped_gemm(e8(160, 0), e8(0), e8(3, 384, 0), e8(0), offs, m.FPROP, out_dtype, out=y)
+        assert torch.all(y == 0)
+        dw = m.grouped_gemm(e8(384, 160), e8(16), e8(0, 160), e8(0), offs, m.WGRAD, out_dtype)
+        assert dw.shape == (3, 384, 0)
+    assert m.device_status() == m.OK
+
+
 def test_grouped_bad_offsets_latched(m):
     qa = torch.zeros((128, 64), dtype=torch.uint8, device=DEV)
     sa = torch.zeros(m.grouped_scale_bytes(128, 64, 2, m.ROW), dtype=torch.uint8, device=DEV)
