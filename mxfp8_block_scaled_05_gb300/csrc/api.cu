@@ -506,8 +506,10 @@ int mxfp8_get_device_status(void* stream) {
   if (st != MXFP8_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const unsigned slot = g_status_slot.fetch_add(1, std::memory_order_relaxed) % kStatusSlots;
-  take_status_kernel<<<1, 1, 0, s>>>(slot);  // after the stream's earlier work
-  if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_CUDA;
+  void* args[] = {const_cast<unsigned*>(&slot)};  // enqueued after the stream's earlier work
+  if (cudaLaunchKernel(reinterpret_cast<const void*>(take_status_kernel), dim3(1), dim3(1), args,
+                       0, s) != cudaSuccess)
+    return MXFP8_ERR_CUDA;
   int v = 0;
   if (cudaMemcpyFromSymbolAsync(&v, g_status_taken, sizeof(int), slot * sizeof(int),
                                 cudaMemcpyDeviceToHost, s) != cudaSuccess)
