@@ -175,13 +175,27 @@ int launch_selfcheck(const SelfcheckArgs& a, cudaStream_t stream) {
   const int st = launch_gemm(g, stream);
   if (st != MXFP8_OK) return st;
   if (cudaMemsetAsync(acc, 0, 2 * sizeof(double), stream) != cudaSuccess) return MXFP8_ERR_CUDA;
-  dim3 grid(static_cast<unsigned>((a.N + kRN - 1) / kRN), static_cast<unsigned>((a.T + kRT - 1) / kRT));
-  selfcheck_ref_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(a.x),
-                                                  static_cast<const uint8_t*>(a.ref_codes),
-                                                  static_cast<const uint8_t*>(a.ref_scales), y,
-                                                  a.T, a.N, a.K, acc);
-  selfcheck_finish_kernel<<<1, 1, 0, stream>>>(acc, a.rel_err);
-  return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
+  // launched with cudaLaunchKernelEx, whose return value is this launch's own status (an
+  // error left pending by an unrelated earlier call is not reported as this one's)
+  const dim3 grid(static_cast<unsigned>((a.N + kRN - 1) / kRN),
+                  static_cast<unsigned>((a.T + kRT - 1) / kRT));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  if (cudaLaunchKernelEx(&cfg, selfcheck_ref_kernel, static_cast<const uint16_t*>(a.x),
+                         static_cast<const uint8_t*>(a.ref_codes),
+                         static_cast<const uint8_t*>(a.ref_scales), static_cast<const float*>(y),
+                         a.T, a.N, a.K, acc) != cudaSuccess)
+    return MXFP8_ERR_CUDA;
+  cudaLaunchConfig_t one = {};
+  one.gridDim = dim3(1, 1, 1);
+  one.blockDim = dim3(1, 1, 1);
+  one.stream = stream;
+  return cudaLaunchKernelEx(&one, selfcheck_finish_kernel, static_cast<const double*>(acc),
+                            a.rel_err) == cudaSuccess
+             ? MXFP8_OK
+             : MXFP8_ERR_CUDA;
 }
 
 }  // namespace mxfp8
