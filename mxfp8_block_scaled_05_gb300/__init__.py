@@ -95,12 +95,26 @@ def _ptr(t: torch.Tensor):
 
 
 def _require(t: torch.Tensor, dtype, name: str):
+    """A tensor handed to the library: CUDA, of this dtype, contiguous, and on the current
+    device (the library runs every call on the current device)."""
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}; the current device is "
+                         f"cuda:{torch.cuda.current_device()}")
+
+
+def _buffer(t: torch.Tensor, dtype, numel: int, name: str):
+    """A buffer the library reads or writes through a raw pointer: as _require, and at least
+    `numel` elements long, so that no kernel touches memory past its end."""
+    _require(t, dtype, name)
+    if t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements; {numel} are needed")
+    return t
 
 
 # ------------------------------------------------------------------------- quantizer
@@ -126,7 +140,10 @@ def quantize(src: torch.Tensor, axis: int = ROW, layout: int = SWIZZLED, out=Non
     oshape = (rows, cols) if axis == ROW else (cols, rows)
     if out is None:
         out = torch.empty(oshape, dtype=torch.uint8, device=src.device)
-    if scales is None:
+    _buffer(out, torch.uint8, rows * cols, "out")
+    if scales is not None:
+        _buffer(scales, torch.uint8, scale_bytes(rows, cols, axis, layout), "scales")
+    else:
         nb = scale_bytes(rows, cols, axis, layout)
         if layout == LINEAR:
             s_rows, s_cols = (rows, cols // 32) if axis == ROW else (cols, rows // 32)
@@ -149,6 +166,14 @@ def _alloc_scales(rows, cols, axis, layout, dev):
     return torch.empty(scale_bytes(rows, cols, axis, layout), dtype=torch.uint8, device=dev)
 
 
+def _dual_buffers(rows, cols, layout, row_out, row_scales, col_out, col_scales):
+    _buffer(row_out, torch.uint8, rows * cols, "row_out")
+    _buffer(col_out, torch.uint8, rows * cols, "col_out")
+    if rows and cols:
+        _buffer(row_scales, torch.uint8, scale_bytes(rows, cols, ROW, layout), "row_scales")
+        _buffer(col_scales, torch.uint8, scale_bytes(rows, cols, COL, layout), "col_scales")
+
+
 def quantize_dual(src: torch.Tensor, layout: int = SWIZZLED, row_out=None, row_scales=None,
                   col_out=None, col_scales=None, stream=None):
     """Row-wise and column-wise copies of a BF16 [rows, cols] tensor from one read.
@@ -162,6 +187,7 @@ def quantize_dual(src: torch.Tensor, layout: int = SWIZZLED, row_out=None, row_s
         row_scales = _alloc_scales(rows, cols, ROW, layout, dev)
     if col_scales is None:
         col_scales = _alloc_scales(rows, cols, COL, layout, dev)
+    _dual_buffers(rows, cols, layout, row_out, row_scales, col_out, col_scales)
     _check(lib().mxfp8_quantize_dual(_ptr(src), rows, cols, _ptr(row_out), _ptr(row_scales),
                                      _ptr(col_out), _ptr(col_scales), layout, _stream(stream)),
            "mxfp8_quantize_dual")
@@ -182,6 +208,8 @@ def quantize_blockwise(src: torch.Tensor, scale_type: int = BW_FP32, out=None, s
     if scale_inv is None:
         scale_inv = torch.empty(((rows + 127) // 128, (cols + 127) // 128), dtype=torch.float32,
                                 device=dev)
+    _buffer(out, torch.uint8, rows * cols, "out")
+    _buffer(scale_inv, torch.float32, ((rows + 127) // 128) * ((cols + 127) // 128), "scale_inv")
     _check(lib().mxfp8_quantize_blockwise(_ptr(src), rows, cols, _ptr(out), _ptr(scale_inv),
                                           scale_type, _stream(stream)),
            "mxfp8_quantize_blockwise")
@@ -211,6 +239,7 @@ def quantize_dual_multi(srcs, layout: int = SWIZZLED, outs=None, stream=None):
         dev = src.device
         if outs is not None:
             ro, rs, co, cs = outs[i]
+            _dual_buffers(rows, cols, layout, ro, rs, co, cs)
         else:
             ro = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
             co = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
@@ -241,6 +270,10 @@ def quantize_grouped_dual(src: torch.Tensor, offsets: torch.Tensor, row_out=None
     if col_scales is None:
         col_scales = torch.empty(grouped_scale_bytes(total, cols, e, COL), dtype=torch.uint8,
                                  device=dev)
+    _buffer(row_out, torch.uint8, total * cols, "row_out")
+    _buffer(col_out, torch.uint8, total * cols, "col_out")
+    _buffer(row_scales, torch.uint8, grouped_scale_bytes(total, cols, e, ROW), "row_scales")
+    _buffer(col_scales, torch.uint8, grouped_scale_bytes(total, cols, e, COL), "col_scales")
     _check(lib().mxfp8_quantize_grouped_dual(_ptr(src), total, cols, _ptr(offsets), e,
                                              _ptr(row_out), _ptr(row_scales), _ptr(col_out),
                                              _ptr(col_scales), _stream(stream)),
@@ -260,6 +293,9 @@ def quantize_batched(src: torch.Tensor, axis: int = ROW, layout: int = SWIZZLED,
     if scales is None:
         scales = torch.empty(batch * scale_bytes(rows, cols, axis, layout), dtype=torch.uint8,
                              device=src.device)
+    _buffer(out, torch.uint8, batch * rows * cols, "out")
+    if rows and cols:
+        _buffer(scales, torch.uint8, batch * scale_bytes(rows, cols, axis, layout), "scales")
     _check(lib().mxfp8_quantize_batched(_ptr(src), batch, rows, cols, axis, _ptr(out),
                                         _ptr(scales), layout, _stream(stream)),
            "mxfp8_quantize_batched")
@@ -280,6 +316,8 @@ def quantize_grouped(src: torch.Tensor, offsets: torch.Tensor, axis: int = ROW, 
     if scales is None:
         scales = torch.empty(grouped_scale_bytes(total, cols, e, axis), dtype=torch.uint8,
                              device=src.device)
+    _buffer(out, torch.uint8, total * cols, "out")
+    _buffer(scales, torch.uint8, grouped_scale_bytes(total, cols, e, axis), "scales")
     _check(lib().mxfp8_quantize_grouped(_ptr(src), total, cols, axis, _ptr(offsets), e,
                                         _ptr(out), _ptr(scales), _stream(stream)),
            "mxfp8_quantize_grouped")
@@ -299,9 +337,13 @@ def gemm(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.Tensor, o
     n, k2 = b.shape
     if k != k2:
         raise ValueError(f"K mismatch: {k} vs {k2}")
+    dt = torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32
     if out is None:
-        dt = torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32
         out = torch.empty((m, n), dtype=dt, device=a.device)
+    _buffer(out, dt, m * n, "out")
+    if m and n and k:  # the scales are read only when there is a reduction to run
+        _buffer(sa, torch.uint8, scale_bytes(m, k, ROW, SWIZZLED), "sA")
+        _buffer(sb, torch.uint8, scale_bytes(n, k, ROW, SWIZZLED), "sB")
     if workspace is None:
         _check(lib().mxfp8_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out), m, n, k, op,
                                 out_dtype, _stream(stream)), "mxfp8_gemm")
@@ -338,6 +380,15 @@ def grouped_gemm(a, sa, b, sb, offsets: torch.Tensor, op: int = FPROP,
         shape = (total, n_)
     if out is None:
         out = torch.empty(shape, dtype=dt, device=a.device)
+    _buffer(out, dt, shape[0] * shape[1] * (shape[2] if len(shape) == 3 else 1), "out")
+    if total and n_ and k_:  # the scales are read only when there is a reduction to run
+        if op == WGRAD:
+            _buffer(sa, torch.uint8, grouped_scale_bytes(total, n_, e, COL), "sA")
+            _buffer(sb, torch.uint8, grouped_scale_bytes(total, k_, e, COL), "sB")
+        else:
+            _buffer(sa, torch.uint8, grouped_scale_bytes(total, k_, e, ROW), "sA")
+            _buffer(b, torch.uint8, e * n_ * k_, "B")
+            _buffer(sb, torch.uint8, e * scale_bytes(n_, k_, ROW, SWIZZLED), "sB")
     _check(lib().mxfp8_grouped_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(out),
                                     _ptr(offsets), e, total, n_, k_, op, out_dtype,
                                     _stream(stream)), "mxfp8_grouped_gemm")

@@ -322,6 +322,42 @@ def test_empty_sizes(m):
     assert m.device_status() == m.OK
 
 
+def test_binding_refuses_short_buffers(m):
+    """The C ABI takes raw pointers and cannot see buffer sizes, so the binding checks every
+    caller-provided buffer against the size the call will read or write. A short one raises
+    ValueError before anything is enqueued; the status word stays clear."""
+    u8 = lambda n: torch.zeros(n, dtype=torch.uint8, device=DEV)
+    x = torch.zeros((256, 512), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(ValueError):
+        m.quantize(x, m.ROW, out=u8(256 * 512 - 1))
+    with pytest.raises(ValueError):
+        m.quantize(x, m.COL, scales=u8(m.scale_bytes(256, 512, m.COL) - 1))
+    with pytest.raises(ValueError):
+        m.quantize_dual(x, col_scales=u8(16))
+    with pytest.raises(ValueError):
+        m.quantize_dual_multi([x], outs=[(u8(256 * 512), u8(8), u8(256 * 512), u8(8))])
+    qa, sa = m.quantize(x, m.ROW)
+    with pytest.raises(ValueError):
+        m.gemm(qa, sa, qa, sa, out=torch.empty((256, 255), dtype=torch.bfloat16, device=DEV))
+    with pytest.raises(ValueError):
+        m.gemm(qa, sa, qa, sa, out_dtype=m.OUT_FP32,
+               out=torch.empty((256, 256), dtype=torch.bfloat16, device=DEV))   # wrong dtype
+    with pytest.raises(ValueError):
+        m.gemm(qa, sa[:-1], qa, sa)
+    with pytest.raises(ValueError):
+        m.gemm(qa, sa, qa, sa, out=torch.empty((512, 256), dtype=torch.bfloat16,
+                                               device=DEV)[:, :128].t())        # not contiguous
+    offs = torch.tensor([0, 128, 256], dtype=torch.int32, device=DEV)
+    qg, sg = m.quantize_grouped(x, offs, m.ROW)
+    qw, sw = m.quantize_batched(torch.zeros((2, 384, 512), dtype=torch.bfloat16, device=DEV))
+    with pytest.raises(ValueError):
+        m.grouped_gemm(qg, sg, qw, sw, offs, out=torch.empty((256, 383), dtype=torch.bfloat16,
+                                                               device=DEV))
+    with pytest.raises(ValueError):
+        m.grouped_gemm(qg, sg, qw, sw[: sw.numel() // 2], offs)
+    assert m.device_status() == m.OK
+
+
 def test_grouped_bad_offsets_latched(m):
     qa = torch.zeros((128, 64), dtype=torch.uint8, device=DEV)
     sa = torch.zeros(m.grouped_scale_bytes(128, 64, 2, m.ROW), dtype=torch.uint8, device=DEV)
