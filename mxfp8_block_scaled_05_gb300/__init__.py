@@ -415,6 +415,12 @@ def selfcheck(w_codes: torch.Tensor, w_scales: torch.Tensor, ref_codes: torch.Te
         raise ValueError(f"no self-check for tokens={t} N={n} K={k}")
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _buffer(w_scales, torch.uint8, scale_bytes(n, k, ROW, SWIZZLED), "w_scales")
+    _buffer(ref_codes, torch.uint8, n * k, "ref_codes")
+    _buffer(ref_scales, torch.uint8, n * (k // 32), "ref_scales")
+    _buffer(workspace, torch.uint8, need, "workspace")
+    if x.shape[1] != k:
+        raise ValueError(f"x has {x.shape[1]} columns; the weight has K = {k}")
     out = torch.empty(1, dtype=torch.float32, device=x.device)
     _check(lib().mxfp8_selfcheck(_ptr(w_codes), _ptr(w_scales), _ptr(ref_codes),
                                  _ptr(ref_scales), n, k, _ptr(x), t, _ptr(workspace),
